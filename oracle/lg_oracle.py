@@ -1,0 +1,366 @@
+"""fp64 CPU oracle for window + dilation + global sparse self-attention (forward).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check in
+``__graft_entry__.smoke`` and the CPU-baseline leg of ``bench.py`` may import
+this module.  The library's product path never calls it, and this module
+shares no code with the CUDA path: it materialises the attention mask from
+the method's definition and runs a plain masked softmax in float64.
+
+Sources (each function names the passage it follows):
+
+* "Longformer: The Long-Document Transformer" (arXiv 2004.05150), commentary
+  page, section 3.4 "Detailed, sentence-based technical breakdown":
+  - "Sliding Window Attention": a token attends to w/2 tokens on its left,
+    w/2 on its right and itself (w + 1 keys).
+  - "Dilated Sliding Window Attention": with dilation d the keys are
+    i - d*w/2, ..., i - d, i, i + d, ..., i + d*w/2 (same key count, span x d).
+  - "Global Attention": a global token attends to every token and every token
+    attends to it; its row and column of the attention matrix are full.
+  - "Separate Linear Projections for Local vs. Global Attention": positions
+    outside the window get -inf before the softmax.
+  - "Autoregressive Language Modeling Configuration": causal mode keeps only
+    the left half of the window (the upper triangle of the band is masked).
+* "ETC: Encoding Long and Structured Inputs in Transformers" (arXiv
+  2004.08483), commentary page, section 3.4, "Global-Local Attention: The Core
+  Sparse Mechanism": g2g, g2l and l2g are full; l2l is the band |i - j| <= r
+  clamped to valid indices; g2g+g2l share one softmax and l2g+l2l share another
+  ("Softmax unification").
+* "LONGNET: Scaling Transformers to 1,000,000,000 Tokens" (arXiv 2307.02486),
+  commentary page, section 3.4, "Standard Self-Attention and Sparse Attention"
+  (a binary mask S sends disallowed logits to -inf) and "Mixture of Dilated
+  Attentions" (outputs computed over parts of the key set, weighted by their
+  softmax denominators, equal one joint softmax over the union of the keys).
+
+Readings taken where the pages are silent or ambiguous (window counted in
+steps of the dilation; stride-style dilation; keys outside [0, N) dropped; a
+global key inside the band counted once; causal limits only the band; natural
+log LSE of the scaled logits) are stated on each function.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against
+hand-derived key sets from the passages above, closed forms, a library
+softmax-attention routine, and invariants of the definition.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# Mask predicates
+# --------------------------------------------------------------------------
+
+def band_mask(N: int, w_left: int, w_right: int, dilation: int, causal: bool) -> np.ndarray:
+    """Boolean [N, N] matrix: key j lies in the (dilated, optionally causal) window of query i.
+
+    Longformer page, "Sliding Window Attention" and "Dilated Sliding Window
+    Attention": query i sees the keys i + d*t for integer steps t running from
+    -w_left to +w_right (w_left = w_right = w/2 in the page's notation), so the
+    key count stays w_left + w_right + 1 while the span grows by d.  Reading:
+    w_left / w_right count steps, not positions; d is a stride (d = 1 is the
+    contiguous window).  Keys outside [0, N) are dropped (ETC page: "clamped
+    to valid indices").  Causal ("Autoregressive Language Modeling
+    Configuration"): only the left half of the window remains, i.e. t <= 0.
+    """
+    if dilation < 1:
+        raise ValueError("dilation must be >= 1")
+    i = np.arange(N, dtype=np.int64)[:, None]
+    j = np.arange(N, dtype=np.int64)[None, :]
+    diff = j - i
+    right = 0 if causal else w_right
+    on_stride = (diff % dilation) == 0
+    steps = diff // dilation  # exact wherever on_stride holds
+    return on_stride & (steps >= -w_left) & (steps <= right)
+
+
+def global_flags(N: int, global_idx) -> np.ndarray:
+    """Boolean [N]: position p is a global token."""
+    flags = np.zeros(N, dtype=bool)
+    g = np.asarray(global_idx, dtype=np.int64).reshape(-1)
+    if g.size:
+        if g.min() < 0 or g.max() >= N:
+            raise ValueError("global index out of range")
+        flags[g] = True
+    return flags
+
+
+def allowed_mask(N: int, w_left: int, w_right: int, dilation: int, causal: bool, global_idx) -> np.ndarray:
+    """Boolean [N, N] attention mask of one head.
+
+    Longformer page, "Global Attention": a global token's row and column of the
+    attention matrix are both full.  The mask is the boolean union of the band
+    and those rows/columns, so a global key that also falls in the band counts
+    once.  Reading: causal restricts only the band; global rows and columns
+    stay full.
+    """
+    mask = band_mask(N, w_left, w_right, dilation, causal)
+    g = global_flags(N, global_idx)
+    mask |= g[:, None]
+    mask |= g[None, :]
+    return mask
+
+
+def allowed_row(i: int, N: int, w_left: int, w_right: int, dilation: int, causal: bool, gflags: np.ndarray) -> np.ndarray:
+    """Boolean [N]: row i of ``allowed_mask`` evaluated from the same predicate.
+
+    Used for sampled-row checks at sizes where the N x N mask does not fit.
+    """
+    j = np.arange(N, dtype=np.int64)
+    diff = j - i
+    right = 0 if causal else w_right
+    inband = ((diff % dilation) == 0) & (diff // dilation >= -w_left) & (diff // dilation <= right)
+    if gflags[i]:
+        return np.ones(N, dtype=bool)
+    return inband | gflags
+
+
+# --------------------------------------------------------------------------
+# Masked softmax attention (one head)
+# --------------------------------------------------------------------------
+
+def masked_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, scale: float):
+    """O, LSE and the probability matrix P of softmax(scale * q k^T masked) v, in float64.
+
+    LongNet page, "Standard Self-Attention and Sparse Attention": logits where
+    the mask is 0 are sent to -inf before the softmax, so they get weight 0.
+    LSE (a reading; no page fixes it) is the natural log of the sum of
+    exp(scale * q.k) over the allowed keys of each row.
+    q: [n_q, D]; k, v: [n_k, D]; mask: [n_q, n_k] bool.  Every row must allow
+    at least one key.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    if not mask.any(axis=1).all():
+        raise ValueError("a row allows no key")
+    logits = scale * (q @ k.T)
+    logits = np.where(mask, logits, -np.inf)
+    row_max = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - row_max)          # masked entries become exactly 0
+    denom = e.sum(axis=1, keepdims=True)
+    probs = e / denom
+    out = probs @ v
+    lse = (row_max + np.log(denom))[:, 0]
+    return out, lse, probs
+
+
+def default_scale(D: int, scale) -> float:
+    """1/sqrt(D) unless a positive scale is given (the pages' 1/sqrt(d_k))."""
+    if scale is None or scale <= 0:
+        return 1.0 / np.sqrt(D)
+    return float(scale)
+
+
+# --------------------------------------------------------------------------
+# Longformer-style call: [B, H, N, D]
+# --------------------------------------------------------------------------
+
+def attn_fwd(q, k, v, w_left, w_right, dilation, causal, global_idx, scale=None):
+    """Dense-mask oracle.  q, k, v: [B, H, N, D]; dilation: H ints.
+
+    Materialises ``allowed_mask`` for each head and applies
+    ``masked_attention``.  Returns O [B, H, N, D] and LSE [B, H, N] (float64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, D = q.shape
+    s = default_scale(D, scale)
+    out = np.empty((B, H, N, D), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    for h in range(H):
+        mask = allowed_mask(N, w_left, w_right, int(dilation[h]), bool(causal), global_idx)
+        for b in range(B):
+            out[b, h], lse[b, h], _ = masked_attention(q[b, h], k[b, h], v[b, h], mask, s)
+    return out, lse
+
+
+def attn_fwd_rows(q, k, v, w_left, w_right, dilation, causal, global_idx, rows, scale=None):
+    """Sampled-row oracle.  Same definition as ``attn_fwd`` for the listed rows only.
+
+    For each (b, h) and each row i in ``rows`` the mask row is evaluated with
+    ``allowed_row`` over all N keys; the allowed keys are then softmaxed.
+    Returns O [B, H, len(rows), D] and LSE [B, H, len(rows)].
+    """
+    B, H, N, D = q.shape
+    s = default_scale(D, scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    gflags = global_flags(N, global_idx)
+    out = np.empty((B, H, rows.size, D), dtype=np.float64)
+    lse = np.empty((B, H, rows.size), dtype=np.float64)
+    for h in range(H):
+        d = int(dilation[h])
+        for r, i in enumerate(rows):
+            keys = np.nonzero(allowed_row(int(i), N, w_left, w_right, d, bool(causal), gflags))[0]
+            for b in range(B):
+                qi = np.asarray(q[b, h, i], dtype=np.float64)[None, :]
+                kk = np.asarray(k[b, h, keys], dtype=np.float64)
+                vv = np.asarray(v[b, h, keys], dtype=np.float64)
+                o, l, _ = masked_attention(qi, kk, vv, np.ones((1, keys.size), dtype=bool), s)
+                out[b, h, r] = o[0]
+                lse[b, h, r] = l[0]
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# ETC global-local call
+# --------------------------------------------------------------------------
+
+def etc_mask(L: int, G: int, radius: int) -> np.ndarray:
+    """Boolean [(G+L), (G+L)] mask over the concatenation (global tokens first, then long).
+
+    ETC page, "Global-Local Attention": the g2g, g2l and l2g blocks are full;
+    the l2l block allows |i - j| <= r, clamped to valid indices.  The
+    per-instance masks M are all ones (no structure given), and no relative
+    position term is added.
+    """
+    n = G + L
+    mask = np.zeros((n, n), dtype=bool)
+    mask[:G, :] = True          # g2g and g2l
+    mask[G:, :G] = True         # l2g
+    i = np.arange(L)[:, None]
+    j = np.arange(L)[None, :]
+    mask[G:, G:] = np.abs(i - j) <= radius   # l2l
+    return mask
+
+
+def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius, scale=None):
+    """ETC oracle.  Long tensors [B, H, L, D], global tensors [B, H, G, D].
+
+    "Softmax unification": a global query takes one softmax over the
+    concatenation of its g2g and g2l logits; a long query takes one softmax
+    over its l2g and l2l logits.  Implemented as one masked softmax over the
+    concatenated token list [global; long] with ``etc_mask``.
+    Returns (out_l, out_g, lse_l, lse_g), float64.
+    """
+    q_l = np.asarray(q_l, dtype=np.float64)
+    B, H, L, D = q_l.shape
+    G = np.asarray(q_g).shape[2]
+    s = default_scale(D, scale)
+    mask = etc_mask(L, G, radius)
+    out_l = np.empty((B, H, L, D)); out_g = np.empty((B, H, G, D))
+    lse_l = np.empty((B, H, L)); lse_g = np.empty((B, H, G))
+    for b in range(B):
+        for h in range(H):
+            qq = np.concatenate([np.asarray(q_g[b, h], np.float64), q_l[b, h]], axis=0)
+            kk = np.concatenate([np.asarray(k_g[b, h], np.float64), np.asarray(k_l[b, h], np.float64)], axis=0)
+            vv = np.concatenate([np.asarray(v_g[b, h], np.float64), np.asarray(v_l[b, h], np.float64)], axis=0)
+            o, l, _ = masked_attention(qq, kk, vv, mask, s)
+            out_g[b, h], out_l[b, h] = o[:G], o[G:]
+            lse_g[b, h], lse_l[b, h] = l[:G], l[G:]
+    return out_l, out_g, lse_l, lse_g
+
+
+def etc_attn_fwd_rows(q_l, k_l, v_l, q_g, k_g, v_g, radius, long_rows, scale=None):
+    """Sampled long rows of ``etc_attn_fwd`` (l2g + l2l in one softmax); global rows are all computed.
+
+    Returns (out_l_rows [B, H, R, D], out_g [B, H, G, D], lse_l_rows, lse_g).
+    """
+    B, H, L, D = q_l.shape
+    G = q_g.shape[2]
+    s = default_scale(D, scale)
+    long_rows = np.asarray(long_rows, dtype=np.int64)
+    out_l = np.empty((B, H, long_rows.size, D)); lse_l = np.empty((B, H, long_rows.size))
+    out_g = np.empty((B, H, G, D)); lse_g = np.empty((B, H, G))
+    for b in range(B):
+        for h in range(H):
+            kk = np.concatenate([np.asarray(k_g[b, h], np.float64), np.asarray(k_l[b, h], np.float64)], axis=0)
+            vv = np.concatenate([np.asarray(v_g[b, h], np.float64), np.asarray(v_l[b, h], np.float64)], axis=0)
+            o, l, _ = masked_attention(np.asarray(q_g[b, h], np.float64), kk, vv, np.ones((G, G + L), bool), s)
+            out_g[b, h], lse_g[b, h] = o, l
+            j = np.arange(L)
+            for r, i in enumerate(long_rows):
+                row_mask = np.concatenate([np.ones(G, bool), np.abs(j - i) <= radius])
+                o, l, _ = masked_attention(np.asarray(q_l[b, h, i], np.float64)[None, :], kk, vv, row_mask[None, :], s)
+                out_l[b, h, r], lse_l[b, h, r] = o[0], l[0]
+    return out_l, out_g, lse_l, lse_g
+
+
+# --------------------------------------------------------------------------
+# Pair counts (the useful-work measure: allowed query-key pairs)
+# --------------------------------------------------------------------------
+
+def count_pairs_bruteforce(N, w_left, w_right, dilation, causal, global_idx) -> int:
+    """Number of allowed (i, j) pairs of one head, by summing the materialised mask."""
+    return int(allowed_mask(N, w_left, w_right, dilation, causal, global_idx).sum())
+
+
+def _band_row_count(i, N, w_left, right, d):
+    """#{t in [-w_left, right] : 0 <= i + d*t < N}."""
+    lo = max(-w_left, -(i // d))            # smallest t with i + d*t >= 0
+    hi = min(right, (N - 1 - i) // d)       # largest t with i + d*t <= N-1
+    return max(0, hi - lo + 1)
+
+
+def _band_col_count(j, N, w_left, right, d):
+    """#{t in [-w_left, right] : 0 <= j - d*t < N} (queries whose band holds key j)."""
+    hi = min(right, j // d)                          # j - d*t >= 0
+    lo = max(-w_left, -((N - 1 - j) // d))           # j - d*t <= N-1
+    return max(0, hi - lo + 1)
+
+
+def count_pairs_closed(N, w_left, w_right, dilation, causal, global_idx) -> int:
+    """Closed-form allowed-pair count of one head.
+
+    Band: sum over steps t of the number of rows whose key i + d*t stays in
+    [0, N): sum_{t=-wl}^{wr'} max(0, N - d*|t|).  Globals add the union of g
+    full rows and g full columns, 2gN - g^2 pairs, minus those already in the
+    band (inclusion-exclusion over band rows and columns of the global set).
+    """
+    d = int(dilation)
+    right = 0 if causal else w_right
+    band = sum(max(0, N - d * abs(t)) for t in range(-w_left, right + 1))
+    g = sorted(set(int(x) for x in np.asarray(global_idx).reshape(-1)))
+    if not g:
+        return band
+    n_g = len(g)
+    rows_cols = 2 * n_g * N - n_g * n_g
+    in_band_rows = sum(_band_row_count(i, N, w_left, right, d) for i in g)
+    in_band_cols = sum(_band_col_count(j, N, w_left, right, d) for j in g)
+    garr = np.asarray(g, dtype=np.int64)
+    diff = garr[None, :] - garr[:, None]
+    both = int((((diff % d) == 0) & (diff // d >= -w_left) & (diff // d <= right)).sum())
+    overlap = in_band_rows + in_band_cols - both
+    return band + rows_cols - overlap
+
+
+def etc_count_pairs(L, G, radius) -> int:
+    """Allowed pairs of one ETC head: l2l band + l2g (L*G) + g2g and g2l (G*(G+L)).
+
+    ETC page, "Global-Local Attention", complexity O(n_g(n_g + n_l) + n_l(n_g + 2r + 1)).
+    """
+    ll = sum(max(0, L - abs(t)) for t in range(-radius, radius + 1))
+    return ll + L * G + G * (G + L)
+
+
+# --------------------------------------------------------------------------
+# Partial softmax statistics and their merge
+# --------------------------------------------------------------------------
+
+def partial_stats(q, k, v, mask, scale):
+    """Softmax statistics of one key subset: row max m, sum l of exp(x - m), unnormalised acc.
+
+    A row with no allowed key in the subset gets m = -inf, l = 0, acc = 0.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    logits = np.where(mask, scale * (q @ k.T), -np.inf)
+    m = logits.max(axis=1)
+    safe = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(logits - safe[:, None])
+    return m, e.sum(axis=1), e @ v
+
+
+def merge_partials(ms, ls, accs):
+    """Joint softmax from per-subset statistics.
+
+    LongNet page, "Mixture of Dilated Attentions": outputs over parts of the
+    key set, weighted by their softmax denominators, equal one softmax over the
+    union of the keys.  With m = max_p m_p: l = sum_p e^{m_p - m} l_p,
+    O = sum_p e^{m_p - m} acc_p / l, LSE = m + ln l.
+    ms, ls: [P, n]; accs: [P, n, D].
+    """
+    ms = np.asarray(ms, np.float64); ls = np.asarray(ls, np.float64); accs = np.asarray(accs, np.float64)
+    m = ms.max(axis=0)
+    w = np.where(np.isfinite(ms), np.exp(ms - m[None, :]), 0.0)
+    l = (w * ls).sum(axis=0)
+    out = (w[:, :, None] * accs).sum(axis=0) / l[:, None]
+    return out, m + np.log(l)

@@ -1,0 +1,119 @@
+"""Seeded synthetic inputs and named workload presets.
+
+This module only draws random numbers and rounds them to the input dtype.  It
+holds none of the attention arithmetic, so both the CUDA path and the
+independent CPU checker can take their inputs from it.
+
+Recipe: Q, K, V are iid N(0, 1) float32 drawn from
+``numpy.random.default_rng(seed)`` in the order q, k, v with shape
+[B, H, N, D] (for the ETC workload: q_l, k_l, v_l [B, H, L, D], then q_g, k_g,
+v_g [B, H, G, D]).  bf16 workloads are rounded to bfloat16 with
+round-to-nearest-even before either side sees them, so a comparison measures
+kernel error only.  Random global positions are distinct, drawn with
+``default_rng(seed + 1000)`` and sorted ascending.
+
+The presets mirror the pages' workloads: a Longformer-base QA shape
+(CLS + question span global), an ETC-base shape (local radius 84, a few
+hundred global tokens), a character-LM shape (causal, dilated heads) and a
+long-sequence sweep.  The pages evaluate on datasets that are not used here;
+these synthetic tensors stand in for them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str                   # "f32" or "bf16"
+    B: int
+    H: int
+    N: int                       # sequence length (ETC: long length L)
+    D: int
+    w_left: int = 0
+    w_right: int = 0
+    dilation: Sequence[int] = ()  # per head; empty means all 1
+    causal: bool = False
+    global_positions: Optional[Sequence[int]] = None   # explicit positions
+    n_random_global: int = 0     # draw this many distinct random positions
+    etc_G: int = 0               # > 0 selects the ETC call with a separate global input
+    radius: int = 0              # ETC local radius
+    seed: int = 0
+
+    @property
+    def is_etc(self) -> bool:
+        return self.etc_G > 0
+
+    def dilations(self):
+        return list(self.dilation) if self.dilation else [1] * self.H
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five reference workloads.
+PRESETS = {
+    "tiny_f32": Workload("tiny_f32 B1 H2 N512 D64 w64/64 G={0}", "f32", 1, 2, 512, 64,
+                         64, 64, (), False, (0,), seed=1),
+    "longformer_base": Workload("longformer_base bf16 B1 H12 N4096 D64 w256/256 G=0..64", "bf16",
+                                1, 12, 4096, 64, 256, 256, (), False, tuple(range(65)), seed=2),
+    "etc_base": Workload("etc_base bf16 B2 H12 L4096 G256 D64 r84", "bf16", 2, 12, 4096, 64,
+                         etc_G=256, radius=84, seed=3),
+    "charlm_dilated": Workload("charlm_dilated bf16 B1 H8 N16384 D64 causal wl512 d=[1,1,2,2,3,3,4,4]",
+                               "bf16", 1, 8, 16384, 64, 512, 0, (1, 1, 2, 2, 3, 3, 4, 4), True, (), seed=4),
+    "long_8k": Workload("long_scale bf16 B1 H16 N8192 D128 w512/512 G=128 random", "bf16",
+                        1, 16, 8192, 128, 512, 512, (), False, None, 128, seed=5),
+    "long_32k": Workload("long_scale bf16 B1 H16 N32768 D128 w512/512 G=128 random", "bf16",
+                         1, 16, 32768, 128, 512, 512, (), False, None, 128, seed=5),
+    "long_128k": Workload("long_scale bf16 B1 H16 N131072 D128 w512/512 G=128 random", "bf16",
+                          1, 16, 131072, 128, 512, 512, (), False, None, 128, seed=5),
+}
+
+
+def global_positions(w: Workload) -> np.ndarray:
+    """Sorted distinct int32 global positions of a (non-ETC) workload."""
+    if w.global_positions is not None:
+        return np.asarray(sorted(set(int(x) for x in w.global_positions)), dtype=np.int32)
+    if w.n_random_global > 0:
+        rng = np.random.default_rng(w.seed + 1000)
+        pos = rng.choice(w.N, size=w.n_random_global, replace=False)
+        return np.sort(pos).astype(np.int32)
+    return np.zeros(0, dtype=np.int32)
+
+
+def _round(x: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(x)
+    if dtype == "bf16":
+        return t.to(torch.bfloat16)
+    return t.contiguous()
+
+
+def make_inputs(w: Workload) -> dict:
+    """Host tensors of the workload in its input dtype, plus global positions.
+
+    Returns a dict with q, k, v (and q_g, k_g, v_g for ETC) as CPU torch
+    tensors of dtype float32 or bfloat16, and ``global_idx`` (int32 numpy).
+    """
+    rng = np.random.default_rng(w.seed)
+    shape = (w.B, w.H, w.N, w.D)
+    out = {}
+    for name in ("q", "k", "v"):
+        out[name] = _round(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    if w.is_etc:
+        gshape = (w.B, w.H, w.etc_G, w.D)
+        for name in ("q_g", "k_g", "v_g"):
+            out[name] = _round(rng.standard_normal(gshape, dtype=np.float32), w.dtype)
+        out["global_idx"] = np.zeros(0, dtype=np.int32)
+    else:
+        out["global_idx"] = global_positions(w)
+    return out
+
+
+def as_f64(t: torch.Tensor) -> np.ndarray:
+    """The exact values of an input tensor as float64 (bf16 and f32 upcast exactly)."""
+    return t.to(torch.float64).numpy()

@@ -1,0 +1,267 @@
+"""Pin checks for the CPU oracle.
+
+Each ``pin_*`` takes an oracle module and raises AssertionError when the
+oracle disagrees with something fixed outside it: hand-derived key sets and
+counts (tests/golden), closed forms, a library softmax-attention routine, or
+an invariant of the definition.  ``test_oracle_pins.py`` runs them on the real
+oracle; ``test_oracle_mutants.py`` runs them on copies with a planted mistake
+and expects at least one pin to fail for each.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                yield line.split()
+
+
+def _parse_list(s):
+    return [] if s == "-" else [int(x) for x in s.split(",")]
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------- golden
+
+def pin_golden_windows(O):
+    for case, N, wl, wr, d, causal, glist, row, keys in _golden_lines("window_keys.txt"):
+        N, wl, wr, d, row = int(N), int(wl), int(wr), int(d), int(row)
+        g = _parse_list(glist)
+        mask = O.allowed_mask(N, wl, wr, d, bool(int(causal)), g)
+        got = np.nonzero(mask[row])[0].tolist()
+        assert got == _parse_list(keys), (case, got, keys)
+        gflags = O.global_flags(N, g)
+        got_row = np.nonzero(O.allowed_row(row, N, wl, wr, d, bool(int(causal)), gflags))[0].tolist()
+        assert got_row == _parse_list(keys), (case, "row", got_row, keys)
+
+
+def pin_golden_etc(O):
+    for case, L, G, r, query, keys in _golden_lines("etc_keys.txt"):
+        L, G, r = int(L), int(G), int(r)
+        mask = O.etc_mask(L, G, r)
+        qi = int(query[1:]) + (0 if query[0] == "g" else G)
+        names = [f"g{j}" for j in range(G)] + [f"l{j}" for j in range(L)]
+        got = [names[j] for j in np.nonzero(mask[qi])[0]]
+        assert got == keys.split(","), (case, got, keys)
+
+
+def pin_golden_counts(O):
+    for parts in _golden_lines("pair_counts.txt"):
+        if parts[0] == "etc":
+            L, G, r, count = map(int, parts[1:])
+            assert O.etc_count_pairs(L, G, r) == count, parts
+            assert int(O.etc_mask(L, G, r).sum()) == count, parts
+            continue
+        case, N, wl, wr, d, causal, glist, count = parts
+        args = (int(N), int(wl), int(wr), int(d), bool(int(causal)), _parse_list(glist))
+        assert O.count_pairs_bruteforce(*args) == int(count), (case, "brute")
+        assert O.count_pairs_closed(*args) == int(count), (case, "closed")
+
+
+# ---------------------------------------------------------------- closed forms
+
+def pin_closed_form_counts(O, trials=120, seed=11):
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        N = int(rng.integers(1, 70))
+        wl = int(rng.integers(0, 12)); wr = int(rng.integers(0, 12))
+        d = int(rng.integers(1, 6)); causal = bool(rng.integers(0, 2))
+        ng = int(rng.integers(0, min(N, 6) + 1))
+        g = sorted(rng.choice(N, size=ng, replace=False).tolist()) if ng else []
+        a = O.count_pairs_bruteforce(N, wl, wr, d, causal, g)
+        b = O.count_pairs_closed(N, wl, wr, d, causal, g)
+        assert a == b, (N, wl, wr, d, causal, g, a, b)
+    # interior rows keep exactly w_left + w_right + 1 keys (w + 1 in the page's notation)
+    mask = O.band_mask(200, 7, 5, 3, False)
+    assert (mask[60:140].sum(axis=1) == 13).all()
+
+
+def pin_linear_in_n(O):
+    """Longformer page: cost O(n*w) + O(n*g) -> the count is affine in N once N exceeds the span."""
+    g = list(range(5))
+    c = [O.count_pairs_closed(n, 16, 16, 2, False, g) for n in (400, 800, 1200, 1600)]
+    assert c[1] - c[0] == c[2] - c[1] == c[3] - c[2]
+    per_row = (c[1] - c[0]) / 400
+    assert per_row == 33 + 2 * len(g)   # w + 1 band keys plus a global row and column per global
+
+
+# ---------------------------------------------------------------- library routine
+
+def _sdpa64(q, k, v, scale):
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v))
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale).numpy()
+
+
+def pin_full_attention(O, seed=3):
+    """A window that covers the sequence (d = 1, non-causal) is full softmax attention."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 3, 37, 16
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    for scale in (None, 0.37):
+        s = 1 / np.sqrt(D) if scale is None else scale
+        out, lse = O.attn_fwd(q, k, v, N - 1, N - 1, [1] * H, False, [], scale)
+        ref = _sdpa64(q, k, v, s)
+        assert np.abs(out - ref).max() < 1e-12
+        logits = torch.from_numpy(s * np.einsum("bhid,bhjd->bhij", q, k))
+        assert np.abs(lse - torch.logsumexp(logits, dim=-1).numpy()).max() < 1e-12
+    # ETC with a radius that covers the long input is full attention over [global; long]
+    G, L = 5, 23
+    ql, kl, vl = _rand(rng, 1, 2, L, D), _rand(rng, 1, 2, L, D), _rand(rng, 1, 2, L, D)
+    qg, kg, vg = _rand(rng, 1, 2, G, D), _rand(rng, 1, 2, G, D), _rand(rng, 1, 2, G, D)
+    ol, og, _, _ = O.etc_attn_fwd(ql, kl, vl, qg, kg, vg, L, None)
+    cat = lambda a, b: np.concatenate([a, b], axis=2)
+    ref = _sdpa64(cat(qg, ql), cat(kg, kl), cat(vg, vl), 1 / np.sqrt(D))
+    assert np.abs(og - ref[:, :, :G]).max() < 1e-12
+    assert np.abs(ol - ref[:, :, G:]).max() < 1e-12
+
+
+def pin_global_rows_are_full_rows(O, seed=4):
+    """Longformer page, "Global Attention": a global query attends to every token."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 2, 50, 8
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    g = [0, 17, 49]
+    out, lse = O.attn_fwd(q, k, v, 3, 2, [1, 3], True, g)
+    ref = _sdpa64(q, k, v, 1 / np.sqrt(D))
+    assert np.abs(out[:, :, g] - ref[:, :, g]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- invariants
+
+def pin_rows_sum_to_one(O, seed=5):
+    rng = np.random.default_rng(seed)
+    N, D = 41, 8
+    q, k, v = _rand(rng, N, D), _rand(rng, N, D), _rand(rng, N, D)
+    mask = O.allowed_mask(N, 4, 2, 3, False, [7, 40])
+    _, _, probs = O.masked_attention(q, k, v, mask, 0.5)
+    assert np.abs(probs.sum(axis=1) - 1).max() < 1e-12
+    assert (probs[~mask] == 0).all()
+    assert (probs[mask] > 0).all()
+
+
+def pin_identity_window(O, seed=6):
+    """w_left = w_right = 0 without globals: each row sees only itself -> O = V, LSE = s<q_i, k_i>."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 2, 19, 8
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    out, lse = O.attn_fwd(q, k, v, 0, 0, [1, 4], False, [])
+    assert np.abs(out - v).max() < 1e-14
+    assert np.abs(lse - np.einsum("bhnd,bhnd->bhn", q, k) / np.sqrt(D)).max() < 1e-13
+    # causal first row sees only itself
+    out, _ = O.attn_fwd(q, k, v, 5, 5, [1, 2], True, [])
+    assert np.abs(out[:, :, 0] - v[:, :, 0]).max() < 1e-14
+
+
+def pin_dilation_residues(O, seed=7):
+    """A dilated head equals an undilated window applied to each residue class {c + d*t}."""
+    rng = np.random.default_rng(seed)
+    N, D, d = 47, 8, 3
+    q, k, v = _rand(rng, 1, 1, N, D), _rand(rng, 1, 1, N, D), _rand(rng, 1, 1, N, D)
+    for causal in (False, True):
+        out, lse = O.attn_fwd(q, k, v, 2, 3, [d], causal, [])
+        for c in range(d):
+            idx = np.arange(c, N, d)
+            o2, l2 = O.attn_fwd(q[:, :, idx], k[:, :, idx], v[:, :, idx], 2, 3, [1], causal, [])
+            assert np.abs(out[:, :, idx] - o2).max() < 1e-13
+            assert np.abs(lse[:, :, idx] - l2).max() < 1e-13
+
+
+def pin_key_shift(O, seed=8):
+    """Adding u to every key leaves O unchanged and shifts LSE_i by s<q_i, u>."""
+    rng = np.random.default_rng(seed)
+    N, D = 33, 8
+    q, k, v = _rand(rng, 1, 2, N, D), _rand(rng, 1, 2, N, D), _rand(rng, 1, 2, N, D)
+    u = _rand(rng, D)
+    o1, l1 = O.attn_fwd(q, k, v, 3, 5, [1, 2], False, [4, 30])
+    o2, l2 = O.attn_fwd(q, k + u, v, 3, 5, [1, 2], False, [4, 30])
+    assert np.abs(o1 - o2).max() < 1e-12
+    assert np.abs((l2 - l1) - np.einsum("bhnd,d->bhn", q, u) / np.sqrt(D)).max() < 1e-12
+
+
+def pin_constant_values(O, seed=9):
+    rng = np.random.default_rng(seed)
+    N, D = 29, 4
+    q, k = _rand(rng, 1, 1, N, D), _rand(rng, 1, 1, N, D)
+    c = np.array([1.5, -2.0, 0.25, 3.0])
+    v = np.broadcast_to(c, (1, 1, N, D)).copy()
+    out, _ = O.attn_fwd(q, k, v, 2, 2, [2], False, [3])
+    assert np.abs(out - c).max() < 1e-13
+
+
+def pin_etc_permutation(O, seed=10):
+    """Permuting the global tokens permutes out_g and leaves out_l unchanged (no positional term)."""
+    rng = np.random.default_rng(seed)
+    L, G, D = 21, 6, 8
+    t = [_rand(rng, 1, 2, L, D) for _ in range(3)] + [_rand(rng, 1, 2, G, D) for _ in range(3)]
+    perm = rng.permutation(G)
+    a = O.etc_attn_fwd(*t, 2)
+    b = O.etc_attn_fwd(*t[:3], *(x[:, :, perm] for x in t[3:]), 2)
+    assert np.abs(a[0] - b[0]).max() < 1e-12
+    assert np.abs(a[1][:, :, perm] - b[1]).max() < 1e-12
+    assert np.abs(a[3][:, :, perm] - b[3]).max() < 1e-12
+
+
+def pin_etc_rows(O, seed=12):
+    """The sampled-row ETC oracle agrees with the dense one."""
+    rng = np.random.default_rng(seed)
+    L, G, D = 30, 4, 8
+    t = [_rand(rng, 2, 1, L, D) for _ in range(3)] + [_rand(rng, 2, 1, G, D) for _ in range(3)]
+    ol, og, ll, lg = O.etc_attn_fwd(*t, 3)
+    rows = [0, 1, 14, 28, 29]
+    rl, rg, rll, rlg = O.etc_attn_fwd_rows(*t, 3, rows)
+    assert np.abs(ol[:, :, rows] - rl).max() < 1e-12 and np.abs(og - rg).max() < 1e-12
+    assert np.abs(ll[:, :, rows] - rll).max() < 1e-12 and np.abs(lg - rlg).max() < 1e-12
+
+
+def pin_rows_vs_dense(O, seed=13):
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 3, 45, 8
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    g = [2, 44]
+    for causal in (False, True):
+        out, lse = O.attn_fwd(q, k, v, 3, 4, [1, 2, 5], causal, g)
+        rows = [0, 2, 3, 20, 43, 44]
+        ro, rl = O.attn_fwd_rows(q, k, v, 3, 4, [1, 2, 5], causal, g, rows)
+        assert np.abs(out[:, :, rows] - ro).max() < 1e-12
+        assert np.abs(lse[:, :, rows] - rl).max() < 1e-12
+
+
+def pin_merge(O, seed=14):
+    """LongNet page: weighting partial outputs by softmax denominators equals one joint softmax."""
+    rng = np.random.default_rng(seed)
+    n, nk, D = 9, 40, 8
+    q, k, v = _rand(rng, n, D), _rand(rng, nk, D), _rand(rng, nk, D)
+    mask = rng.random((n, nk)) < 0.6
+    mask[:, 0] = True
+    full_o, full_l, _ = O.masked_attention(q, k, v, mask, 0.7)
+    for parts in (1, 2, 3, 7):
+        cuts = np.sort(rng.choice(np.arange(1, nk), size=parts - 1, replace=False)) if parts > 1 else []
+        bounds = [0, *cuts, nk]
+        ms, ls, accs = [], [], []
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            sub = np.zeros_like(mask); sub[:, a:b] = mask[:, a:b]
+            m, l, acc = O.partial_stats(q, k, v, sub, 0.7)
+            ms.append(m); ls.append(l); accs.append(acc)
+        o, lse = O.merge_partials(ms, ls, accs)
+        assert np.abs(o - full_o).max() < 1e-12
+        assert np.abs(lse - full_l).max() < 1e-12
+
+
+ALL_PINS = [
+    pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
+    pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
+    pin_identity_window, pin_dilation_residues, pin_key_shift, pin_constant_values,
+    pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
+]

@@ -1,0 +1,129 @@
+"""Plant plausible mistakes in copies of the CPU oracle and check that a pin catches each.
+
+The mutants live only in this test, on the CPU.  Each replaces one function of
+a fresh copy of the oracle module with a subtly wrong version (a dropped term,
+a swapped sign or index, a transposed operand); the pins must reject it.
+"""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+from tests import oracle_pins
+
+ORACLE_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "lg_oracle.py")
+
+
+def fresh_oracle():
+    spec = importlib.util.spec_from_file_location("lg_oracle_mutant", ORACLE_PATH)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def mut_swap_sides(O):
+    orig = O.band_mask
+    O.band_mask = lambda N, wl, wr, d, causal: orig(N, wr, wl, d, causal)
+    orig_row = O.allowed_row
+    O.allowed_row = lambda i, N, wl, wr, d, causal, g: orig_row(i, N, wr, wl, d, causal, g)
+
+
+def mut_ignore_dilation(O):
+    orig = O.band_mask
+    O.band_mask = lambda N, wl, wr, d, causal: orig(N, wl, wr, 1, causal)
+
+
+def mut_span_not_steps(O):
+    # window counted in positions instead of dilation steps
+    orig = O.band_mask
+    O.band_mask = lambda N, wl, wr, d, causal: orig(N, wl // d, wr // d, d, causal)
+
+
+def mut_causal_keeps_right(O):
+    orig = O.band_mask
+    O.band_mask = lambda N, wl, wr, d, causal: orig(N, wl, wr, d, False)
+
+
+def mut_no_global_columns(O):
+    def allowed_mask(N, wl, wr, d, causal, g):
+        m = O.band_mask(N, wl, wr, d, causal)
+        m |= O.global_flags(N, g)[:, None]
+        return m
+    O.allowed_mask = allowed_mask
+
+
+def mut_no_scale(O):
+    orig = O.masked_attention
+    O.masked_attention = lambda q, k, v, mask, scale: orig(q, k, v, mask, 1.0)
+
+
+def mut_transposed_logits(O):
+    def masked_attention(q, k, v, mask, scale):
+        q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+        logits = scale * (q @ k.T)
+        if logits.shape[0] == logits.shape[1]:
+            logits = logits.T
+        logits = np.where(mask, logits, -np.inf)
+        mx = logits.max(axis=1, keepdims=True)
+        e = np.exp(logits - mx); den = e.sum(axis=1, keepdims=True)
+        return (e / den) @ v, (mx + np.log(den))[:, 0], e / den
+    O.masked_attention = masked_attention
+
+
+def mut_lse_log2(O):
+    orig = O.masked_attention
+    def masked_attention(q, k, v, mask, scale):
+        o, l, p = orig(q, k, v, mask, scale)
+        return o, l / np.log(2.0), p
+    O.masked_attention = masked_attention
+
+
+def mut_etc_radius_off_by_one(O):
+    orig = O.etc_mask
+    O.etc_mask = lambda L, G, r: orig(L, G, r + 1)
+
+
+def mut_etc_no_l2g(O):
+    orig = O.etc_mask
+    def etc_mask(L, G, r):
+        m = orig(L, G, r); m[G:, :G] = False
+        return m
+    O.etc_mask = etc_mask
+
+
+def mut_closed_form_no_overlap(O):
+    orig = O.count_pairs_closed
+    def count(N, wl, wr, d, causal, g):
+        g = list(g)
+        if not g:
+            return orig(N, wl, wr, d, causal, g)
+        band = orig(N, wl, wr, d, causal, [])
+        return band + 2 * len(g) * N - len(g) ** 2
+    O.count_pairs_closed = count
+
+
+def mut_merge_no_rescale(O):
+    def merge_partials(ms, ls, accs):
+        ls = np.asarray(ls); accs = np.asarray(accs); ms = np.asarray(ms)
+        l = ls.sum(axis=0)
+        return accs.sum(axis=0) / l[:, None], ms.max(axis=0) + np.log(l)
+    O.merge_partials = merge_partials
+
+
+MUTANTS = [mut_swap_sides, mut_ignore_dilation, mut_span_not_steps, mut_causal_keeps_right,
+           mut_no_global_columns, mut_no_scale, mut_transposed_logits, mut_lse_log2,
+           mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
+def test_mutant_is_caught(mutant):
+    O = fresh_oracle()
+    mutant(O)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"{mutant.__name__} passed every pin"
