@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Sparse attention forward throughput: TFLOP/s over useful (allowed) pairs.
+
+FLOPs = 4 * D * P, P the number of allowed (query, key) pairs over all
+batches and heads (one multiply-add of q.k and one of p*v per pair and
+dimension).  Default workload: bf16 B1 H16 N131072 D128, window 512/512,
+128 uniform-random global tokens (the long-sequence case).  Inputs are
+seeded synthetic iid N(0, 1) tensors, larger than L2; the timed region holds
+only the library call (inputs resident in HBM).  The "e2e" figure times the
+same call through the public API with the inputs copied from pinned host
+memory and the outputs read back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Under torchrun each rank runs one replica of the workload on its own GPU
+(no data exchange); the time is the max over ranks and the value the work of
+all ranks over that time.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded; set before numpy loads its BLAS.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_long_sequence_window_gb300 import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def useful_pairs(lg, w: workloads.Workload) -> int:
+    if w.is_etc:
+        return w.B * w.H * lg.etc_count_pairs(w.N, w.etc_G, w.radius)
+    g = workloads.global_positions(w)
+    per_head = {}
+    total = 0
+    for d in w.dilations():
+        if d not in per_head:
+            per_head[d] = lg.count_pairs(w.N, w.w_left, w.w_right, d, w.causal, g)
+        total += per_head[d]
+    return w.B * total
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd[1:1] = ["-i", uuid]
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1])); mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- inputs
+
+def device_inputs(w, dev, torch):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def rnd(*shape):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(dt)
+
+    t = {n: rnd(w.B, w.H, w.N, w.D) for n in ("q", "k", "v")}
+    if w.is_etc:
+        for n in ("q_g", "k_g", "v_g"):
+            t[n] = rnd(w.B, w.H, w.etc_G, w.D)
+        t["g"] = None
+    else:
+        g = workloads.global_positions(w)
+        t["g"] = torch.from_numpy(g).to(dev) if g.size else None
+    return t
+
+
+def make_call(lg, w, t, torch):
+    """Returns f() that runs one forward pass with preallocated outputs and workspace."""
+    dev = t["q"].device
+    if w.is_etc:
+        B, H, L, D, G = w.B, w.H, w.N, w.D, w.etc_G
+        out_l, out_g = torch.empty_like(t["q"]), torch.empty_like(t["q_g"])
+        lse_l = torch.empty(B, H, L, device=dev); lse_g = torch.empty(B, H, G, device=dev)
+        ws = torch.empty(lg.etc_attn_fwd_workspace_size(B, H, L, G, D, 1 if w.dtype == "bf16" else 0),
+                         dtype=torch.uint8, device=dev)
+
+        def f():
+            lg.etc_attn_fwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], w.radius,
+                            out_l=out_l, out_g=out_g, lse_l=lse_l, lse_g=lse_g, workspace=ws)
+        outs = (out_l, out_g, lse_l, lse_g)
+    else:
+        out = torch.empty_like(t["q"])
+        lse = torch.empty(w.B, w.H, w.N, device=dev)
+        ng = 0 if t["g"] is None else t["g"].numel()
+        ws = torch.empty(max(256, lg.attn_fwd_workspace_size(w.B, w.H, w.N, w.D, ng, 1 if w.dtype == "bf16" else 0)),
+                         dtype=torch.uint8, device=dev)
+
+        def f():
+            lg.attn_fwd(t["q"], t["k"], t["v"], w.w_left, w.w_right, w.dilations(), w.causal, t["g"],
+                        out=out, lse=lse, workspace=ws)
+        outs = (out, lse)
+    return f, outs, ws
+
+
+def launches_per_call(w):
+    if w.dtype == "f32":
+        return 2 if (not w.is_etc and (w.global_positions or w.n_random_global)) else 1
+    if w.is_etc:
+        return 2  # tensor-core kernel + merge
+    dil = [d for d in set(w.dilations()) if d != 1]
+    groups = max(1, -(-len(dil) // 3))
+    has_g = bool(w.global_positions) or w.n_random_global > 0
+    return groups + (2 if has_g else 0)
+
+
+# ---------------------------------------------------------------------- native arm
+
+def time_steps(torch, f, steps, flush):
+    """Per-step CUDA-event times (ms) on the current stream; L2 flushed between steps if asked."""
+    stream = torch.cuda.current_stream()
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    times = []
+    for _ in range(steps):
+        if scratch is not None:
+            scratch.zero_()
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        a.record(stream); f(); b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def run_native(args, rank, world):
+    import torch
+    import sparse_long_sequence_window_gb300 as lg
+    lg.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workloads.PRESETS[args.workload]
+    t = device_inputs(w, dev, torch)
+    f, outs, ws = make_call(lg, w, t, torch)
+    pairs = useful_pairs(lg, w)
+    flops = 4.0 * w.D * pairs
+    in_bytes = sum(x.numel() * x.element_size() for k, x in t.items() if x is not None)
+    flush = in_bytes < 2 * L2_BYTES
+
+    for _ in range(args.warmup):
+        f()
+    torch.cuda.synchronize()
+    st = lg.query_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {lg.status_string(st)}")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(uuid)
+    lg.profile_begin()
+    step_ms = time_steps(torch, f, args.steps, flush)
+    kernel_ms, kernel_launches = lg.profile_end()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = float(sum(step_ms))
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = flops * args.steps * world / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs -> device -> call -> host outputs
+    e2e = None
+    host = {k: (x.cpu().pin_memory() if x is not None else None) for k, x in t.items()}
+    host_out = [o.cpu().pin_memory() for o in outs]
+    e2e_steps = max(1, min(args.steps, 10))
+    stream = torch.cuda.current_stream()
+    h2d = sum(x.numel() * x.element_size() for x in host.values() if x is not None)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+    e_times = []
+    for _ in range(e2e_steps):
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k_, x in host.items():
+            if x is not None:
+                t[k_].copy_(x, non_blocking=True)
+        f()
+        for ho, o in zip(host_out, outs):
+            ho.copy_(o, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e_times.append(a.elapsed_time(b))
+    e_ms = float(sum(e_times))
+    if dist:
+        tt = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e2e = {"value": flops * e2e_steps * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    # ---- roofline of the dominant kernel (the tensor-core attention kernel does every useful FLOP)
+    peaks, peak_kind = measured_peaks()
+    if w.dtype == "bf16":
+        peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) if peaks else FALLBACK_BF16_TFLOPS
+        kernel_per_step = kernel_ms / max(1, args.steps)
+        achieved = flops / (kernel_per_step / 1e3) / 1e12
+        traffic = committed_traffic(w)
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "peak_source": f"bf16_tflops of {peak_kind}", "kernel": "tc_attn_kernel",
+                    "kernel_ms_per_launch": round(kernel_ms / max(1, kernel_launches), 4),
+                    "launches": kernel_launches}
+    else:
+        roofline = None
+
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        per_config = sweep(lg, torch, dev)
+
+    line = {
+        "metric": "sparse attn fwd TFLOP/s (in-band pairs) & % bf16 tensor peak, N=512-128K",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic iid N(0,1), seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "useful_pairs": pairs, "useful_flops_per_step": flops,
+                   "l2": "flushed between steps" if flush else "inputs larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_bf16_peak": round(100 * value / world / (roofline["peak"] if roofline else FALLBACK_BF16_TFLOPS), 2),
+        "e2e": e2e,
+        "gpu_launches": launches_per_call(w) * args.steps,
+        "roofline": roofline,
+        "clocks": clk,
+        "step_ms_median": round(statistics.median(step_ms), 5),
+    }
+    if per_config:
+        line["per_config"] = per_config
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+def sweep(lg, torch, dev):
+    """Every preset, briefly: TFLOP/s and ms per call (runtime against N for the long-scale trio)."""
+    res = {}
+    for name, w in workloads.PRESETS.items():
+        t = device_inputs(w, dev, torch)
+        f, outs, ws = make_call(lg, w, t, torch)
+        flops = 4.0 * w.D * useful_pairs(lg, w)
+        in_bytes = sum(x.numel() * x.element_size() for x in t.values() if x is not None)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        steps = 30 if w.N >= 100000 else 100
+        ms = time_steps(torch, f, steps, in_bytes < 2 * L2_BYTES)
+        st = lg.query_status(ws)
+        med = statistics.median(ms)
+        res[name] = {"tflops": round(flops / (med / 1e3) / 1e12, 2), "ms": round(med, 5),
+                     "status": lg.status_string(st)}
+        del t, f, outs, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def committed_traffic(w):
+    """DRAM bytes per launch from a committed ncu capture of the current kernel source, else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        import hashlib
+        with open(path) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "sparse_long_sequence_window_gb300", "csrc", "lg_tc.cu")
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        ent = rec.get(w.name)
+        if ent and ent.get("kernel_sha") == digest:
+            return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+# ---------------------------------------------------------------------- CPU oracle
+
+def cpu_sample(w, budget_s, seed=1234):
+    """Runs the CPU oracle on uniformly sampled rows of one head for about budget_s seconds.
+
+    Returns (useful FLOPs computed, seconds, rows).
+    """
+    from oracle import lg_oracle
+    rng = np.random.default_rng(seed)
+    D, N = w.D, w.N
+    if w.is_etc:
+        G = w.etc_G
+        arrs = [rng.standard_normal((1, 1, n, D), dtype=np.float32) for n in (N, N, N, G, G, G)]
+        flops = 0.0; rows = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            i = int(rng.integers(0, N))
+            lg_oracle.etc_attn_fwd_rows(*arrs, w.radius, [i])
+            lo, hi = max(0, i - w.radius), min(N - 1, i + w.radius)
+            flops += 4.0 * D * ((hi - lo + 1) + G)
+            rows += 1
+        return flops, time.perf_counter() - t0, rows
+    g = workloads.global_positions(w)
+    gflags = np.zeros(N, bool); gflags[g] = True
+    q, k, v = (rng.standard_normal((1, 1, N, D), dtype=np.float32) for _ in range(3))
+    d = w.dilations()[0]
+    flops = 0.0; rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        i = int(rng.integers(0, N))
+        lg_oracle.attn_fwd_rows(q, k, v, w.w_left, w.w_right, [d], w.causal, g, [i])
+        n_keys = int(lg_oracle.allowed_row(i, N, w.w_left, w.w_right, d, w.causal, gflags).sum())
+        flops += 4.0 * D * n_keys
+        rows += 1
+    return flops, time.perf_counter() - t0, rows
+
+
+def cpu_baseline(w, budget_s=15.0):
+    flops, secs, rows = cpu_sample(w, budget_s)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} uniformly drawn query rows of one head of {w.name}, fp64 numpy, "
+                      f"{secs:.1f} s, one thread"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step a bounded sample of the workload's rows."""
+    w = workloads.PRESETS[args.workload]
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_sample(w, per_step, seed=99)
+    total_f, total_s, total_rows = 0.0, 0.0, 0
+    for s in range(args.steps):
+        fl, sec, rows = cpu_sample(w, per_step, seed=1000 + s)
+        total_f += fl; total_s += sec; total_rows += rows
+    value = total_f / total_s / 1e12
+    sample = (f"{total_rows} uniformly drawn query rows of one head of {w.name} over {args.steps} steps "
+              f"of ~{per_step:.1f} s each, fp64 numpy, one thread")
+    return {
+        "impl": "reference",
+        "metric": "sparse attn fwd TFLOP/s (in-band pairs) & % bf16 tensor peak, N=512-128K",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic iid N(0,1), seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="long_128k", choices=sorted(workloads.PRESETS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    line = run_native(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

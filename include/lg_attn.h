@@ -1,0 +1,171 @@
+/*
+ * lg_attn.h -- C ABI of the window + dilation + global sparse self-attention
+ * forward pass for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What is computed (per batch b and head h, query i, key j, 0 <= i, j < N):
+ *
+ *   inband(i, j)  <=>  j = i + d_h * t  for an integer t with
+ *                      -w_left <= t <= (causal ? 0 : w_right)
+ *     "Longformer: The Long-Document Transformer", section 3.4, "Sliding
+ *     Window Attention" (w/2 keys on each side plus the token itself) and
+ *     "Dilated Sliding Window Attention" (keys i +- d*k for k <= w/2, same key
+ *     count, span times d); causal mode from "Autoregressive Language
+ *     Modeling Configuration" (only the keys to the left).  w_left / w_right
+ *     count steps of the dilation; keys outside [0, N) are dropped.
+ *
+ *   allowed(i, j) <=>  inband(i, j) or i in G or j in G
+ *     Longformer page, "Global Attention": a global token attends to every
+ *     token and every token attends to it.  A global key that is also in the
+ *     band counts once.  Causal mode restricts only the band.
+ *
+ *   LSE_i = ln sum_{j allowed} exp(s * <q_i, k_j>),
+ *   O_i   = sum_{j allowed} exp(s * <q_i, k_j> - LSE_i) * v_j.
+ *
+ * The ETC call follows "ETC: Encoding Long and Structured Inputs in
+ * Transformers", section 3.4, "Global-Local Attention": a separate global
+ * input of G tokens; g2g, g2l and l2g are full, l2l is |i - j| <= radius
+ * (clamped), and g2g+g2l / l2g+l2l each share one softmax.
+ *
+ * Conventions for every call:
+ *  - Tensors q, k, v, out are contiguous row-major [B, H, N, D] of dtype dt,
+ *    in device memory, 16-byte aligned.  lse is contiguous fp32 [B, H, N] in
+ *    device memory.  Outputs have the input dtype (LG_F32 or LG_BF16); every
+ *    softmax statistic and accumulation is fp32.
+ *  - The caller owns every buffer, including the workspace; the library
+ *    allocates no device memory.  Tensor-map descriptors are built on the host
+ *    for each call and passed as kernel parameters.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *    none synchronises.  Argument errors are returned before anything is
+ *    launched.  Errors found on the device (bad global indices, a bounded
+ *    wait that ran out) are recorded in the workspace's status word and
+ *    returned by lg_query_status.  Each call clears that word first.
+ *  - Calls that share a workspace must not overlap on the device.
+ */
+#ifndef LG_ATTN_H
+#define LG_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* lg_stream_t;
+
+typedef enum {
+  LG_OK = 0,
+  LG_ERR_INVALID_ARG = 1,   /* a pointer, size or value is out of its documented range */
+  LG_ERR_UNSUPPORTED = 2,   /* valid arguments this build does not run (e.g. bf16 with D not 64/128) */
+  LG_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  LG_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out; outputs are undefined */
+  LG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than the *_workspace_size result */
+  LG_ERR_GLOBAL_IDX = 6     /* global_idx not strictly increasing or outside [0, N) (found on the device) */
+} lg_status;
+
+typedef enum { LG_F32 = 0, LG_BF16 = 1 } lg_dtype;
+
+/* Largest head count of one call, and largest per-head dilation of the bf16 path. */
+#define LG_MAX_HEADS 128
+#define LG_MAX_BF16_DILATION 8
+
+/* Static string naming a status; never NULL. */
+const char* lg_status_string(lg_status s);
+
+/* Library version string, e.g. "0.1.0 sm_103a". */
+const char* lg_version(void);
+
+/*
+ * Bytes of device workspace lg_attn_fwd needs for these sizes.  The workspace
+ * holds the device status word, the gathered global-token rows (bf16) and the
+ * partial softmax statistics of the global-query rows.  It must be 256-byte
+ * aligned.  Returns 0 if the sizes are invalid.
+ */
+size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_dtype dt);
+
+/*
+ * Longformer-style window + dilation + global attention, forward.
+ *
+ *  q, k, v     device, [B, H, N, D], dtype dt, read only.
+ *  out         device, [B, H, N, D], dtype dt, written (every row).
+ *  lse         device, fp32 [B, H, N], written: natural log of the softmax
+ *              denominator of each row over the scaled logits.
+ *  dt          LG_F32 (CUDA-core fp32 path, 1 <= D <= 128, D % 4 == 0) or
+ *              LG_BF16 (tensor-core path, D in {64, 128}).
+ *  w_left, w_right  window steps on each side, >= 0.  w_right is ignored
+ *              when causal != 0.
+ *  dilation    HOST pointer to H ints >= 1 (bf16: <= LG_MAX_BF16_DILATION);
+ *              read during the call only.
+ *  causal      0 or 1.
+ *  global_idx  DEVICE pointer to n_global int32 positions, strictly
+ *              increasing, in [0, N); may be NULL iff n_global == 0.  A bad
+ *              list is reported as LG_ERR_GLOBAL_IDX by lg_query_status; no
+ *              memory outside the tensors is touched in that case.
+ *  n_global    0 <= n_global <= N.
+ *  scale       logit scale s; a value <= 0 selects 1/sqrt(D).
+ *  workspace   device, >= lg_attn_fwd_workspace_size(...) bytes.
+ *  stream      CUDA stream the work is queued on.
+ */
+lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      lg_dtype dt, int B, int H, int N, int D,
+                      int w_left, int w_right, const int32_t* dilation, int causal,
+                      const int32_t* global_idx, int n_global, float scale,
+                      void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/* Bytes of device workspace lg_etc_attn_fwd needs; 0 if the sizes are invalid. */
+size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt);
+
+/*
+ * ETC-style global-local attention, forward.
+ *
+ *  q_l, k_l, v_l   device, long input [B, H, L, D], dtype dt.
+ *  q_g, k_g, v_g   device, global input [B, H, G, D], dtype dt.
+ *  out_l, out_g    device, [B, H, L, D] and [B, H, G, D], dtype dt, written.
+ *  lse_l, lse_g    device, fp32 [B, H, L] and [B, H, G], written.
+ *  radius          local radius r >= 0: long query i sees long keys with
+ *                  |i - j| <= r plus all G global keys, in one softmax;
+ *                  global query sees all G + L keys, in one softmax.
+ *  L >= 1, G >= 1; dt, D, scale, workspace, stream as for lg_attn_fwd.
+ */
+lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l,
+                          const void* q_g, const void* k_g, const void* v_g,
+                          void* out_l, void* out_g, float* lse_l, float* lse_g,
+                          lg_dtype dt, int B, int H, int L, int G, int D, int radius, float scale,
+                          void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device status recorded in
+ * `workspace` by the last call that used it (LG_OK if none) and clears it.
+ * Returns LG_ERR_CUDA if the synchronisation or the read fails.
+ */
+lg_status lg_query_status(const void* workspace, lg_stream_t stream);
+
+/*
+ * Number of allowed (query, key) pairs of ONE head of lg_attn_fwd (host
+ * computation; global_idx_host is a HOST array, sorted and unique).  The
+ * useful work of a call is 4 * D * (sum over heads and batches) FLOPs:
+ * one multiply-add of q.k and one of p*v per pair and dimension.
+ * Returns -1 on invalid arguments.
+ */
+int64_t lg_count_pairs(int N, int w_left, int w_right, int dilation, int causal,
+                       const int32_t* global_idx_host, int n_global);
+
+/* Allowed pairs of ONE head of lg_etc_attn_fwd; -1 on invalid arguments. */
+int64_t lg_etc_count_pairs(int L, int G, int radius);
+
+/*
+ * Kernel timing of the dominant attention kernel.  After lg_profile_begin,
+ * each launch of that kernel is bracketed by CUDA events on its stream;
+ * lg_profile_end synchronises those events and returns the summed elapsed
+ * milliseconds and the number of launches, then stops recording.  Not for
+ * use during stream capture; not thread safe.
+ */
+lg_status lg_profile_begin(void);
+lg_status lg_profile_end(float* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LG_ATTN_H */

@@ -1,0 +1,212 @@
+"""Window + dilation + global sparse self-attention (forward) for one GB300 GPU.
+
+Python binding of the C ABI in ``include/lg_attn.h``.  This module only
+marshals arguments (device pointers, sizes, the current CUDA stream) into the
+shared library ``liblg_attn.so``; every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "LgError", "load", "attn_fwd", "etc_attn_fwd", "attn_fwd_workspace_size",
+    "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
+    "profile_begin", "profile_end", "status_string", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblg_attn.so")
+
+LG_OK, LG_ERR_INVALID_ARG, LG_ERR_UNSUPPORTED, LG_ERR_CUDA, LG_ERR_TIMEOUT, LG_ERR_WORKSPACE, LG_ERR_GLOBAL_IDX = range(7)
+LG_F32, LG_BF16 = 0, 1
+
+_lib = None
+
+
+class LgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def load() -> ctypes.CDLL:
+    """Loads liblg_attn.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m sparse_long_sequence_window_gb300._build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    lib.lg_status_string.restype = ctypes.c_char_p
+    lib.lg_status_string.argtypes = [i32]
+    lib.lg_version.restype = ctypes.c_char_p
+    lib.lg_attn_fwd_workspace_size.restype = sz
+    lib.lg_attn_fwd_workspace_size.argtypes = [i32] * 5 + [i32]
+    lib.lg_etc_attn_fwd_workspace_size.restype = sz
+    lib.lg_etc_attn_fwd_workspace_size.argtypes = [i32] * 5 + [i32]
+    lib.lg_attn_fwd.restype = i32
+    lib.lg_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32,
+                                vp, sz, vp]
+    lib.lg_etc_attn_fwd.restype = i32
+    lib.lg_etc_attn_fwd.argtypes = [vp] * 10 + [i32] * 7 + [f32, vp, sz, vp]
+    lib.lg_query_status.restype = i32
+    lib.lg_query_status.argtypes = [vp, vp]
+    lib.lg_count_pairs.restype = ctypes.c_int64
+    lib.lg_count_pairs.argtypes = [i32, i32, i32, i32, i32, vp, i32]
+    lib.lg_etc_count_pairs.restype = ctypes.c_int64
+    lib.lg_etc_count_pairs.argtypes = [i32, i32, i32]
+    lib.lg_profile_begin.restype = i32
+    lib.lg_profile_begin.argtypes = []
+    lib.lg_profile_end.restype = i32
+    lib.lg_profile_end.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(i32)]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().lg_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != LG_OK:
+        raise LgError(status, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return LG_F32
+    if t.dtype == torch.bfloat16:
+        return LG_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def attn_fwd_workspace_size(B, H, N, D, n_global, dtype_code) -> int:
+    return int(load().lg_attn_fwd_workspace_size(B, H, N, D, n_global, dtype_code))
+
+
+def etc_attn_fwd_workspace_size(B, H, L, G, D, dtype_code) -> int:
+    return int(load().lg_etc_attn_fwd_workspace_size(B, H, L, G, D, dtype_code))
+
+
+def _workspace(nbytes: int, device, workspace):
+    import torch
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int]] = None,
+             causal: bool = False, global_idx=None, scale: Optional[float] = None,
+             out=None, lse=None, workspace=None, stream=None):
+    """Longformer-style window + dilation + global attention forward.
+
+    q, k, v: CUDA tensors [B, H, N, D] (float32 or bfloat16, contiguous).
+    dilation: H ints (default all 1).  global_idx: sorted unique int32 CUDA
+    tensor of positions (or None).  Returns (out [B, H, N, D], lse [B, H, N]
+    float32).  Asynchronous on the current stream.
+    """
+    import torch
+    lib = load()
+    B, H, N, D = q.shape
+    dil = np.ascontiguousarray(np.asarray(dilation if dilation is not None else [1] * H, dtype=np.int32))
+    if dil.size != H:
+        raise ValueError("dilation needs H entries")
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    if global_idx is not None and global_idx.dtype != torch.int32:
+        raise TypeError("global_idx must be int32")
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = attn_fwd_workspace_size(B, H, N, D, n_global, dt)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.lg_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), dt, B, H, N, D,
+                         int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
+                         _ptr(global_idx) if n_global else None, n_global,
+                         float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "lg_attn_fwd")
+    attn_fwd.last_workspace = ws
+    return out, lse
+
+
+def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius: int, scale: Optional[float] = None,
+                 out_l=None, out_g=None, lse_l=None, lse_g=None, workspace=None, stream=None):
+    """ETC-style global-local attention forward.  Returns (out_l, out_g, lse_l, lse_g)."""
+    import torch
+    lib = load()
+    B, H, L, D = q_l.shape
+    G = q_g.shape[2]
+    dt = _dtype_code(q_l)
+    out_l = torch.empty_like(q_l) if out_l is None else out_l
+    out_g = torch.empty_like(q_g) if out_g is None else out_g
+    lse_l = torch.empty((B, H, L), dtype=torch.float32, device=q_l.device) if lse_l is None else lse_l
+    lse_g = torch.empty((B, H, G), dtype=torch.float32, device=q_l.device) if lse_g is None else lse_g
+    need = etc_attn_fwd_workspace_size(B, H, L, G, D, dt)
+    ws = _workspace(need, q_l.device, workspace)
+    st = lib.lg_etc_attn_fwd(_ptr(q_l), _ptr(k_l), _ptr(v_l), _ptr(q_g), _ptr(k_g), _ptr(v_g),
+                             _ptr(out_l), _ptr(out_g), _ptr(lse_l), _ptr(lse_g), dt, B, H, L, G, D,
+                             int(radius), float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(),
+                             _stream(stream))
+    _check(st, "lg_etc_attn_fwd")
+    etc_attn_fwd.last_workspace = ws
+    return out_l, out_g, lse_l, lse_g
+
+
+def query_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status of the last call."""
+    return int(load().lg_query_status(workspace.data_ptr(), _stream(stream)))
+
+
+def count_pairs(N, w_left, w_right, dilation, causal, global_idx_host=None) -> int:
+    """Allowed pairs of one head (host computation in the library)."""
+    g = np.ascontiguousarray(np.asarray([] if global_idx_host is None else global_idx_host, dtype=np.int32))
+    r = load().lg_count_pairs(int(N), int(w_left), int(w_right), int(dilation), int(bool(causal)),
+                              g.ctypes.data if g.size else None, int(g.size))
+    if r < 0:
+        raise ValueError("invalid arguments to lg_count_pairs")
+    return int(r)
+
+
+def etc_count_pairs(L, G, radius) -> int:
+    r = load().lg_etc_count_pairs(int(L), int(G), int(radius))
+    if r < 0:
+        raise ValueError("invalid arguments to lg_etc_count_pairs")
+    return int(r)
+
+
+def profile_begin():
+    _check(load().lg_profile_begin(), "lg_profile_begin")
+
+
+def profile_end():
+    """Returns (total milliseconds, launches) of the dominant kernel since profile_begin."""
+    ms = ctypes.c_float(0.0)
+    n = ctypes.c_int(0)
+    _check(load().lg_profile_end(ctypes.byref(ms), ctypes.byref(n)), "lg_profile_end")
+    return float(ms.value), int(n.value)

@@ -1,0 +1,123 @@
+// Support kernels of the bf16 path:
+//  * prep: checks that the global positions are strictly increasing and inside
+//    [0, N) (a bad list sets a status bit; nothing outside the tensors is
+//    touched) and gathers the global tokens' q, k, v rows into contiguous
+//    [BH, g, D] buffers that the tensor-core kernel reads with TMA.
+//  * merge: combines the partial softmax statistics of the global-query rows
+//    over the key splits.  With m = max_p m_p: l = sum_p 2^{m_p - m} l_p,
+//    O = sum_p 2^{m_p - m} acc_p / l, LSE = (m + log2 l) ln 2 (statistics are
+//    kept in log2 units).  This is the softmax-denominator weighting of
+//    "LONGNET: Scaling Transformers to 1,000,000,000 Tokens", section 3.4,
+//    "Mixture of Dilated Attentions", which equals one joint softmax over the
+//    union of the key splits.  One warp per global row: lanes split the
+//    partials for the max and the sum (shuffle reductions) and the
+//    dimensions for the output.
+#include <math.h>
+
+#include "lg_internal.h"
+
+namespace lg {
+namespace {
+
+__global__ void prep_kernel(const PrepParams p) {
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthreads = gridDim.x * blockDim.x;
+  for (int r = tid; r < p.n_glob; r += nthreads) {
+    const int pos = p.gidx[r];
+    bool bad = pos < 0 || pos >= p.N;
+    if (r > 0 && p.gidx[r - 1] >= pos) bad = true;
+    if (bad) atomicOr(p.status, ST_GLOBAL_IDX);
+  }
+  if (p.q == nullptr) return;
+  const int lane = threadIdx.x & 31;
+  const int chunks = p.D / 8;  // 16-byte pieces of a row
+  const long long total = static_cast<long long>(p.BH) * p.n_glob;
+  for (long long wid = tid >> 5; wid < total; wid += nthreads >> 5) {
+    const int bh = static_cast<int>(wid / p.n_glob);
+    const int r = static_cast<int>(wid % p.n_glob);
+    const int pos = p.gidx[r];
+    const bool ok = pos >= 0 && pos < p.N;
+    if (lane < chunks) {
+      const size_t src = (static_cast<size_t>(bh) * p.N + (ok ? pos : 0)) * p.D + lane * 8;
+      const size_t dst = (static_cast<size_t>(bh) * p.n_glob + r) * p.D + lane * 8;
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(p.qg + dst) = ok ? *reinterpret_cast<const uint4*>(p.q + src) : zero;
+      *reinterpret_cast<uint4*>(p.kg + dst) = ok ? *reinterpret_cast<const uint4*>(p.k + src) : zero;
+      *reinterpret_cast<uint4*>(p.vg + dst) = ok ? *reinterpret_cast<const uint4*>(p.v + src) : zero;
+    }
+  }
+}
+
+template <int D>
+__global__ void merge_kernel(const MergeParams p, int bf16_out) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<long long>(p.BH) * p.n_glob) return;
+  const int bh = static_cast<int>(wid / p.n_glob);
+  const int r = static_cast<int>(wid % p.n_glob);
+  const size_t base = static_cast<size_t>(wid) * p.n_splits;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base;
+
+  float m = -INFINITY;
+  for (int s = lane; s < p.n_splits; s += 32) m = fmaxf(m, ml[s].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+  for (int s = lane; s < p.n_splits; s += 32) {
+    const float2 v = ml[s];
+    if (v.x != -INFINITY) l += exp2f(v.x - m) * v.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int t = 0; t < PER; ++t) acc[t] = 0.f;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float2 v = ml[s];
+    if (v.x == -INFINITY) continue;
+    const float wgt = exp2f(v.x - m);
+    const float* a = p.part_acc + (base + s) * D;
+#pragma unroll
+    for (int t = 0; t < PER; ++t) acc[t] = fmaf(wgt, a[lane + 32 * t], acc[t]);
+  }
+  const int row = p.gidx ? p.gidx[r] : r;
+  if (row < 0 || row >= p.N_out) return;
+  const float inv_l = 1.f / l;
+  const size_t orow = (static_cast<size_t>(bh) * p.N_out + row) * D;
+  if (bf16_out) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + orow;
+#pragma unroll
+    for (int t = 0; t < PER; ++t) o[lane + 32 * t] = __float2bfloat16_rn(acc[t] * inv_l);
+  } else {
+    float* o = reinterpret_cast<float*>(p.out) + orow;
+#pragma unroll
+    for (int t = 0; t < PER; ++t) o[lane + 32 * t] = acc[t] * inv_l;
+  }
+  if (lane == 0) p.lse[static_cast<size_t>(bh) * p.N_out + row] = (m + log2f(l)) * 0.6931471805599453f;
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
+  if (p.n_glob <= 0) return cudaSuccess;
+  long long work = p.q ? static_cast<long long>(p.BH) * p.n_glob * 32 : p.n_glob;
+  long long nb = (work + 255) / 256;
+  int blocks = static_cast<int>(nb < 4096 ? nb : 4096);
+  if (blocks < 1) blocks = 1;
+  prep_kernel<<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s) {
+  const long long warps = static_cast<long long>(p.BH) * p.n_glob;
+  if (warps <= 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+  if (p.D == 64) merge_kernel<64><<<blocks, 256, 0, s>>>(p, bf16_out);
+  else if (p.D == 128) merge_kernel<128><<<blocks, 256, 0, s>>>(p, bf16_out);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace lg

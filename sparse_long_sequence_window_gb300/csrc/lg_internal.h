@@ -1,0 +1,98 @@
+// Internal declarations shared by the CUDA translation units of liblg_attn.
+// Not part of the public ABI (that is include/lg_attn.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/lg_attn.h"
+
+namespace lg {
+
+// Device status word bits (workspace offset 0).  The host maps the highest
+// set bit to an lg_status.
+enum : int {
+  ST_GLOBAL_IDX = 1 << 0,
+  ST_TIMEOUT = 1 << 1,
+};
+
+constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace
+constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
+constexpr int kTileN = 128;              // keys per tile
+constexpr int kSplitTiles = 16;          // key tiles per split of a global-query row block
+constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
+
+// ---------------------------------------------------------------- fp32 CUDA-core path
+
+struct SimtParams {
+  const float* q; const float* k; const float* v;   // [BH, N, D] (ETC: long input, N = L)
+  const float* qg; const float* kg; const float* vg; // ETC only: global input [BH, G, D]
+  float* out; float* lse;                           // [BH, N, D], [BH, N]
+  float* out_g; float* lse_g;                       // ETC only
+  const int* gidx;                                   // Longformer global positions (device)
+  int BH, H, N, D;
+  int wl, wr;                                        // wr already 0 when causal
+  int n_glob;                                        // Longformer: g; ETC: G
+  int etc;
+  float scale;
+  int dil[LG_MAX_HEADS];
+};
+
+// ---------------------------------------------------------------- bf16 tensor-core path
+
+// One launch covers all batches and the heads whose dilation has a slot here.
+// Work units: first the global-query row units (gtile, split) per (b, h), then
+// the band units (dilation residue class c, query tile) per (b, h).
+struct TcParams {
+  CUtensorMap mapQ[kMaxSlots];   // main q/k/v viewed as {D, N, BH}, rows strided by the slot's dilation
+  CUtensorMap mapK[kMaxSlots];
+  CUtensorMap mapV[kMaxSlots];
+  CUtensorMap mapQg, mapKg, mapVg;  // global side {D, g, BH}: gathered rows (Longformer) or q_g/k_g/v_g (ETC)
+  void* out;                      // bf16 [BH, N, D]
+  float* lse;                     // [BH, N]
+  float* part_acc;                // [BH, n_glob, n_splits, D] unnormalised partial outputs
+  float* part_ml;                 // [BH, n_glob, n_splits, 2] partial (max, sum), max in log2 units
+  const int* gidx;                // Longformer global positions (device), for band de-duplication
+  int* status;
+  long long wait_cap;             // clock64 cycles a bounded wait may spin
+  float scale_log2;               // scale * log2(e)
+  int BH, H, N, D;                // N = L for ETC
+  int wl, wr;                     // wr already 0 when causal
+  int n_glob;                     // g (Longformer) or G (ETC)
+  int etc;
+  int n_grow_units;               // global-query row units (placed first)
+  int n_gtiles;                   // query tiles of the global rows
+  int n_splits;                   // key splits of the global rows
+  int n_key_tiles_grow;           // key tiles of one global row block (ETC: ceil(G/128) + ceil(L/128))
+  int band_units_per_batch;
+  int slot_dil[kMaxSlots];
+  int slot_units[kMaxSlots];      // band units of one head with this slot's dilation
+  unsigned char head_slot[LG_MAX_HEADS];  // 255: head not in this launch
+  int head_unit_start[LG_MAX_HEADS + 1];  // prefix of band units over heads (one batch)
+};
+
+struct MergeParams {
+  const float* part_acc; const float* part_ml;
+  void* out; float* lse;          // Longformer: out/lse of the main tensor; ETC: out_g/lse_g
+  const int* gidx;                // Longformer: scatter rows; NULL for ETC (row r -> row r)
+  int BH, N_out, D, n_glob, n_splits;
+};
+
+struct PrepParams {
+  const int* gidx; int n_glob; int N;
+  const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;  // NULL: validate only
+  __nv_bfloat16* qg; __nv_bfloat16* kg; __nv_bfloat16* vg;                 // [BH, g, D]
+  int BH, D;
+  int* status;
+};
+
+// Host-side launchers (each defined next to its kernel).
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s);
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
+size_t tc_smem_bytes(int D);
+
+}  // namespace lg

@@ -1,0 +1,136 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+rejects bad arguments before touching CUDA, and its host-side pair count
+agrees with the CPU oracle's (independently written) counts."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import sparse_long_sequence_window_gb300 as lg
+from oracle import lg_oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lg_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(lg.LIB_PATH):
+        from sparse_long_sequence_window_gb300 import _build
+        _build.build()
+    return lg.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lg.status_string(s).startswith("LG_")
+    assert b"sm_103a" in lib.lg_version()
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced on these paths
+
+
+def call_fwd(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, dt=lg.LG_BF16, B=1, H=2, N=256, D=64, wl=8, wr=8,
+             dil=(ctypes.c_int32 * 2)(1, 1), causal=0, gidx=None, ng=0, scale=0.0, ws=FAKE,
+             wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.lg_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dt"], a["B"], a["H"], a["N"],
+                           a["D"], a["wl"], a["wr"], ctypes.cast(a["dil"], ctypes.c_void_p) if a["dil"] else None,
+                           a["causal"], a["gidx"], a["ng"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), lg.LG_ERR_INVALID_ARG),
+    (dict(out=FAKE + 8), lg.LG_ERR_INVALID_ARG),
+    (dict(N=0), lg.LG_ERR_INVALID_ARG),
+    (dict(B=0), lg.LG_ERR_INVALID_ARG),
+    (dict(wl=-1), lg.LG_ERR_INVALID_ARG),
+    (dict(causal=2), lg.LG_ERR_INVALID_ARG),
+    (dict(dil=(ctypes.c_int32 * 2)(1, 0)), lg.LG_ERR_INVALID_ARG),
+    (dict(dil=None), lg.LG_ERR_INVALID_ARG),
+    (dict(ng=3, gidx=None), lg.LG_ERR_INVALID_ARG),
+    (dict(ng=300), lg.LG_ERR_INVALID_ARG),
+    (dict(dt=7), lg.LG_ERR_INVALID_ARG),
+    (dict(D=96), lg.LG_ERR_UNSUPPORTED),
+    (dict(dt=lg.LG_F32, D=130), lg.LG_ERR_UNSUPPORTED),
+    (dict(dil=(ctypes.c_int32 * 2)(1, 9)), lg.LG_ERR_UNSUPPORTED),
+    (dict(H=200, dil=(ctypes.c_int32 * 200)(*([1] * 200))), lg.LG_ERR_UNSUPPORTED),
+    (dict(ws=None), lg.LG_ERR_WORKSPACE),
+    (dict(ws=FAKE + 16), lg.LG_ERR_WORKSPACE),
+    (dict(wsb=16), lg.LG_ERR_WORKSPACE),
+])
+def test_argument_errors_return_before_launch(lib, over, expect):
+    assert call_fwd(lib, **over) == expect
+
+
+def test_etc_argument_errors(lib):
+    args = [FAKE] * 10 + [lg.LG_BF16, 1, 2, 100, 8, 64, 4, 0.0, FAKE, 1 << 30, None]
+    bad = list(args); bad[0] = None
+    assert lib.lg_etc_attn_fwd(*bad) == lg.LG_ERR_INVALID_ARG
+    bad = list(args); bad[13] = 0        # L = 0
+    assert lib.lg_etc_attn_fwd(*bad) == lg.LG_ERR_INVALID_ARG
+    bad = list(args); bad[16] = -1       # radius
+    assert lib.lg_etc_attn_fwd(*bad) == lg.LG_ERR_INVALID_ARG
+    bad = list(args); bad[15] = 32       # D
+    assert lib.lg_etc_attn_fwd(*bad) == lg.LG_ERR_UNSUPPORTED
+    bad = list(args); bad[19] = 64       # workspace bytes
+    assert lib.lg_etc_attn_fwd(*bad) == lg.LG_ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    assert lg.attn_fwd_workspace_size(1, 2, 512, 64, 0, lg.LG_F32) == 256
+    base = lg.attn_fwd_workspace_size(1, 12, 4096, 64, 0, lg.LG_BF16)
+    with_g = lg.attn_fwd_workspace_size(1, 12, 4096, 64, 65, lg.LG_BF16)
+    assert base == 256 and with_g > base
+    # the partial statistics grow with the number of key splits (linear in N)
+    a = lg.attn_fwd_workspace_size(1, 16, 8192, 128, 128, lg.LG_BF16)
+    b = lg.attn_fwd_workspace_size(1, 16, 32768, 128, 128, lg.LG_BF16)
+    assert b > a
+    assert lg.attn_fwd_workspace_size(0, 1, 1, 64, 0, lg.LG_BF16) == 0
+    assert lg.etc_attn_fwd_workspace_size(2, 12, 4096, 256, 64, lg.LG_BF16) > 256
+
+
+def test_count_pairs_agrees_with_oracle(lib):
+    rng = np.random.default_rng(21)
+    for _ in range(150):
+        N = int(rng.integers(1, 90))
+        wl, wr = int(rng.integers(0, 15)), int(rng.integers(0, 15))
+        d = int(rng.integers(1, 7)); causal = bool(rng.integers(0, 2))
+        ng = int(rng.integers(0, min(N, 7) + 1))
+        g = sorted(rng.choice(N, size=ng, replace=False).tolist()) if ng else []
+        expect = lg_oracle.count_pairs_bruteforce(N, wl, wr, d, causal, g)
+        assert lg.count_pairs(N, wl, wr, d, causal, g) == expect
+    # large sizes: against the oracle's closed form
+    for N, wl, wr, d, causal, g in [(4096, 256, 256, 1, False, list(range(65))),
+                                    (16384, 512, 0, 3, True, []),
+                                    (131072, 512, 512, 1, False, list(range(0, 131072, 1024)))]:
+        assert lg.count_pairs(N, wl, wr, d, causal, g) == lg_oracle.count_pairs_closed(N, wl, wr, d, causal, g)
+
+
+def test_etc_count_pairs(lib):
+    for L, G, r in [(6, 2, 1), (4, 3, 0), (4096, 256, 84), (100, 7, 200)]:
+        assert lg.etc_count_pairs(L, G, r) == lg_oracle.etc_count_pairs(L, G, r)
+        assert lg.etc_count_pairs(L, G, r) == int(lg_oracle.etc_mask(L, G, r).sum()) or L > 1000
+
+
+def test_count_pairs_rejects_bad_lists(lib):
+    with pytest.raises(ValueError):
+        lg.count_pairs(10, 1, 1, 1, False, [3, 3])
+    with pytest.raises(ValueError):
+        lg.count_pairs(10, 1, 1, 1, False, [11])

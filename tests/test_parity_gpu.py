@@ -1,0 +1,142 @@
+"""CUDA path against the CPU oracle on the same seeded inputs (needs a GB300).
+
+Small cases compare every output element (several tiles plus a ragged tail,
+every edge case the method has); the full-size workloads compare sampled rows
+that the oracle computes one by one, in the same launch configuration the
+benchmark times.  Tolerances: fp32 max |dO| <= 1e-5; bf16 max |dO| <= 2e-2 and
+mean |dO| <= 2e-3; |dLSE| <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_long_sequence_window_gb300 import workloads
+from sparse_long_sequence_window_gb300.workloads import Workload
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def W(name, dtype, B, H, N, D, wl, wr, dil=(), causal=False, g=None, nrand=0, seed=100, **kw):
+    return Workload(name, dtype, B, H, N, D, wl, wr, tuple(dil), causal, g, nrand, seed=seed, **kw)
+
+
+# ---------------------------------------------------------------- fp32 path (CUDA cores)
+
+F32_CASES = [
+    W("f32 single token", "f32", 1, 1, 1, 64, 3, 3),
+    W("f32 ragged D=36 window", "f32", 2, 3, 77, 36, 5, 2, (1, 2, 3), False, (0, 40, 76)),
+    W("f32 causal dilated", "f32", 1, 4, 190, 64, 9, 9, (1, 2, 5, 11), True, (3, 100)),
+    W("f32 full window", "f32", 1, 2, 150, 128, 200, 200),
+    W("f32 identity window", "f32", 1, 2, 64, 16, 0, 0, (1, 3)),
+    W("f32 every token global", "f32", 1, 1, 40, 8, 1, 1, (), False, tuple(range(40))),
+]
+
+
+@pytest.mark.parametrize("w", F32_CASES, ids=lambda w: w.name)
+def test_f32_small(cuda_lib, w):
+    pu.run_longformer(cuda_lib, w)
+
+
+def test_f32_tiny_preset(cuda_lib):
+    """fp32 B1 H2 N512 D64, window 64/64, one global token at 0: every element."""
+    pu.run_longformer(cuda_lib, workloads.PRESETS["tiny_f32"])
+
+
+def test_f32_etc_small(cuda_lib):
+    pu.run_etc(cuda_lib, W("f32 etc", "f32", 2, 2, 130, 32, 0, 0, etc_G=9, radius=6))
+
+
+# ---------------------------------------------------------------- bf16 path (tensor cores)
+
+BF16_CASES = [
+    W("bf16 D64 two tiles + tail", "bf16", 1, 2, 300, 64, 16, 16),
+    W("bf16 D128 two tiles + tail", "bf16", 1, 2, 300, 128, 16, 16),
+    W("bf16 single token", "bf16", 1, 1, 1, 64, 4, 4),
+    W("bf16 identity window", "bf16", 1, 2, 200, 64, 0, 0),
+    W("bf16 asymmetric window", "bf16", 2, 2, 700, 64, 100, 37),
+    W("bf16 full window", "bf16", 1, 2, 513, 64, 600, 600),
+    W("bf16 causal D128", "bf16", 1, 2, 777, 128, 200, 50, (), True),
+    W("bf16 dilation 1..4 + globals", "bf16", 1, 4, 1000, 64, 60, 20, (1, 2, 3, 4), False, (0, 5, 999)),
+    W("bf16 dilation 1..8", "bf16", 1, 8, 1500, 64, 40, 40, (1, 2, 3, 4, 5, 6, 7, 8)),
+    W("bf16 dilation 5..8 causal D128", "bf16", 1, 4, 1100, 128, 50, 9, (5, 6, 7, 8), True),
+    W("bf16 130 globals (two tiles)", "bf16", 1, 2, 2000, 64, 64, 64, (), False, None, 130),
+    W("bf16 globals at edges D128", "bf16", 1, 3, 1025, 128, 100, 100, (1, 1, 2), False, (0, 1, 511, 1023, 1024)),
+    W("bf16 causal with globals", "bf16", 1, 2, 600, 64, 64, 64, (1, 3), True, (10, 590)),
+    W("bf16 dilation beyond N", "bf16", 1, 2, 5, 64, 2, 2, (7, 8)),
+    W("bf16 every token global", "bf16", 1, 1, 140, 64, 2, 2, (), False, tuple(range(140))),
+    W("bf16 many heads", "bf16", 3, 16, 257, 64, 30, 30, tuple([1, 2] * 8)),
+]
+
+
+@pytest.mark.parametrize("w", BF16_CASES, ids=lambda w: w.name)
+def test_bf16_small(cuda_lib, w):
+    pu.run_longformer(cuda_lib, w)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_etc_small(cuda_lib, D):
+    pu.run_etc(cuda_lib, W(f"bf16 etc D{D}", "bf16", 2, 2, 700, D, 0, 0, etc_G=70, radius=20))
+
+
+def test_bf16_etc_star(cuda_lib):
+    """ETC with r = 1 and one global token (the star pattern)."""
+    pu.run_etc(cuda_lib, W("bf16 etc star", "bf16", 1, 2, 300, 64, 0, 0, etc_G=1, radius=1))
+
+
+# ---------------------------------------------------------------- the reference workloads at full size
+
+def test_longformer_base_full(cuda_lib):
+    """bf16 B1 H12 N4096 D64, window 256/256, globals 0..64: every element."""
+    pu.run_longformer(cuda_lib, workloads.PRESETS["longformer_base"])
+
+
+def test_etc_base_sampled(cuda_lib):
+    """bf16 ETC B2 H12 L4096 G256 D64 r84: every global row and sampled long rows."""
+    w = workloads.PRESETS["etc_base"]
+    pu.run_etc(cuda_lib, w, pu.sample_rows(w.N, n_random=64, seed=3))
+
+
+def test_charlm_dilated_sampled(cuda_lib):
+    """bf16 B1 H8 N16384 D64 causal wl 512, dilation [1,1,2,2,3,3,4,4]: sampled rows."""
+    w = workloads.PRESETS["charlm_dilated"]
+    pu.run_longformer(cuda_lib, w, pu.sample_rows(w.N, dilations=(1, 2, 3, 4), n_random=64, seed=4))
+
+
+@pytest.mark.parametrize("preset", ["long_8k", "long_32k", "long_128k"])
+def test_long_scale_sampled(cuda_lib, preset):
+    """bf16 B1 H16 D128, window 512/512, 128 random globals: sampled rows incl. global rows."""
+    w = workloads.PRESETS[preset]
+    g = workloads.global_positions(w)
+    pu.run_longformer(cuda_lib, w, pu.sample_rows(w.N, globals_=g.tolist(), n_random=40, seed=5))
+
+
+# ---------------------------------------------------------------- device-side status
+
+def test_bad_global_list_reports_status(cuda_lib):
+    lg = cuda_lib
+    dev = torch.device("cuda")
+    q = torch.randn(1, 2, 300, 64, device=dev).to(torch.bfloat16)
+    for bad in ([5, 3], [0, 300], [-1, 4], [7, 7]):
+        gidx = torch.tensor(bad, dtype=torch.int32, device=dev)
+        lg.attn_fwd(q, q, q, 8, 8, None, False, gidx)
+        assert lg.query_status(lg.attn_fwd.last_workspace) == lg.LG_ERR_GLOBAL_IDX
+    # a good call on the same workspace reports OK again
+    gidx = torch.tensor([3, 5], dtype=torch.int32, device=dev)
+    ws = lg.attn_fwd.last_workspace
+    lg.attn_fwd(q, q, q, 8, 8, None, False, gidx, workspace=ws)
+    assert lg.query_status(ws) == 0
+
+
+def test_repeat_calls_are_deterministic(cuda_lib):
+    lg = cuda_lib
+    w = W("repeat", "bf16", 1, 4, 1200, 128, 128, 128, (1, 2, 1, 3), False, (0, 600))
+    inp = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    g = torch.from_numpy(inp["global_idx"]).to(dev)
+    o1, l1 = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, g)
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2 = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, g)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
