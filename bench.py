@@ -180,6 +180,23 @@ def launches_per_call(w):
     return groups + (2 if has_g else 0)
 
 
+# ---------------------------------------------------------------------- rank bookkeeping
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The maximum of `value` over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica, timed by the slowest rank."""
+    return flops_per_step * steps * world / (max_ms / 1e3) / 1e12
+
+
 # ---------------------------------------------------------------------- native arm
 
 def time_steps(torch, f, steps, flush):
@@ -240,12 +257,8 @@ def run_native(args, rank, world):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = float(sum(step_ms))
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = flops * args.steps * world / (total_ms / 1e3) / 1e12
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
+    value = job_throughput(flops, args.steps, world, total_ms)
 
     # ---- end to end through the public API: pinned host inputs -> device -> call -> host outputs
     e2e = None
@@ -268,12 +281,8 @@ def run_native(args, rank, world):
         b.record(stream)
         b.synchronize()
         e_times.append(a.elapsed_time(b))
-    e_ms = float(sum(e_times))
-    if dist:
-        tt = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms = float(tt.item())
-    e2e = {"value": flops * e2e_steps * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    e_ms = max_over_ranks(float(sum(e_times)), dist, dev)
+    e2e = {"value": job_throughput(flops, e2e_steps, world, e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     # ---- roofline of the dominant kernel (the tensor-core attention kernel does every useful FLOP)
