@@ -113,6 +113,33 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       const int32_t* global_idx, int n_global, float scale,
                       void* workspace, size_t workspace_bytes, lg_stream_t stream);
 
+/*
+ * lg_attn_fwd without a caller-supplied workspace.  (Not a step of the
+ * method: the paper has no counterpart; this exists for integration.)
+ *
+ * For callers that cannot allocate device memory while they run, e.g. code
+ * inside a host framework that plans all device memory up front, or a process
+ * whose GPU memory is already held by another allocator.  The scratch space
+ * comes from one fixed array of LG_NOALLOC_SCRATCH_BYTES inside the library;
+ * each GPU this is used on keeps that array until the process exits.
+ *
+ * Arguments are those of lg_attn_fwd minus the workspace.  The caller still
+ * owns and passes inputs and outputs.  Returns LG_ERR_WORKSPACE, before any
+ * CUDA call, when lg_attn_fwd_workspace_size(...) exceeds the fixed size
+ * (for bf16 with global tokens the scratch grows with B*H*g*N/2048).  The
+ * first call on a device looks up the array's device address (once, with
+ * that device current); make it before any stream capture.  All calls share
+ * the one array: calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.  Device-side status
+ * (lg_query_status) is not available through this entry point.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+#define LG_NOALLOC_SCRATCH_BYTES (16u << 20)
+lg_status lg_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                              lg_dtype dt, int B, int H, int N, int D,
+                              int w_left, int w_right, const int32_t* dilation, int causal,
+                              const int32_t* global_idx, int n_global, float scale, lg_stream_t stream);
+
 /* Bytes of device workspace lg_etc_attn_fwd needs; 0 if the sizes are invalid. */
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt);
 
