@@ -64,18 +64,21 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int rows, int BH, int d
   return r == CUDA_SUCCESS;
 }
 
-// Band work units of one head: query tiles of 128 steps in each residue class.
+// Band work units of one head: pairs of 128-step query tiles in each residue class.
 int band_units_for(int N, int d) {
   int units = 0;
   for (int c = 0; c < d && c < N; ++c) {
     const int n_c = (N - c + d - 1) / d;
-    units += cdiv(n_c, kTileM);
+    units += cdiv(n_c, 2 * kTileM);
   }
   return units;
 }
 
+// Global-query rows: 128-row tiles against splits of kGrowSplitTiles key
+// tiles; the two warpgroups of a unit take alternate key tiles, so each split
+// leaves two partial slots per row.
 struct GrowPlan {
-  int n_gtiles = 0, n_key_tiles = 0, n_splits = 0;
+  int n_gtiles = 0, n_key_tiles = 0, n_splits = 0, n_parts = 0;
 };
 
 GrowPlan grow_plan(int n_glob, int key_tiles) {
@@ -83,7 +86,8 @@ GrowPlan grow_plan(int n_glob, int key_tiles) {
   if (n_glob <= 0) return g;
   g.n_gtiles = cdiv(n_glob, kTileM);
   g.n_key_tiles = key_tiles;
-  g.n_splits = cdiv(key_tiles, kSplitTiles);
+  g.n_splits = cdiv(key_tiles, kGrowSplitTiles);
+  g.n_parts = 2 * g.n_splits;
   return g;
 }
 
@@ -173,14 +177,14 @@ size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_d
   if (B < 1 || H < 1 || N < 1 || D < 1 || n_global < 0 || n_global > N || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(n_global, cdiv(N, kTileN));
-  return ws_layout(B * H, n_global, D, g.n_splits, true).total;
+  return ws_layout(B * H, n_global, D, g.n_parts, true).total;
 }
 
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || G < 1 || D < 1 || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  return ws_layout(B * H, G, D, g.n_splits, false).total;
+  return ws_layout(B * H, G, D, g.n_parts, false).total;
 }
 
 lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
@@ -236,7 +240,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   // ---- bf16 tensor-core path
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(n_global, cdiv(N, kTileN));
-  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_splits, true);
+  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true);
   __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(ws + lay.qg);
   __nv_bfloat16* kg = reinterpret_cast<__nv_bfloat16*>(ws + lay.kg);
   __nv_bfloat16* vg = reinterpret_cast<__nv_bfloat16*>(ws + lay.vg);
@@ -300,7 +304,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.gidx = global_idx; tp.status = status; tp.wait_cap = wait_cap_cycles();
     tp.scale_log2 = s * 1.4426950408889634f;
     tp.BH = BH; tp.H = H; tp.N = N; tp.D = D; tp.wl = wl; tp.wr = wr; tp.n_glob = n_global; tp.etc = 0;
-    tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_key_tiles_grow = gp.n_key_tiles;
+    tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
+    tp.n_key_tiles_grow = gp.n_key_tiles;
     tp.n_grow_units = (grp == 0 && n_global > 0) ? BH * gp.n_gtiles * gp.n_splits : 0;
     const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
     if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
@@ -313,7 +318,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     mp.part_acc = reinterpret_cast<const float*>(ws + lay.acc);
     mp.part_ml = reinterpret_cast<const float*>(ws + lay.ml);
     mp.out = out; mp.lse = lse; mp.gidx = global_idx;
-    mp.BH = BH; mp.N_out = N; mp.D = D; mp.n_glob = n_global; mp.n_splits = gp.n_splits;
+    mp.BH = BH; mp.N_out = N; mp.D = D; mp.n_glob = n_global; mp.n_splits = gp.n_parts;
     if ((e = launch_merge(mp, 1, stream)) != cudaSuccess) return LG_ERR_CUDA;
   }
   return LG_OK;
@@ -358,7 +363,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
 
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  const WsLayout lay = ws_layout(BH, G, D, gp.n_splits, false);
+  const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false);
   static TcParams tp;
   tp = TcParams{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
@@ -382,7 +387,8 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.gidx = nullptr; tp.status = status; tp.wait_cap = wait_cap_cycles();
   tp.scale_log2 = s * 1.4426950408889634f;
   tp.BH = BH; tp.H = H; tp.N = L; tp.D = D; tp.wl = r; tp.wr = r; tp.n_glob = G; tp.etc = 1;
-  tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_key_tiles_grow = gp.n_key_tiles;
+  tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
+    tp.n_key_tiles_grow = gp.n_key_tiles;
   tp.n_grow_units = BH * gp.n_gtiles * gp.n_splits;
   const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * tp.band_units_per_batch;
   if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
@@ -393,7 +399,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   mp.part_acc = reinterpret_cast<const float*>(ws + lay.acc);
   mp.part_ml = reinterpret_cast<const float*>(ws + lay.ml);
   mp.out = out_g; mp.lse = lse_g; mp.gidx = nullptr;
-  mp.BH = BH; mp.N_out = G; mp.D = D; mp.n_glob = G; mp.n_splits = gp.n_splits;
+  mp.BH = BH; mp.N_out = G; mp.D = D; mp.n_glob = G; mp.n_splits = gp.n_parts;
   if ((e = launch_merge(mp, 1, stream)) != cudaSuccess) return LG_ERR_CUDA;
   return LG_OK;
 }

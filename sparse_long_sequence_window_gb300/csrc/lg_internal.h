@@ -21,7 +21,7 @@ enum : int {
 constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace
 constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;              // keys per tile
-constexpr int kSplitTiles = 16;          // key tiles per split of a global-query row block
+constexpr int kGrowSplitTiles = 32;      // key tiles per split of a global-query row block (two partials)
 constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
 
 // ---------------------------------------------------------------- fp32 CUDA-core path
@@ -52,8 +52,8 @@ struct TcParams {
   CUtensorMap mapQg, mapKg, mapVg;  // global side {D, g, BH}: gathered rows (Longformer) or q_g/k_g/v_g (ETC)
   void* out;                      // bf16 [BH, N, D]
   float* lse;                     // [BH, N]
-  float* part_acc;                // [BH, n_glob, n_splits, D] unnormalised partial outputs
-  float* part_ml;                 // [BH, n_glob, n_splits, 2] partial (max, sum), max in log2 units
+  float* part_acc;                // [BH, n_glob, n_parts, D] unnormalised partial outputs
+  float* part_ml;                 // [BH, n_glob, n_parts, 2] partial (max, sum), max in log2 units
   const int* gidx;                // Longformer global positions (device), for band de-duplication
   int* status;
   long long wait_cap;             // clock64 cycles a bounded wait may spin
@@ -65,6 +65,7 @@ struct TcParams {
   int n_grow_units;               // global-query row units (placed first)
   int n_gtiles;                   // query tiles of the global rows
   int n_splits;                   // key splits of the global rows
+  int n_parts;                    // partial slots per global row (two per split)
   int n_key_tiles_grow;           // key tiles of one global row block (ETC: ceil(G/128) + ceil(L/128))
   int band_units_per_batch;
   int slot_dil[kMaxSlots];

@@ -7,45 +7,58 @@
 // "ETC: Encoding Long and Structured Inputs in Transformers", section 3.4
 // ("Global-Local Attention", "Softmax unification").
 //
-// One CTA handles one work unit: 128 query rows against a list of 128-key
-// tiles.
-//  * Band unit: the query rows t0..t0+127 of one dilation residue class
-//    c (positions c + d*t).  Inside a class the dilated window is the
-//    contiguous step range [t - w_left, t + w_right], so the key tiles are the
-//    contiguous class rows that intersect it; the strided rows are fetched by
+// One CTA handles one work unit with two 128-row query tiles (q = 0, 1), each
+// owned by its own softmax warpgroup, against a list of 128-key tiles:
+//  * Band unit: query steps t0 .. t0+255 of one dilation residue class c
+//    (positions c + d*t).  Inside a class the dilated window is the contiguous
+//    step range [t - w_left, t + w_right]; the key tiles are the contiguous
+//    class rows intersecting the union of the two tiles' windows, fetched by
 //    TMA with an element stride of d along the row dimension (the dilation is
-//    folded into the TMA coordinates).  The global-key tiles follow; a global
-//    key that is already in a row's band is masked there (counted once).
-//  * Global-row unit: 128 global queries against one split of all keys.  It
-//    writes partial softmax statistics that a merge kernel combines.
-// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs (one thread), warps 4..7 run the online softmax: one thread
-// per query row, fp32 row max and row sum, exp2 of log2-scaled logits.
-// S = Q K^T lands in TMEM (two 128-column buffers), P is written to shared
-// memory as bf16 in the 128-byte swizzled K-major layout, and O += P V
-// accumulates in TMEM (D columns).
+//    folded into the TMA coordinates).  Each K/V tile is loaded once and used
+//    by both query tiles (a query tile skips tiles outside its own windows).
+//    The global-key tiles follow; a global key already inside a row's band is
+//    masked there (it counts once).
+//  * Global-row unit: 128 global queries against one split of all keys; the
+//    two warpgroups take alternate key tiles and each writes partial softmax
+//    statistics that a merge kernel combines.
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (one thread), warps 4..7 and 8..11 are the two softmax
+// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128
+// fp32 columns, reused for P_q as packed bf16) and O_q (D columns) for both
+// tiles.  The MMA order per key tile j is PV_0(j-1), QK_0(j), PV_1(j-1),
+// QK_1(j), so the tensor core works on one tile while the other tile's
+// softmax runs.  Because tcgen05 MMAs of one thread execute in order, the
+// completion of QK_q(j) also means PV_q(j-1) is done: the softmax may then
+// rescale O_q and overwrite S_q with P_q without further waits.
 #include "lg_internal.h"
 #include "lg_ptx.cuh"
 
 namespace lg {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+// Register split between the warpgroups (setmaxnreg): the producer/MMA
+// warpgroup gives registers to the two softmax warpgroups.  The launch holds
+// kThreads x (registers per thread at launch); the split must fit in it.
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsLaunchMin = (128 * kRegsControl + 256 * kRegsSoftmax + kThreads - 1) / kThreads;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only when the max grows more
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kTileM * D * 2;      // 128 rows x D bf16
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kPBytes = kTileM * kTileN * 2;    // 128 x 128 bf16
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffMisc = kOffP + kPBytes;
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 4 : 2;
+  static constexpr int kOffQ = 0;                        // two query tiles
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffMisc = kOffV + kVStages * kTileBytes;
   static constexpr int kMiscBytes = 1024;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
+  static constexpr uint32_t kColS = 0;                   // S_q at q * 128
+  static constexpr uint32_t kColO = 256;                 // O_q at 256 + q * D
 };
 
 // Rows one strided TMA box delivers for a dilation d (box height R*d <= 256).
@@ -57,13 +70,14 @@ struct Unit {
   int grow;          // 1: global-row unit, 0: band unit
   int bh;
   int slot, d, c;    // band: dilation slot, stride, residue class
-  int t0, n_c;       // band: first query step, class length
+  int t0, n_c;       // band: first query step of tile 0, class length
   int band_lo;       // band: first key step of the tiles
   int n_band;        // band: band key tiles
-  int n_gt;          // band: appended global-key tiles
   int kt0;           // grow: first key tile of the split
   int grow0;         // grow: first global row of the tile
   int n_tiles;
+  int first[2], last[2];  // band: range of band tiles each query tile needs (first > last: none)
+  int active[2];
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
@@ -74,9 +88,10 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     const int r = u / p.n_splits;
     w.grow0 = (r % p.n_gtiles) * kTileM;
     w.bh = r / p.n_gtiles;
-    w.kt0 = split * kSplitTiles;
-    w.n_tiles = min(kSplitTiles, p.n_key_tiles_grow - w.kt0);
+    w.kt0 = split * kGrowSplitTiles;
+    w.n_tiles = min(kGrowSplitTiles, p.n_key_tiles_grow - w.kt0);
     w.slot = 0; w.d = 1;
+    w.active[0] = 1; w.active[1] = w.n_tiles > 1;
     return w;
   }
   const int v = u - p.n_grow_units;
@@ -91,22 +106,46 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   w.d = p.slot_dil[w.slot];
   for (int c = 0; c < w.d; ++c) {
     const int n_c = (p.N - c + w.d - 1) / w.d;
-    const int tiles = (n_c + kTileM - 1) / kTileM;
-    if (rem < tiles) { w.c = c; w.n_c = n_c; w.t0 = rem * kTileM; break; }
-    rem -= tiles;
+    const int units = (n_c + 2 * kTileM - 1) / (2 * kTileM);
+    if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
+    rem -= units;
   }
   if (w.n_c <= 0) { w.n_tiles = 0; return w; }
-  const int t_last = min(w.t0 + kTileM - 1, w.n_c - 1);
+  const int t_last = min(w.t0 + 2 * kTileM - 1, w.n_c - 1);
   w.band_lo = max(0, w.t0 - p.wl);
   const int band_hi = min(w.n_c - 1, t_last + p.wr);
   w.n_band = (band_hi - w.band_lo + kTileN) / kTileN;
-  w.n_gt = (p.n_glob + kTileN - 1) / kTileN;
-  w.n_tiles = w.n_band + w.n_gt;
+  const int n_gt = (p.n_glob + kTileN - 1) / kTileN;
+  w.n_tiles = w.n_band + n_gt;
+  for (int q = 0; q < 2; ++q) {
+    const int a = w.t0 + q * kTileM;
+    w.active[q] = a < w.n_c;
+    if (!w.active[q]) { w.first[q] = 1; w.last[q] = 0; continue; }
+    const int b_ = min(a + kTileM - 1, w.n_c - 1);
+    const int klo = max(0, a - p.wl), khi = min(w.n_c - 1, b_ + p.wr);
+    w.first[q] = (klo - w.band_lo) / kTileN;
+    w.last[q] = (khi - w.band_lo) / kTileN;
+  }
   return w;
 }
 
-// Issues the TMA loads of one 128-row operand tile.  main == true: the
-// dilation-strided view of the slot; otherwise the global-side view.
+// Does query tile q work on key tile j?
+__device__ __forceinline__ bool uses(const Unit& w, int q, int j) {
+  if (w.grow) return (j & 1) == q;
+  if (!w.active[q]) return false;
+  if (j >= w.n_band) return true;  // global-key tiles
+  return j >= w.first[q] && j <= w.last[q];
+}
+
+// Last key tile query tile q works on (-1: none).
+__device__ __forceinline__ int last_use(const Unit& w, int q) {
+  for (int j = w.n_tiles - 1; j >= 0; --j)
+    if (uses(w, q, j)) return j;
+  return -1;
+}
+
+// Issues the TMA loads of one 128-row operand tile.  strided: the
+// dilation-strided view of a slot; otherwise a plain view.
 template <int D>
 __device__ __forceinline__ void load_tile(const CUtensorMap* map, bool strided, int d, int y0, int bh,
                                           uint32_t dst, uint32_t bar) {
@@ -120,6 +159,9 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, bool strided, 
   }
 }
 
+// Column of the 128-wide tile whose exp2 goes to the FMA pipe (one in four).
+__host__ __device__ constexpr bool poly_col(int col) { return (col & 15) >= 12; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<D>;
@@ -127,15 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV,
-                 sP = sbase + C::kOffP;
+  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
   unsigned char* misc = smem + C::kOffMisc;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
-  // barrier indices
-  constexpr int S = C::kStages;
-  const int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + S, B_VFULL = 1 + 2 * S, B_VEMPTY = 1 + 3 * S,
-            B_SFULL = 1 + 4 * S, B_SFREE = 3 + 4 * S, B_PFULL = 5 + 4 * S, B_PVDONE = 6 + 4 * S,
-            B_FIN = 7 + 4 * S, NBARS = 8 + 4 * S;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
+  constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + KS, B_VFULL = 1 + 2 * KS,
+                B_VEMPTY = 1 + 2 * KS + VS, B_SFULL = 1 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
+                B_ODONE = B_PFULL + 2, B_FIN = B_ODONE + 2, NBARS = B_FIN + 1;
+  static_assert(NBARS * 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
@@ -145,8 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
-      uint32_t count = 1;
-      if (i == B_SFREE || i == B_SFREE + 1 || i == B_PFULL) count = 128;
+      const uint32_t count = (i == B_PFULL || i == B_PFULL + 1) ? 128 : 1;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -163,26 +203,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   const Unit w = decode_unit(p, blockIdx.x);
   const int T = w.n_tiles;
   const long long cap = p.wait_cap;
+  const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
 
   auto fail = [&]() {
     *abort_flag = 1;
     atomicOr(p.status, ST_TIMEOUT);
   };
 
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued_k = 0, issued_v = 0;
-      mbar_arrive_expect_tx(bar(B_QFULL), C::kTileBytes);
       if (w.grow) {
+        mbar_arrive_expect_tx(bar(B_QFULL), C::kTileBytes);
         load_tile<D>(&p.mapQg, false, 1, w.grow0, w.bh, sQ, bar(B_QFULL));
       } else {
+        mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
         load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * w.t0, w.bh, sQ, bar(B_QFULL));
+        load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * (w.t0 + kTileM), w.bh, sQ + C::kTileBytes,
+                     bar(B_QFULL));
       }
-      const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
       for (int j = 0; j < T; ++j) {
-        const int st = j % S;
-        // which view and row coordinate holds key tile j
         const CUtensorMap *mk, *mv;
         bool strided;
         int y;
@@ -203,78 +246,96 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
             y = (kt - (p.etc ? gt_src : 0)) * kTileN;
           }
         }
-        if (j >= S && !mbar_wait(bar(B_KEMPTY + st), ((j / S) - 1) & 1, abort_flag, cap)) { fail(); break; }
-        mbar_arrive_expect_tx(bar(B_KFULL + st), C::kTileBytes);
-        load_tile<D>(mk, strided, strided ? w.d : 1, y, w.bh, sK + st * C::kTileBytes, bar(B_KFULL + st));
+        const int ks = j % KS, vs = j % VS;
+        if (j >= KS && !mbar_wait(bar(B_KEMPTY + ks), ((j / KS) - 1) & 1, abort_flag, cap)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(B_KFULL + ks), C::kTileBytes);
+        load_tile<D>(mk, strided, strided ? w.d : 1, y, w.bh, sK + ks * C::kTileBytes, bar(B_KFULL + ks));
         issued_k = j + 1;
-        if (j >= S && !mbar_wait(bar(B_VEMPTY + st), ((j / S) - 1) & 1, abort_flag, cap)) { fail(); break; }
-        mbar_arrive_expect_tx(bar(B_VFULL + st), C::kTileBytes);
-        load_tile<D>(mv, strided, strided ? w.d : 1, y, w.bh, sV + st * C::kTileBytes, bar(B_VFULL + st));
+        if (j >= VS && !mbar_wait(bar(B_VEMPTY + vs), ((j / VS) - 1) & 1, abort_flag, cap)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(B_VFULL + vs), C::kTileBytes);
+        load_tile<D>(mv, strided, strided ? w.d : 1, y, w.bh, sV + vs * C::kTileBytes, bar(B_VFULL + vs));
         issued_v = j + 1;
       }
       // Drain: every load issued here has landed before the CTA exits (these
       // waits ignore the abort flag and are bounded by the cap alone).
       mbar_wait(bar(B_QFULL), 0, nullptr, cap);
-      for (int j = max(0, issued_k - S); j < issued_k; ++j)
-        mbar_wait(bar(B_KFULL + j % S), (j / S) & 1, nullptr, cap);
-      for (int j = max(0, issued_v - S); j < issued_v; ++j)
-        mbar_wait(bar(B_VFULL + j % S), (j / S) & 1, nullptr, cap);
+      for (int j = max(0, issued_k - KS); j < issued_k; ++j)
+        mbar_wait(bar(B_KFULL + j % KS), (j / KS) & 1, nullptr, cap);
+      for (int j = max(0, issued_v - VS); j < issued_v; ++j)
+        mbar_wait(bar(B_VFULL + j % VS), (j / VS) & 1, nullptr, cap);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      const uint32_t tO = tmem + 256;
+      const int lastq[2] = {last_use(w, 0), last_use(w, 1)};
+      int pending[2] = {-1, -1};
+      int n_pv[2] = {0, 0};
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, cap);
       if (!ok) fail();
-      auto issue_pv = [&](int jj) -> bool {
-        const int st = jj % S;
-        if (!mbar_wait(bar(B_PFULL), jj & 1, abort_flag, cap)) return false;
-        if (!mbar_wait(bar(B_VFULL + st), (jj / S) & 1, abort_flag, cap)) return false;
+      // O_q += P_q V_jj, P_q read from TMEM (the S_q columns).
+      auto issue_pv = [&](int q) -> bool {
+        const int jj = pending[q];
+        const int vs = jj % VS;
+        if (!mbar_wait(bar(B_PFULL + q), n_pv[q] & 1, abort_flag, cap)) return false;
+        if (!mbar_wait(bar(B_VFULL + vs), (jj / VS) & 1, abort_flag, cap)) return false;
         tc_fence_after();
-        const uint32_t vbase = sV + st * C::kTileBytes;
+        const uint32_t vbase = sV + vs * C::kTileBytes;
+        const uint32_t tP = tmem + C::kColS + q * 128;
+        const uint32_t tO = tmem + C::kColO + q * D;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sP + (kk >> 2) * (kTileM * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kTileN * 128, 1024);
-          umma_bf16_ss(tO, a, b, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tO, tP + kk * 8, b, idesc_pv, (n_pv[q] > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_PVDONE));
-        umma_commit(bar(B_VEMPTY + st));
+        ++n_pv[q];
+        if (jj == lastq[q]) umma_commit(bar(B_ODONE + q));
+        if (q == 1 || !uses(w, 1, jj)) umma_commit(bar(B_VEMPTY + vs));  // last reader of V_jj
+        pending[q] = -1;
         return true;
       };
       for (int j = 0; j < T && ok; ++j) {
-        const int st = j % S;
-        const int sb = j & 1;
-        if (!mbar_wait(bar(B_KFULL + st), (j / S) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-        if (j >= 2 && !mbar_wait(bar(B_SFREE + sb), ((j >> 1) - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-        tc_fence_after();
-        const uint32_t kbase = sK + st * C::kTileBytes;
+        const int ks = j % KS;
+        if (!mbar_wait(bar(B_KFULL + ks), (j / KS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+        const uint32_t kbase = sK + ks * C::kTileBytes;
+        for (int q = 0; q < 2 && ok; ++q) {
+          if (pending[q] >= 0 && !issue_pv(q)) { fail(); ok = false; break; }
+          if (!uses(w, q, j)) continue;
+          tc_fence_after();
+          const uint32_t qbase = sQ + (w.grow ? 0 : q * C::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
-          umma_bf16_ss(tmem + sb * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                       idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::kColS + q * 128, sdesc_sw128(qbase + off, 16, 1024),
+                         sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(B_SFULL + q));
+          pending[q] = j;
         }
-        umma_commit(bar(B_SFULL + sb));
-        umma_commit(bar(B_KEMPTY + st));
-        if (j >= 1 && !issue_pv(j - 1)) { fail(); ok = false; break; }
+        if (ok) umma_commit(bar(B_KEMPTY + ks));
       }
-      if (ok && T > 0 && !issue_pv(T - 1)) { fail(); ok = false; }
+      for (int q = 0; q < 2 && ok; ++q)
+        if (pending[q] >= 0 && !issue_pv(q)) { fail(); ok = false; }
       // Every MMA issued here has completed before TMEM is released.
       umma_commit(bar(B_FIN));
       mbar_wait(bar(B_FIN), 0, nullptr, cap);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = threadIdx.x - 128;                    // query row in the tile == TMEM lane
+    const int q = (warp - 4) >> 2;                      // query tile of this warpgroup
+    const int r = threadIdx.x & 127;                    // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int t_q = w.t0 + r;                           // band: query step in the class
+    const uint32_t tS = tmem + lane_off + C::kColS + q * 128;
+    const uint32_t tO = tmem + lane_off + C::kColO + q * D;
+    const int t_q = w.t0 + q * kTileM + r;              // band: query step in the class
     const int pos_q = w.c + w.d * t_q;                  // band: query position
     const bool row_valid = w.grow ? (w.grow0 + r < p.n_glob) : (t_q < w.n_c);
-    const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
-    float m_run = -INFINITY, l_run = 0.f;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;               // m_run in log2 units of the scaled logits
+    int n_done = 0;
     bool ok = true;
     // Every lane of a warp takes the same decision, so the warp-collective
     // tcgen05.ld/st and votes below always run converged.
@@ -283,10 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       return __all_sync(0xffffffffu, got);
     };
     for (int j = 0; j < T; ++j) {
-      const int sb = j & 1;
-      // Column window [lo, hi] of allowed keys for band tiles, and the tile kind.
+      if (!uses(w, q, j)) continue;
+      // Allowed columns: [lo, hi] (band and plain tiles), or the global-key
+      // de-duplication test (Longformer global tiles).
       int lo = 0, hi = kTileN - 1;
-      int kind = 0;  // 0: [lo, hi] range, 1: global-key tile with de-duplication (Longformer)
+      bool dedup = false;
       int jj0 = 0;
       if (!w.grow) {
         if (j < w.n_band) {
@@ -296,32 +358,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         } else {
           jj0 = (j - w.n_band) * kTileN;
           hi = min(kTileN, p.n_glob - jj0) - 1;
-          if (!p.etc) kind = 1;
+          dedup = !p.etc;
         }
       } else {
         const int kt = w.kt0 + j;
-        int limit;
-        if (p.etc && kt < gt_src) limit = p.n_glob - kt * kTileN;
-        else limit = p.N - (kt - (p.etc ? gt_src : 0)) * kTileN;
+        const int limit = (p.etc && kt < gt_src) ? p.n_glob - kt * kTileN
+                                                 : p.N - (kt - (p.etc ? gt_src : 0)) * kTileN;
         hi = min(kTileN, limit) - 1;
       }
-      if (!wait_all(bar(B_SFULL + sb), (j >> 1) & 1)) { fail(); ok = false; break; }
+      const bool need_mask = __any_sync(0xffffffffu, dedup || lo > 0 || hi < kTileN - 1);
+
+      if (!wait_all(bar(B_SFULL + q), n_done & 1)) { fail(); ok = false; break; }
       tc_fence_after();
       float s[kTileN];
-#pragma unroll
-      for (int cc = 0; cc < kTileN / 32; ++cc) {
-        float* dst = s + cc * 32;
-        tmem_ld32(tmem + lane_off + sb * 128 + cc * 32, *reinterpret_cast<float(*)[32]>(dst));
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE + sb));
+      tmem_ld128(tS, s);
 
       float tmax = -INFINITY;
-      if (kind == 0) {
+      if (!need_mask) {
+#pragma unroll
+        for (int col = 0; col < kTileN; ++col) tmax = fmaxf(tmax, s[col]);
+      } else if (!dedup) {
 #pragma unroll
         for (int col = 0; col < kTileN; ++col) {
-          const bool ok_col = (col >= lo) && (col <= hi);
-          s[col] = ok_col ? s[col] * p.scale_log2 : -INFINITY;
+          s[col] = (col >= lo && col <= hi) ? s[col] : -INFINITY;
           tmax = fmaxf(tmax, s[col]);
         }
       } else {
@@ -336,56 +395,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
               if (tt >= -p.wl && tt <= p.wr) ok_col = false;  // already counted in the band
             }
           }
-          s[col] = ok_col ? s[col] * p.scale_log2 : -INFINITY;
+          s[col] = ok_col ? s[col] : -INFINITY;
           tmax = fmaxf(tmax, s[col]);
         }
       }
+      const float tmax2 = tmax * sl2;                   // log2 units (scale > 0 keeps the order)
       const float m_prev = m_run;
       float m_new = m_prev;
-      if (tmax > m_prev + kRescaleThreshold) m_new = tmax;
+      if (tmax2 > m_prev + kRescaleThreshold) m_new = tmax2;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float corr = ex2_approx(m_prev - m_use);
-      const bool need_rescale = (j > 0) && (m_prev != -INFINITY) && (m_new != m_prev);
+      const bool need_rescale = (m_prev != -INFINITY) && (m_new != m_prev);
       uint32_t pk[kTileN / 2];
-      float psum = 0.f;
+      float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
       for (int i = 0; i < kTileN / 2; ++i) {
-        const float p0 = ex2_approx(s[2 * i] - m_use);
-        const float p1 = ex2_approx(s[2 * i + 1] - m_use);
-        psum += p0 + p1;
+        const float x0 = fmaf(s[2 * i], sl2, -m_use);
+        const float x1 = fmaf(s[2 * i + 1], sl2, -m_use);
+        const float p0 = poly_col(2 * i) ? exp2_poly(x0) : ex2_approx(x0);
+        const float p1 = poly_col(2 * i + 1) ? exp2_poly(x1) : ex2_approx(x1);
+        psum0 += p0;
+        psum1 += p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l_run = l_run * corr + psum;
+      l_run = l_run * corr + (psum0 + psum1);
       m_run = m_new;
-      if (j > 0) {
-        if (!wait_all(bar(B_PVDONE), (j - 1) & 1)) { fail(); ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need_rescale)) {
-          const float f = need_rescale ? corr : 1.f;
+      // O_q is idle here: PV_q of the previous tile finished before QK_q of
+      // this one (same issuing thread, in order), and PV_q of this tile waits
+      // for P_q below.
+      if (__any_sync(0xffffffffu, need_rescale)) {
+        const float f = need_rescale ? corr : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float o[32];
-            tmem_ld32(tmem + lane_off + 256 + cc * 32, o);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
-            tmem_st32(tmem + lane_off + 256 + cc * 32, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st32(tO + cc * 32, o);
         }
       }
-      // P (bf16) into the 128-byte swizzled K-major tile: two 64-key blocks.
-#pragma unroll
-      for (int q = 0; q < kTileN / 8; ++q) {
-        const uint32_t addr = sP + (q >> 3) * (kTileM * 128) + r * 128 + (((q & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
-                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      tmem_st64(tS, pk);                                 // P_q over the first 64 columns of S_q
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + q));
+      ++n_done;
     }
-    if (ok && T > 0) {
-      if (!wait_all(bar(B_PVDONE), (T - 1) & 1)) {
+    if (ok && n_done > 0) {
+      if (!wait_all(bar(B_ODONE + q), 0)) {
         fail();
       } else {
         tc_fence_after();
@@ -396,38 +451,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             float o[32];
-            tmem_ld32(tmem + lane_off + 256 + cc * 32, o);
+            tmem_ld32(tO + cc * 32, o);
             if (row_valid) {
               uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int k = 0; k < 4; ++k) {
                 uint4 val;
-                val.x = pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-                val.y = pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-                val.z = pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-                val.w = pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
-                dst[q] = val;
+                val.x = pack_bf16x2(o[8 * k + 0] * inv_l, o[8 * k + 1] * inv_l);
+                val.y = pack_bf16x2(o[8 * k + 2] * inv_l, o[8 * k + 3] * inv_l);
+                val.z = pack_bf16x2(o[8 * k + 4] * inv_l, o[8 * k + 5] * inv_l);
+                val.w = pack_bf16x2(o[8 * k + 6] * inv_l, o[8 * k + 7] * inv_l);
+                dst[k] = val;
               }
             }
           }
           if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
         } else {
-          const int split = w.kt0 / kSplitTiles;
+          const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;   // partial slot of this warpgroup
           const int grow = w.grow0 + r;
-          const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + grow) * p.n_splits + split;
+          const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + grow) * p.n_parts + slot;
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             float o[32];
-            tmem_ld32(tmem + lane_off + 256 + cc * 32, o);
+            tmem_ld32(tO + cc * 32, o);
             if (row_valid) {
               float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + cc * 32);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+              for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }
           }
           if (row_valid) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
         }
       }
+    } else if (ok && w.grow && row_valid) {
+      // A warpgroup with no key tile in this split leaves an empty partial.
+      const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;
+      const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
+      reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(-INFINITY, 0.f);
     }
   }
 
@@ -443,19 +503,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 
 size_t tc_smem_bytes(int D) { return D == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem; }
 
+// The register split only fits if the kernel launches with at least
+// kRegsLaunchMin registers per thread; refuse to launch otherwise.
+template <int D>
+cudaError_t prepare_kernel() {
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, tc_attn_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (a.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
+  return cudaFuncSetAttribute(tc_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+}
+
 cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
   if (n_units <= 0) return cudaSuccess;
   static bool attr_done[2] = {false, false};
   if (p.D == 64) {
     if (!attr_done[0]) {
-      cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<64>::kSmem);
+      cudaError_t e = prepare_kernel<64>();
       if (e != cudaSuccess) return e;
       attr_done[0] = true;
     }
     tc_attn_kernel<64><<<n_units, kThreads, Cfg<64>::kSmem, s>>>(p);
   } else {
     if (!attr_done[1]) {
-      cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmem);
+      cudaError_t e = prepare_kernel<128>();
       if (e != cudaSuccess) return e;
       attr_done[1] = true;
     }
