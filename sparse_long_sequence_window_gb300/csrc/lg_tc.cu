@@ -46,10 +46,17 @@ constexpr int kRegsLaunchMin = (128 * kRegsControl + 256 * kRegsSoftmax + kThrea
 constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only when the max grows more
 constexpr float kLn2 = 0.6931471805599453f;
 
+#ifndef LG_TC_KSTAGES128
+#define LG_TC_KSTAGES128 3
+#endif
+#ifndef LG_TC_POLY_SHIFT
+#define LG_TC_POLY_SHIFT 0   // one exp2 in 2^shift columns runs on the FMA pipe (0: none)
+#endif
+
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kTileM * D * 2;      // 128 rows x D bf16
-  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kKStages = (D == 64) ? 4 : LG_TC_KSTAGES128;
   static constexpr int kVStages = (D == 64) ? 4 : 2;
   static constexpr int kOffQ = 0;                        // two query tiles
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
@@ -159,8 +166,35 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, bool strided, 
   }
 }
 
-// Column of the 128-wide tile whose exp2 goes to the FMA pipe (one in four).
-__host__ __device__ constexpr bool poly_col(int col) { return (col & 15) >= 12; }
+// Columns of the 128-wide tile whose exp2 goes to the FMA pipe (one in
+// 2^LG_TC_POLY_SHIFT), the rest to the MUFU.
+__host__ __device__ constexpr bool poly_col(int col) {
+  return LG_TC_POLY_SHIFT > 0 && (col & ((1 << LG_TC_POLY_SHIFT) - 1)) == (1 << LG_TC_POLY_SHIFT) - 1;
+}
+
+// Bits of the columns [lo, hi] that fall in the 32-column word starting at `base`.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
+  const int a = max(lo - base, 0), b = min(hi - base, 31);
+  if (a > b) return 0u;
+  const uint32_t upper = (b >= 31) ? 0xFFFFFFFFu : ((1u << (b + 1)) - 1u);
+  return upper & ~((1u << a) - 1u);
+}
+
+// First index in the sorted list g[0..n) whose value is >= x.
+__device__ __forceinline__ int lower_bound_dev(const int* g, int n, long long x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<long long>(__ldg(g + mid)) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ TcParams p) {
@@ -343,22 +377,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const bool got = mbar_wait(b, parity, abort_flag, cap);
       return __all_sync(0xffffffffu, got);
     };
+    // Global keys (Longformer) already inside this row's band are masked in the
+    // global tiles, so they count once.  The global list is sorted, so they
+    // have list indices in [g_a, g_b): the positions in [pos_q - d*w_left,
+    // pos_q + d*w_right]; for d > 1 only those on the row's stride lattice.
+    int g_a = 0, g_b = 0;
+    if (!w.grow && !p.etc && p.n_glob > 0 && row_valid) {
+      g_a = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl);
+      g_b = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1);
+    }
     for (int j = 0; j < T; ++j) {
       if (!uses(w, q, j)) continue;
-      // Allowed columns: [lo, hi] (band and plain tiles), or the global-key
-      // de-duplication test (Longformer global tiles).
+      // Allowed columns of this tile as a 128-bit keep mask.
       int lo = 0, hi = kTileN - 1;
-      bool dedup = false;
-      int jj0 = 0;
+      int jj0 = -1;                                     // first global index of a Longformer global tile
       if (!w.grow) {
         if (j < w.n_band) {
           const int k0 = w.band_lo + j * kTileN;
           lo = t_q - p.wl - k0;
           hi = min(t_q + p.wr, w.n_c - 1) - k0;
         } else {
-          jj0 = (j - w.n_band) * kTileN;
-          hi = min(kTileN, p.n_glob - jj0) - 1;
-          dedup = !p.etc;
+          const int g0 = (j - w.n_band) * kTileN;
+          hi = min(kTileN, p.n_glob - g0) - 1;
+          if (!p.etc) jj0 = g0;
         }
       } else {
         const int kt = w.kt0 + j;
@@ -366,39 +407,50 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
                                                  : p.N - (kt - (p.etc ? gt_src : 0)) * kTileN;
         hi = min(kTileN, limit) - 1;
       }
-      const bool need_mask = __any_sync(0xffffffffu, dedup || lo > 0 || hi < kTileN - 1);
+      uint32_t keep[4];
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) keep[wd] = range_bits(lo, hi, 32 * wd);
+      if (jj0 >= 0) {
+        const int ca = max(g_a - jj0, 0), cb = min(g_b - jj0, kTileN);  // in-band columns [ca, cb)
+        if (ca < cb) {
+          if (w.d == 1) {
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) keep[wd] &= ~range_bits(ca, cb - 1, 32 * wd);
+          } else {
+            for (int c = ca; c < cb; ++c) {
+              if ((__ldg(p.gidx + jj0 + c) - pos_q) % w.d == 0) {
+                const uint32_t bit = 1u << (c & 31);
+                if ((c >> 5) == 0) keep[0] &= ~bit;
+                else if ((c >> 5) == 1) keep[1] &= ~bit;
+                else if ((c >> 5) == 2) keep[2] &= ~bit;
+                else keep[3] &= ~bit;
+              }
+            }
+          }
+        }
+      }
+      const bool full = (keep[0] & keep[1] & keep[2] & keep[3]) == 0xFFFFFFFFu;
+      const bool need_mask = __any_sync(0xffffffffu, !full);
 
       if (!wait_all(bar(B_SFULL + q), n_done & 1)) { fail(); ok = false; break; }
       tc_fence_after();
       float s[kTileN];
       tmem_ld128(tS, s);
 
-      float tmax = -INFINITY;
-      if (!need_mask) {
+      if (need_mask) {
 #pragma unroll
-        for (int col = 0; col < kTileN; ++col) tmax = fmaxf(tmax, s[col]);
-      } else if (!dedup) {
-#pragma unroll
-        for (int col = 0; col < kTileN; ++col) {
-          s[col] = (col >= lo && col <= hi) ? s[col] : -INFINITY;
-          tmax = fmaxf(tmax, s[col]);
-        }
-      } else {
-#pragma unroll
-        for (int col = 0; col < kTileN; ++col) {
-          const int gp = (col <= hi) ? __ldg(p.gidx + jj0 + col) : -1;
-          bool ok_col = gp >= 0;
-          if (ok_col) {
-            const int diff = gp - pos_q;
-            if (diff % w.d == 0) {
-              const int tt = diff / w.d;
-              if (tt >= -p.wl && tt <= p.wr) ok_col = false;  // already counted in the band
-            }
-          }
-          s[col] = ok_col ? s[col] : -INFINITY;
-          tmax = fmaxf(tmax, s[col]);
-        }
+        for (int col = 0; col < kTileN; ++col)
+          s[col] = ((keep[col >> 5] >> (col & 31)) & 1u) ? s[col] : -INFINITY;
       }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[8 + k]);
+#pragma unroll
+      for (int col = 16; col < kTileN; col += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[col + k], s[col + 8 + k]);
+      }
+      const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float tmax2 = tmax * sl2;                   // log2 units (scale > 0 keeps the order)
       const float m_prev = m_run;
       float m_new = m_prev;
@@ -407,18 +459,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const float corr = ex2_approx(m_prev - m_use);
       const bool need_rescale = (m_prev != -INFINITY) && (m_new != m_prev);
       uint32_t pk[kTileN / 2];
-      float psum0 = 0.f, psum1 = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
 #pragma unroll
       for (int i = 0; i < kTileN / 2; ++i) {
         const float x0 = fmaf(s[2 * i], sl2, -m_use);
         const float x1 = fmaf(s[2 * i + 1], sl2, -m_use);
         const float p0 = poly_col(2 * i) ? exp2_poly(x0) : ex2_approx(x0);
         const float p1 = poly_col(2 * i + 1) ? exp2_poly(x1) : ex2_approx(x1);
-        psum0 += p0;
-        psum1 += p1;
+        ps[(2 * i) & 7] += p0;
+        ps[(2 * i + 1) & 7] += p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l_run = l_run * corr + (psum0 + psum1);
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l_run = l_run * corr + psum;
       m_run = m_new;
       // O_q is idle here: PV_q of the previous tile finished before QK_q of
       // this one (same issuing thread, in order), and PV_q of this tile waits

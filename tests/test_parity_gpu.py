@@ -66,6 +66,10 @@ BF16_CASES = [
     W("bf16 dilation beyond N", "bf16", 1, 2, 5, 64, 2, 2, (7, 8)),
     W("bf16 every token global", "bf16", 1, 1, 140, 64, 2, 2, (), False, tuple(range(140))),
     W("bf16 many heads", "bf16", 3, 16, 257, 64, 30, 30, tuple([1, 2] * 8)),
+    W("bf16 dense globals in dilated bands", "bf16", 1, 4, 700, 64, 40, 40, (1, 2, 3, 5), False,
+      tuple(range(100, 400, 3))),
+    W("bf16 globals in causal dilated bands D128", "bf16", 1, 3, 900, 128, 70, 0, (2, 4, 7), True,
+      tuple(range(0, 900, 7))),
 ]
 
 
