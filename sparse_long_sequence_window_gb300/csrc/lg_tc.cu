@@ -21,8 +21,9 @@
 //  * Global-row unit: 128 global queries against one split of all keys; the
 //    two warpgroups take alternate key tiles and each writes partial softmax
 //    statistics that a merge kernel combines.
-// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs (one thread), warps 4..7 and 8..11 are the two softmax
+// Warp roles (384 threads): warps 0 and 2 issue TMA loads (Q and K, V),
+// warp 1 owns TMEM; one thread of warp 1 (tile 0) and of warp 3 (tile 1)
+// issue the MMAs, warps 4..7 and 8..11 are the two softmax
 // warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128
 // fp32 columns, reused for P_q as packed bf16) and O_q (D columns) for both
 // tiles.  The MMA order per key tile j is PV_0(j-1), QK_0(j), PV_1(j-1),
@@ -151,6 +152,27 @@ __device__ __forceinline__ int last_use(const Unit& w, int q) {
   return -1;
 }
 
+// The tile list of one query tile in scalars (a runtime q indexing the
+// Unit's arrays would move the whole Unit to local memory).
+struct TileView {
+  int grow, active, first, last, n_band, q;
+  __device__ __forceinline__ bool uses(int j) const {
+    if (grow) return (j & 1) == q;
+    if (!active) return false;
+    if (j >= n_band) return true;
+    return j >= first && j <= last;
+  }
+};
+
+__device__ __forceinline__ TileView tile_view(const Unit& w, int q) {
+  TileView v;
+  v.grow = w.grow; v.n_band = w.n_band; v.q = q;
+  v.active = q ? w.active[1] : w.active[0];
+  v.first = q ? w.first[1] : w.first[0];
+  v.last = q ? w.last[1] : w.last[0];
+  return v;
+}
+
 // Issues the TMA loads of one 128-row operand tile.  strided: the
 // dilation-strided view of a slot; otherwise a plain view.
 template <int D>
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + KS, B_VFULL = 1 + 2 * KS,
                 B_VEMPTY = 1 + 2 * KS + VS, B_SFULL = 1 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
-                B_ODONE = B_PFULL + 2, B_FIN = B_ODONE + 2, NBARS = B_FIN + 1;
+                B_ODONE = B_PFULL + 2, B_FIN = B_ODONE + 2, NBARS = B_FIN + 2;
   static_assert(NBARS * 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -220,7 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
-      const uint32_t count = (i == B_PFULL || i == B_PFULL + 1) ? 128 : 1;
+      // K/V stages are released by both MMA issuers (one arrival each).
+      uint32_t count = 1;
+      if (i == B_PFULL || i == B_PFULL + 1) count = 128;
+      if ((i >= B_KEMPTY && i < B_KEMPTY + KS) || (i >= B_VEMPTY && i < B_VEMPTY + VS)) count = 2;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -246,114 +271,135 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 0 loads Q and the K ring, warp 2 the V ring: the two rings run
+    // independently, so a K load never queues behind a V stage that is
+    // still being read (V is released later in the pipeline than K).
     if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      if (w.grow) {
-        mbar_arrive_expect_tx(bar(B_QFULL), C::kTileBytes);
-        load_tile<D>(&p.mapQg, false, 1, w.grow0, w.bh, sQ, bar(B_QFULL));
-      } else {
-        mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
-        load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * w.t0, w.bh, sQ, bar(B_QFULL));
-        load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * (w.t0 + kTileM), w.bh, sQ + C::kTileBytes,
-                     bar(B_QFULL));
+      const bool is_k = (warp == 0);
+      int issued = 0;
+      if (is_k) {
+        if (w.grow) {
+          mbar_arrive_expect_tx(bar(B_QFULL), C::kTileBytes);
+          load_tile<D>(&p.mapQg, false, 1, w.grow0, w.bh, sQ, bar(B_QFULL));
+        } else {
+          mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
+          load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * w.t0, w.bh, sQ, bar(B_QFULL));
+          load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * (w.t0 + kTileM), w.bh, sQ + C::kTileBytes,
+                       bar(B_QFULL));
+        }
       }
+      const int S = is_k ? KS : VS;
+      const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+      const uint32_t ring = is_k ? sK : sV;
       for (int j = 0; j < T; ++j) {
-        const CUtensorMap *mk, *mv;
+        const CUtensorMap* m;
         bool strided;
         int y;
         if (!w.grow) {
           if (j < w.n_band) {
-            mk = &p.mapK[w.slot]; mv = &p.mapV[w.slot]; strided = true;
+            m = is_k ? &p.mapK[w.slot] : &p.mapV[w.slot]; strided = true;
             y = w.c + w.d * (w.band_lo + j * kTileN);
           } else {
-            mk = &p.mapKg; mv = &p.mapVg; strided = false;
+            m = is_k ? &p.mapKg : &p.mapVg; strided = false;
             y = (j - w.n_band) * kTileN;
           }
         } else {
           const int kt = w.kt0 + j;
           if (p.etc && kt < gt_src) {
-            mk = &p.mapKg; mv = &p.mapVg; strided = false; y = kt * kTileN;
+            m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
           } else {
-            mk = &p.mapK[0]; mv = &p.mapV[0]; strided = true;
+            m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
             y = (kt - (p.etc ? gt_src : 0)) * kTileN;
           }
         }
-        const int ks = j % KS, vs = j % VS;
-        if (j >= KS && !mbar_wait(bar(B_KEMPTY + ks), ((j / KS) - 1) & 1, abort_flag, cap)) { fail(); break; }
-        mbar_arrive_expect_tx(bar(B_KFULL + ks), C::kTileBytes);
-        load_tile<D>(mk, strided, strided ? w.d : 1, y, w.bh, sK + ks * C::kTileBytes, bar(B_KFULL + ks));
-        issued_k = j + 1;
-        if (j >= VS && !mbar_wait(bar(B_VEMPTY + vs), ((j / VS) - 1) & 1, abort_flag, cap)) { fail(); break; }
-        mbar_arrive_expect_tx(bar(B_VFULL + vs), C::kTileBytes);
-        load_tile<D>(mv, strided, strided ? w.d : 1, y, w.bh, sV + vs * C::kTileBytes, bar(B_VFULL + vs));
-        issued_v = j + 1;
+        const int st = j % S;
+        if (j >= S && !mbar_wait(bar(b_empty + st), ((j / S) - 1) & 1, abort_flag, cap)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
+        load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
+        issued = j + 1;
       }
       // Drain: every load issued here has landed before the CTA exits (these
       // waits ignore the abort flag and are bounded by the cap alone).
-      mbar_wait(bar(B_QFULL), 0, nullptr, cap);
-      for (int j = max(0, issued_k - KS); j < issued_k; ++j)
-        mbar_wait(bar(B_KFULL + j % KS), (j / KS) & 1, nullptr, cap);
-      for (int j = max(0, issued_v - VS); j < issued_v; ++j)
-        mbar_wait(bar(B_VFULL + j % VS), (j / VS) & 1, nullptr, cap);
+      if (is_k) mbar_wait(bar(B_QFULL), 0, nullptr, cap);
+      for (int j = max(0, issued - S); j < issued; ++j)
+        mbar_wait(bar(b_full + j % S), (j / S) & 1, nullptr, cap);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile (warp 1: tile 0, warp 3: tile 1), so
+    // each tile's QK -> softmax -> PV chain waits only on its own barriers
+    // and one thread's waits overlap the other's MMAs.  The tensor core only
+    // stays busy if MMAs are issued back to back, so every descriptor is
+    // precomputed: a K-major step adds 32 B (2 in 16-B units) inside a 128-B
+    // row and 16 KB per 64-column block, an MN-major V step adds 2 KB, a
+    // stage adds one tile; shared-memory addresses stay below 256 KB, so the
+    // additions never carry out of the 14-bit address field.  K and V stages
+    // are released by both issuers: the user after its MMAs (commit), the
+    // other after the stage was filled for this tile (plain arrival).
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      const int lastq[2] = {last_use(w, 0), last_use(w, 1)};
-      int pending[2] = {-1, -1};
-      int n_pv[2] = {0, 0};
+      const int q = warp >> 1;
+      constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, true);
+      constexpr uint64_t kStage = C::kTileBytes >> 4;
+      const uint64_t dQ = sdesc_sw128(sQ + ((w.grow || q == 0) ? 0 : C::kTileBytes), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
+      const uint32_t tS = tmem + C::kColS + q * 128;
+      const uint32_t tO = tmem + C::kColO + q * D;
+      const TileView tv = tile_view(w, q);
+      int last = -1;
+      for (int j = T - 1; j >= 0; --j)
+        if (tv.uses(j)) { last = j; break; }
+      int pend = -1;                   // key tile whose P waits for its PV
+      int npv = 0;                     // PVs issued
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, cap);
       if (!ok) fail();
-      // O_q += P_q V_jj, P_q read from TMEM (the S_q columns).
-      auto issue_pv = [&](int q) -> bool {
-        const int jj = pending[q];
-        const int vs = jj % VS;
-        if (!mbar_wait(bar(B_PFULL + q), n_pv[q] & 1, abort_flag, cap)) return false;
-        if (!mbar_wait(bar(B_VFULL + vs), (jj / VS) & 1, abort_flag, cap)) return false;
+      // O += P V_pend with P read from TMEM (the first 64 columns of S).
+      auto issue_pv = [&]() -> bool {
+        const int vs = pend % VS;
+        if (!mbar_wait(bar(B_PFULL + q), npv & 1, abort_flag, cap)) return false;
+        if (!mbar_wait(bar(B_VFULL + vs), (pend / VS) & 1, abort_flag, cap)) return false;
         tc_fence_after();
-        const uint32_t vbase = sV + vs * C::kTileBytes;
-        const uint32_t tP = tmem + C::kColS + q * 128;
-        const uint32_t tO = tmem + C::kColO + q * D;
+        const uint64_t dv = dV0 + vs * kStage;
+        umma_bf16_ts(tO, tS, dv, kIdPV, npv > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kTileN * 128, 1024);
-          umma_bf16_ts(tO, tP + kk * 8, b, idesc_pv, (n_pv[q] > 0 || kk > 0) ? 1u : 0u);
-        }
-        ++n_pv[q];
-        if (jj == lastq[q]) umma_commit(bar(B_ODONE + q));
-        if (q == 1 || !uses(w, 1, jj)) umma_commit(bar(B_VEMPTY + vs));  // last reader of V_jj
-        pending[q] = -1;
+        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
+        ++npv;
+        if (pend == last) umma_commit(bar(B_ODONE + q));
+        umma_commit(bar(B_VEMPTY + vs));
+        pend = -1;
         return true;
       };
       for (int j = 0; j < T && ok; ++j) {
         const int ks = j % KS;
         if (!mbar_wait(bar(B_KFULL + ks), (j / KS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-        const uint32_t kbase = sK + ks * C::kTileBytes;
-        for (int q = 0; q < 2 && ok; ++q) {
-          if (pending[q] >= 0 && !issue_pv(q)) { fail(); ok = false; break; }
-          if (!uses(w, q, j)) continue;
+        if (tv.uses(j)) {
+          if (pend >= 0 && !issue_pv()) { fail(); ok = false; break; }
           tc_fence_after();
-          const uint32_t qbase = sQ + (w.grow ? 0 : q * C::kTileBytes);
+          const uint64_t dk = dK0 + ks * kStage;
+          umma_bf16_ss(tS, dQ, dk, kIdQK, 0u);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
-            umma_bf16_ss(tmem + C::kColS + q * 128, sdesc_sw128(qbase + off, 16, 1024),
-                         sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 1; kk < D / 16; ++kk) {
+            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (kTileM * 128) + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(tS, dQ + o, dk + o, kIdQK, 1u);
           }
           umma_commit(bar(B_SFULL + q));
-          pending[q] = j;
+          umma_commit(bar(B_KEMPTY + ks));
+          pend = j;
+        } else {
+          // Not used by this tile: release both stages once they hold tile j.
+          mbar_arrive(bar(B_KEMPTY + ks));
+          const int vs = j % VS;
+          if (!mbar_wait(bar(B_VFULL + vs), (j / VS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+          mbar_arrive(bar(B_VEMPTY + vs));
         }
-        if (ok) umma_commit(bar(B_KEMPTY + ks));
       }
-      for (int q = 0; q < 2 && ok; ++q)
-        if (pending[q] >= 0 && !issue_pv(q)) { fail(); ok = false; }
+      if (ok && pend >= 0 && !issue_pv()) { fail(); ok = false; }
       // Every MMA issued here has completed before TMEM is released.
-      umma_commit(bar(B_FIN));
-      mbar_wait(bar(B_FIN), 0, nullptr, cap);
+      umma_commit(bar(B_FIN + q));
+      mbar_wait(bar(B_FIN + q), 0, nullptr, cap);
     }
   }
   } else {
@@ -386,8 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       g_a = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl);
       g_b = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1);
     }
+    const TileView tv = tile_view(w, q);
     for (int j = 0; j < T; ++j) {
-      if (!uses(w, q, j)) continue;
+      if (!tv.uses(j)) continue;
       // Allowed columns of this tile as a 128-bit keep mask.
       int lo = 0, hi = kTileN - 1;
       int jj0 = -1;                                     // first global index of a Longformer global tile
