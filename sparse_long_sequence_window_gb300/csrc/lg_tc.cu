@@ -219,7 +219,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ TcParams p, int n_units) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -229,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   unsigned char* misc = smem + C::kOffMisc;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   constexpr int KS = C::kKStages, VS = C::kVStages;
-  constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + KS, B_VFULL = 1 + 2 * KS,
-                B_VEMPTY = 1 + 2 * KS + VS, B_SFULL = 1 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
-                B_ODONE = B_PFULL + 2, B_FIN = B_ODONE + 2, NBARS = B_FIN + 2;
+  constexpr int B_QFULL = 0, B_KFULL = 2, B_KEMPTY = B_KFULL + KS, B_VFULL = B_KEMPTY + KS,
+                B_VEMPTY = B_VFULL + VS, B_SFULL = B_VEMPTY + VS, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
+                B_OFREE = B_ODONE + 2, B_FIN = B_OFREE + 2, NBARS = B_FIN + 2;
   static_assert(NBARS * 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -242,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
-      // K/V stages are released by both MMA issuers (one arrival each).
       uint32_t count = 1;
-      if (i == B_PFULL || i == B_PFULL + 1) count = 128;
+      if (i == B_PFULL || i == B_PFULL + 1 || i == B_OFREE || i == B_OFREE + 1) count = 128;
+      // K/V stages are released by both MMA issuers (one arrival each).
       if ((i >= B_KEMPTY && i < B_KEMPTY + KS) || (i >= B_VEMPTY && i < B_VEMPTY + VS)) count = 2;
       mbar_init(bar(i), count);
     }
@@ -259,123 +259,144 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Unit w = decode_unit(p, blockIdx.x);
-  const int T = w.n_tiles;
   const long long cap = p.wait_cap;
   const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
+  const int u0 = blockIdx.x, ustep = gridDim.x;   // this CTA's units: u0, u0 + ustep, ...
 
   auto fail = [&]() {
     *abort_flag = 1;
     atomicOr(p.status, ST_TIMEOUT);
+  };
+  // Query tile q of unit w into Q slot q (global-row units: the same rows in both slots).
+  auto load_q = [&](int q, const Unit& w) {
+    const uint32_t dst = sQ + q * C::kTileBytes;
+    mbar_arrive_expect_tx(bar(B_QFULL + q), C::kTileBytes);
+    if (w.grow) load_tile<D>(&p.mapQg, false, 1, w.grow0, w.bh, dst, bar(B_QFULL + q));
+    else load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * (w.t0 + q * kTileM), w.bh, dst, bar(B_QFULL + q));
   };
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers
-    // Warp 0 loads Q and the K ring, warp 2 the V ring: the two rings run
-    // independently, so a K load never queues behind a V stage that is
-    // still being read (V is released later in the pipeline than K).
+    // Warp 0 loads the K ring, warp 2 the V ring, over all units of this CTA
+    // (one global tile counter, so a ring never drains between units).
     if (lane == 0) {
       const bool is_k = (warp == 0);
-      int issued = 0;
-      if (is_k) {
-        if (w.grow) {
-          mbar_arrive_expect_tx(bar(B_QFULL), C::kTileBytes);
-          load_tile<D>(&p.mapQg, false, 1, w.grow0, w.bh, sQ, bar(B_QFULL));
-        } else {
-          mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
-          load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * w.t0, w.bh, sQ, bar(B_QFULL));
-          load_tile<D>(&p.mapQ[w.slot], true, w.d, w.c + w.d * (w.t0 + kTileM), w.bh, sQ + C::kTileBytes,
-                       bar(B_QFULL));
-        }
-      }
       const int S = is_k ? KS : VS;
       const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
       const uint32_t ring = is_k ? sK : sV;
-      for (int j = 0; j < T; ++j) {
-        const CUtensorMap* m;
-        bool strided;
-        int y;
-        if (!w.grow) {
-          if (j < w.n_band) {
-            m = is_k ? &p.mapK[w.slot] : &p.mapV[w.slot]; strided = true;
-            y = w.c + w.d * (w.band_lo + j * kTileN);
+      int g = 0, issued = 0;
+      bool ok = true;
+      for (int u = u0; u < n_units && ok; u += ustep) {
+        const Unit w = decode_unit(p, u);
+        for (int j = 0; j < w.n_tiles; ++j, ++g) {
+          const CUtensorMap* m;
+          bool strided;
+          int y;
+          if (!w.grow) {
+            if (j < w.n_band) {
+              m = is_k ? &p.mapK[w.slot] : &p.mapV[w.slot]; strided = true;
+              y = w.c + w.d * (w.band_lo + j * kTileN);
+            } else {
+              m = is_k ? &p.mapKg : &p.mapVg; strided = false;
+              y = (j - w.n_band) * kTileN;
+            }
           } else {
-            m = is_k ? &p.mapKg : &p.mapVg; strided = false;
-            y = (j - w.n_band) * kTileN;
+            const int kt = w.kt0 + j;
+            if (p.etc && kt < gt_src) {
+              m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
+            } else {
+              m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
+              y = (kt - (p.etc ? gt_src : 0)) * kTileN;
+            }
           }
-        } else {
-          const int kt = w.kt0 + j;
-          if (p.etc && kt < gt_src) {
-            m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
-          } else {
-            m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
-            y = (kt - (p.etc ? gt_src : 0)) * kTileN;
-          }
+          const int st = g % S;
+          if (g >= S && !mbar_wait(bar(b_empty + st), ((g / S) - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+          mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
+          load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
+          issued = g + 1;
         }
-        const int st = j % S;
-        if (j >= S && !mbar_wait(bar(b_empty + st), ((j / S) - 1) & 1, abort_flag, cap)) { fail(); break; }
-        mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
-        load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
-        issued = j + 1;
       }
       // Drain: every load issued here has landed before the CTA exits (these
       // waits ignore the abort flag and are bounded by the cap alone).
-      if (is_k) mbar_wait(bar(B_QFULL), 0, nullptr, cap);
-      for (int j = max(0, issued - S); j < issued; ++j)
-        mbar_wait(bar(b_full + j % S), (j / S) & 1, nullptr, cap);
+      for (int x = max(0, issued - S); x < issued; ++x)
+        mbar_wait(bar(b_full + x % S), (x / S) & 1, nullptr, cap);
     }
-  } else if (warp == 1 || warp == 3) {
+  } else {
     // ------------------------------------------------------------ MMA issuers
     // One issuing thread per query tile (warp 1: tile 0, warp 3: tile 1), so
     // each tile's QK -> softmax -> PV chain waits only on its own barriers
-    // and one thread's waits overlap the other's MMAs.  The tensor core only
-    // stays busy if MMAs are issued back to back, so every descriptor is
-    // precomputed: a K-major step adds 32 B (2 in 16-B units) inside a 128-B
-    // row and 16 KB per 64-column block, an MN-major V step adds 2 KB, a
-    // stage adds one tile; shared-memory addresses stay below 256 KB, so the
-    // additions never carry out of the 14-bit address field.  K and V stages
-    // are released by both issuers: the user after its MMAs (commit), the
-    // other after the stage was filled for this tile (plain arrival).
+    // and one thread's waits overlap the other's MMAs.  The chains continue
+    // from one unit to the next: the issuer reloads its Q slot as soon as its
+    // last QK of a unit has completed, and a unit's first PV (which
+    // overwrites O) waits until the softmax warpgroup has read the previous
+    // unit's O.  Every descriptor is precomputed: a K-major step adds 32 B (2
+    // in 16-B units) inside a 128-B row and 16 KB per 64-column block, an
+    // MN-major V step adds 2 KB, a stage adds one tile; shared-memory
+    // addresses stay below 256 KB, so the additions never carry out of the
+    // 14-bit address field.  A K or V stage is released by both issuers: the
+    // user after its MMAs (commit), the other once the stage holds the tile.
     if (lane == 0) {
       const int q = warp >> 1;
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, true);
       constexpr uint64_t kStage = C::kTileBytes >> 4;
-      const uint64_t dQ = sdesc_sw128(sQ + ((w.grow || q == 0) ? 0 : C::kTileBytes), 16, 1024);
+      const uint64_t dQ = sdesc_sw128(sQ + q * C::kTileBytes, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
       const uint32_t tS = tmem + C::kColS + q * 128;
       const uint32_t tO = tmem + C::kColO + q * D;
-      const TileView tv = tile_view(w, q);
-      int last = -1;
-      for (int j = T - 1; j >= 0; --j)
-        if (tv.uses(j)) { last = j; break; }
-      int pend = -1;                   // key tile whose P waits for its PV
-      int npv = 0;                     // PVs issued
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, cap);
-      if (!ok) fail();
-      // O += P V_pend with P read from TMEM (the first 64 columns of S).
-      auto issue_pv = [&]() -> bool {
-        const int vs = pend % VS;
-        if (!mbar_wait(bar(B_PFULL + q), npv & 1, abort_flag, cap)) return false;
-        if (!mbar_wait(bar(B_VFULL + vs), (pend / VS) & 1, abort_flag, cap)) return false;
-        tc_fence_after();
-        const uint64_t dv = dV0 + vs * kStage;
-        umma_bf16_ts(tO, tS, dv, kIdPV, npv > 0 ? 1u : 0u);
+      int g = 0;            // key tiles seen (all units of this CTA)
+      int ns = 0;           // QKs issued
+      int npv = 0;          // PVs issued
+      int nact = 0;         // units in which this query tile was active
+      int q_loads = 0, q_seen = 0;
+      bool ok = true;
+      if (u0 < n_units) { load_q(q, decode_unit(p, u0)); ++q_loads; }
+      for (int u = u0; u < n_units && ok; u += ustep) {
+        const Unit w = decode_unit(p, u);
+        const TileView tv = tile_view(w, q);
+        const int T = w.n_tiles;
+        int last = -1;
+        for (int j = T - 1; j >= 0; --j)
+          if (tv.uses(j)) { last = j; break; }
+        if (!mbar_wait(bar(B_QFULL + q), q_seen & 1, abort_flag, cap)) { fail(); ok = false; break; }
+        ++q_seen;
+        const int un = u + ustep;
+        int pend = -1, pend_g = 0;
+        bool first_pv = true;
+        // O += P V_pend with P read from TMEM (the first 64 columns of S).
+        auto issue_pv = [&]() -> bool {
+          const int vs = pend_g % VS;
+          if (!mbar_wait(bar(B_PFULL + q), npv & 1, abort_flag, cap)) return false;
+          if (first_pv && nact > 0 && !mbar_wait(bar(B_OFREE + q), (nact - 1) & 1, abort_flag, cap)) return false;
+          if (!mbar_wait(bar(B_VFULL + vs), (pend_g / VS) & 1, abort_flag, cap)) return false;
+          tc_fence_after();
+          const uint64_t dv = dV0 + vs * kStage;
+          umma_bf16_ts(tO, tS, dv, kIdPV, first_pv ? 0u : 1u);
 #pragma unroll
-        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
-        ++npv;
-        if (pend == last) umma_commit(bar(B_ODONE + q));
-        umma_commit(bar(B_VEMPTY + vs));
-        pend = -1;
-        return true;
-      };
-      for (int j = 0; j < T && ok; ++j) {
-        const int ks = j % KS;
-        if (!mbar_wait(bar(B_KFULL + ks), (j / KS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-        if (tv.uses(j)) {
+          for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
+          first_pv = false;
+          ++npv;
+          if (pend == last) umma_commit(bar(B_ODONE + q));
+          umma_commit(bar(B_VEMPTY + vs));
+          pend = -1;
+          return true;
+        };
+        for (int j = 0; j < T && ok; ++j, ++g) {
+          // Every K/V full phase is observed in order (a parity wait is only
+          // sound once the barrier's previous phase has been seen): a tile this
+          // query tile does not use is waited for and released at once.
+          const int ks = g % KS;
+          if (!mbar_wait(bar(B_KFULL + ks), (g / KS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+          if (!tv.uses(j)) {
+            mbar_arrive(bar(B_KEMPTY + ks));
+            const int vs = g % VS;
+            if (!mbar_wait(bar(B_VFULL + vs), (g / VS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+            mbar_arrive(bar(B_VEMPTY + vs));
+            continue;
+          }
           if (pend >= 0 && !issue_pv()) { fail(); ok = false; break; }
           tc_fence_after();
           const uint64_t dk = dK0 + ks * kStage;
@@ -387,17 +408,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           }
           umma_commit(bar(B_SFULL + q));
           umma_commit(bar(B_KEMPTY + ks));
+          ++ns;
           pend = j;
-        } else {
-          // Not used by this tile: release both stages once they hold tile j.
-          mbar_arrive(bar(B_KEMPTY + ks));
-          const int vs = j % VS;
-          if (!mbar_wait(bar(B_VFULL + vs), (j / VS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-          mbar_arrive(bar(B_VEMPTY + vs));
+          pend_g = g;
+          if (j == last && un < n_units) {
+            // The Q slot is free once this QK has completed: load the next unit's tile.
+            if (!mbar_wait(bar(B_SFULL + q), (ns - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+            load_q(q, decode_unit(p, un));
+            ++q_loads;
+          }
         }
+        if (ok && pend >= 0 && !issue_pv()) { fail(); ok = false; }
+        if (ok && last < 0 && un < n_units) { load_q(q, decode_unit(p, un)); ++q_loads; }
+        if (last >= 0) ++nact;
       }
-      if (ok && pend >= 0 && !issue_pv()) { fail(); ok = false; }
-      // Every MMA issued here has completed before TMEM is released.
+      // Drain: a Q load issued for a unit never started has landed, and
+      // every MMA issued here has completed before TMEM is released.
+      if (q_loads > q_seen) mbar_wait(bar(B_QFULL + q), q_seen & 1, nullptr, cap);
       umma_commit(bar(B_FIN + q));
       mbar_wait(bar(B_FIN + q), 0, nullptr, cap);
     }
@@ -410,12 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS + q * 128;
     const uint32_t tO = tmem + lane_off + C::kColO + q * D;
-    const int t_q = w.t0 + q * kTileM + r;              // band: query step in the class
-    const int pos_q = w.c + w.d * t_q;                  // band: query position
-    const bool row_valid = w.grow ? (w.grow0 + r < p.n_glob) : (t_q < w.n_c);
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;               // m_run in log2 units of the scaled logits
-    int n_done = 0;
+    int ns = 0;                                         // tiles processed (all units)
+    int nact = 0;                                       // units in which this tile was active
     bool ok = true;
     // Every lane of a warp takes the same decision, so the warp-collective
     // tcgen05.ld/st and votes below always run converged.
@@ -423,18 +447,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const bool got = mbar_wait(b, parity, abort_flag, cap);
       return __all_sync(0xffffffffu, got);
     };
-    // Global keys (Longformer) already inside this row's band are masked in the
-    // global tiles, so they count once.  The global list is sorted, so they
-    // have list indices in [g_a, g_b): the positions in [pos_q - d*w_left,
-    // pos_q + d*w_right]; for d > 1 only those on the row's stride lattice.
-    int g_a = 0, g_b = 0;
-    if (!w.grow && !p.etc && p.n_glob > 0 && row_valid) {
-      g_a = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl);
-      g_b = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1);
-    }
-    const TileView tv = tile_view(w, q);
-    for (int j = 0; j < T; ++j) {
-      if (!tv.uses(j)) continue;
+    for (int u = u0; u < n_units && ok; u += ustep) {
+      const Unit w = decode_unit(p, u);
+      const TileView tv = tile_view(w, q);
+      const int T = w.n_tiles;
+      const int t_q = w.t0 + q * kTileM + r;            // band: query step in the class
+      const int pos_q = w.c + w.d * t_q;                // band: query position
+      const bool row_valid = w.grow ? (w.grow0 + r < p.n_glob) : (t_q < w.n_c);
+      float m_run = -INFINITY, l_run = 0.f;             // m_run in log2 units of the scaled logits
+      int n_unit = 0;
+      // Global keys (Longformer) already inside this row's band are masked in
+      // the global tiles, so they count once.  The global list is sorted, so
+      // they have list indices in [g_a, g_b): the positions in [pos_q -
+      // d*w_left, pos_q + d*w_right]; for d > 1 only those on the row's stride
+      // lattice.
+      int g_a = 0, g_b = 0;
+      if (!w.grow && !p.etc && p.n_glob > 0 && row_valid) {
+        g_a = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl);
+        g_b = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1);
+      }
+      for (int j = 0; j < T; ++j) {
+        if (!tv.uses(j)) continue;
       // Allowed columns of this tile as a 128-bit keep mask.
       int lo = 0, hi = kTileN - 1;
       int jj0 = -1;                                     // first global index of a Longformer global tile
@@ -479,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const bool full = (keep[0] & keep[1] & keep[2] & keep[3]) == 0xFFFFFFFFu;
       const bool need_mask = __any_sync(0xffffffffu, !full);
 
-      if (!wait_all(bar(B_SFULL + q), n_done & 1)) { fail(); ok = false; break; }
+      if (!wait_all(bar(B_SFULL + q), ns & 1)) { fail(); ok = false; break; }
       tc_fence_after();
       float s[kTileN];
       tmem_ld128(tS, s);
@@ -506,20 +539,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const float corr = ex2_approx(m_prev - m_use);
       const bool need_rescale = (m_prev != -INFINITY) && (m_new != m_prev);
       uint32_t pk[kTileN / 2];
-      float ps[8];
+      uint64_t ps2[4];                                  // row sum in four packed pairs
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+      for (int k = 0; k < 4; ++k) ps2[k] = 0ull;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
 #pragma unroll
       for (int i = 0; i < kTileN / 2; ++i) {
-        const float x0 = fmaf(s[2 * i], sl2, -m_use);
-        const float x1 = fmaf(s[2 * i + 1], sl2, -m_use);
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
         const float p0 = poly_col(2 * i) ? exp2_poly(x0) : ex2_approx(x0);
         const float p1 = poly_col(2 * i + 1) ? exp2_poly(x1) : ex2_approx(x1);
-        ps[(2 * i) & 7] += p0;
-        ps[(2 * i + 1) & 7] += p1;
+        ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
-      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      float a0, a1, b0, b1;
+      f2_unpack(f2_add(ps2[0], ps2[1]), a0, a1);
+      f2_unpack(f2_add(ps2[2], ps2[3]), b0, b1);
+      const float psum = (a0 + a1) + (b0 + b1);
       l_run = l_run * corr + psum;
       m_run = m_new;
       // O_q is idle here: PV_q of the previous tile finished before QK_q of
@@ -539,57 +575,49 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       tmem_st64(tS, pk);                                 // P_q over the first 64 columns of S_q
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + q));
-      ++n_done;
-    }
-    if (ok && n_done > 0) {
-      if (!wait_all(bar(B_ODONE + q), 0)) {
-        fail();
-      } else {
-        tc_fence_after();
-        if (!w.grow) {
-          const float inv_l = 1.f / l_run;
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                (static_cast<size_t>(w.bh) * p.N + pos_q) * D;
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float o[32];
-            tmem_ld32(tO + cc * 32, o);
-            if (row_valid) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                uint4 val;
-                val.x = pack_bf16x2(o[8 * k + 0] * inv_l, o[8 * k + 1] * inv_l);
-                val.y = pack_bf16x2(o[8 * k + 2] * inv_l, o[8 * k + 3] * inv_l);
-                val.z = pack_bf16x2(o[8 * k + 4] * inv_l, o[8 * k + 5] * inv_l);
-                val.w = pack_bf16x2(o[8 * k + 6] * inv_l, o[8 * k + 7] * inv_l);
-                dst[k] = val;
-              }
-            }
-          }
-          if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
-        } else {
-          const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;   // partial slot of this warpgroup
-          const int grow = w.grow0 + r;
-          const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + grow) * p.n_parts + slot;
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float o[32];
-            tmem_ld32(tO + cc * 32, o);
-            if (row_valid) {
-              float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + cc * 32);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-            }
-          }
-          if (row_valid) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
-        }
+      ++ns;
+      ++n_unit;
       }
-    } else if (ok && w.grow && row_valid) {
-      // A warpgroup with no key tile in this split leaves an empty partial.
-      const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;
-      const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
-      reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(-INFINITY, 0.f);
+      if (!ok) break;
+      if (n_unit > 0) {
+        if (!wait_all(bar(B_ODONE + q), nact & 1)) { fail(); ok = false; break; }
+        tc_fence_after();
+        float o[D];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, *reinterpret_cast<float(*)[32]>(o + cc * 32));
+        tc_fence_before();
+        mbar_arrive(bar(B_OFREE + q));                  // O may be overwritten by the next unit
+        ++nact;
+        if (!w.grow) {
+          if (row_valid) {
+            const float inv_l = 1.f / l_run;
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                  (static_cast<size_t>(w.bh) * p.N + pos_q) * D);
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+              uint4 val;
+              val.x = pack_bf16x2(o[8 * k + 0] * inv_l, o[8 * k + 1] * inv_l);
+              val.y = pack_bf16x2(o[8 * k + 2] * inv_l, o[8 * k + 3] * inv_l);
+              val.z = pack_bf16x2(o[8 * k + 4] * inv_l, o[8 * k + 5] * inv_l);
+              val.w = pack_bf16x2(o[8 * k + 6] * inv_l, o[8 * k + 7] * inv_l);
+              dst[k] = val;
+            }
+            p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
+          }
+        } else if (row_valid) {
+          const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;   // partial slot of this warpgroup
+          const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D);
+#pragma unroll
+          for (int k = 0; k < D / 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
+        }
+      } else if (w.grow && row_valid) {
+        // A warpgroup with no key tile in this split leaves an empty partial.
+        const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;
+        const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
+        reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(-INFINITY, 0.f);
+      }
     }
   }
 
@@ -616,6 +644,20 @@ cudaError_t prepare_kernel() {
   return cudaFuncSetAttribute(tc_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
 }
 
+// Persistent grid: one CTA per SM (shared memory allows no second one), each
+// walking units blockIdx.x, blockIdx.x + gridDim.x, ...
+int grid_for(int n_units) {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (sms[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    sms[dev] = v;
+  }
+  return n_units < sms[dev] ? n_units : sms[dev];
+}
+
 cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
   if (n_units <= 0) return cudaSuccess;
   static bool attr_done[2] = {false, false};
@@ -625,14 +667,14 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       attr_done[0] = true;
     }
-    tc_attn_kernel<64><<<n_units, kThreads, Cfg<64>::kSmem, s>>>(p);
+    tc_attn_kernel<64><<<grid_for(n_units), kThreads, Cfg<64>::kSmem, s>>>(p, n_units);
   } else {
     if (!attr_done[1]) {
       cudaError_t e = prepare_kernel<128>();
       if (e != cudaSuccess) return e;
       attr_done[1] = true;
     }
-    tc_attn_kernel<128><<<n_units, kThreads, Cfg<128>::kSmem, s>>>(p);
+    tc_attn_kernel<128><<<grid_for(n_units), kThreads, Cfg<128>::kSmem, s>>>(p, n_units);
   }
   return cudaGetLastError();
 }
