@@ -235,12 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   static_assert(NBARS * 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  volatile int* issued = reinterpret_cast<volatile int*>(misc + 264);  // last key tile each issuer issued a QK for
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    issued[0] = -1;
+    issued[1] = -1;
     for (int i = 0; i < NBARS; ++i) {
       uint32_t count = 1;
       if (i == B_PFULL || i == B_PFULL + 1 || i == B_OFREE || i == B_OFREE + 1) count = 128;
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       if (u0 < n_units) { load_q(q, decode_unit(p, u0)); ++q_loads; }
       for (int u = u0; u < n_units && ok; u += ustep) {
         const Unit w = decode_unit(p, u);
-        const TileView tv = tile_view(w, q);
+        const TileView tv = tile_view(w, q), tvo = tile_view(w, 1 - q);
         const int T = w.n_tiles;
         int last = -1;
         for (int j = T - 1; j >= 0; --j)
@@ -397,6 +400,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
             mbar_arrive(bar(B_VEMPTY + vs));
             continue;
           }
+          // Ping-pong on key tiles both query tiles use: tile 1's group (PV of
+          // its previous tile + QK of this one) goes after tile 0's, and tile
+          // 0's next group after tile 1's, so one tile's softmax overlaps the
+          // other's MMAs instead of both running at once.  Monotonic counters
+          // (not barrier phases), so no phase can alias.
+          const int need_other = (q == 0) ? ((j >= 1 && tv.uses(j - 1) && tvo.uses(j - 1)) ? g - 1 : -2)
+                                          : (tvo.uses(j) ? g : -2);
+          if (need_other >= -1 && issued[1 - q] < need_other) {
+            const long long t0 = clock64();
+            while (issued[1 - q] < need_other) {
+              if (*abort_flag || clock64() - t0 > cap) { fail(); ok = false; break; }
+            }
+            if (!ok) break;
+          }
           if (pend >= 0 && !issue_pv()) { fail(); ok = false; break; }
           tc_fence_after();
           const uint64_t dk = dK0 + ks * kStage;
@@ -408,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           }
           umma_commit(bar(B_SFULL + q));
           umma_commit(bar(B_KEMPTY + ks));
+          issued[q] = g;
           ++ns;
           pend = j;
           pend_g = g;
