@@ -21,16 +21,16 @@
 //  * Global-row unit: 128 global queries against one split of all keys; the
 //    two warpgroups take alternate key tiles and each writes partial softmax
 //    statistics that a merge kernel combines.
-// Warp roles (384 threads): warps 0 and 2 issue TMA loads (Q and K, V),
-// warp 1 owns TMEM; one thread of warp 1 (tile 0) and of warp 3 (tile 1)
-// issue the MMAs, warps 4..7 and 8..11 are the two softmax
-// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128
-// fp32 columns, reused for P_q as packed bf16) and O_q (D columns) for both
-// tiles.  The MMA order per key tile j is PV_0(j-1), QK_0(j), PV_1(j-1),
-// QK_1(j), so the tensor core works on one tile while the other tile's
-// softmax runs.  Because tcgen05 MMAs of one thread execute in order, the
-// completion of QK_q(j) also means PV_q(j-1) is done: the softmax may then
-// rescale O_q and overwrite S_q with P_q without further waits.
+// Warp roles (384 threads): warp 0 issues the K loads, warp 2 the V loads
+// (TMA); warp 1 owns TMEM and issues the MMAs and Q loads of query tile 0,
+// warp 3 those of tile 1; warps 4..7 and 8..11 are the two softmax
+// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128 fp32 columns, reused for
+// P_q as packed bf16) and O_q (D columns) for both tiles.  The MMA order per
+// key tile j is PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j), so the tensor core
+// works on one tile while the other tile's softmax runs.  Because the MMAs
+// of one thread execute in order, the completion of QK_q(j) also means
+// PV_q(j-1) is done: the softmax may then rescale O_q and overwrite S_q with
+// P_q without further waits.
 #include "lg_internal.h"
 #include "lg_ptx.cuh"
 
@@ -137,30 +137,14 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   return w;
 }
 
-// Does query tile q work on key tile j?
-__device__ __forceinline__ bool uses(const Unit& w, int q, int j) {
-  if (w.grow) return (j & 1) == q;
-  if (!w.active[q]) return false;
-  if (j >= w.n_band) return true;  // global-key tiles
-  return j >= w.first[q] && j <= w.last[q];
-}
-
-// Last key tile query tile q works on (-1: none).
-__device__ __forceinline__ int last_use(const Unit& w, int q) {
-  for (int j = w.n_tiles - 1; j >= 0; --j)
-    if (uses(w, q, j)) return j;
-  return -1;
-}
-
 // The tile list of one query tile in scalars (a runtime q indexing the
 // Unit's arrays would move the whole Unit to local memory).
 struct TileView {
   int grow, active, first, last, n_band, q;
   __device__ __forceinline__ bool uses(int j) const {
-    if (grow) return (j & 1) == q;
-    if (!active) return false;
-    if (j >= n_band) return true;
-    return j >= first && j <= last;
+    const bool in_band = (j >= first) & (j <= last);
+    const bool global_tile = j >= n_band;
+    return grow ? (((j ^ q) & 1) == 0) : (active & (in_band | global_tile));
   }
 };
 
@@ -216,6 +200,29 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+
+// Where key/value tile j of unit w comes from: the tensor map, whether it is
+// the dilation-strided view, and the row coordinate.
+__device__ __forceinline__ void tile_source(const TcParams& p, const Unit& w, int j, bool is_k, int gt_src,
+                                            const CUtensorMap*& m, bool& strided, int& y) {
+  if (!w.grow) {
+    if (j < w.n_band) {
+      m = is_k ? &p.mapK[w.slot] : &p.mapV[w.slot]; strided = true;
+      y = w.c + w.d * (w.band_lo + j * kTileN);
+    } else {
+      m = is_k ? &p.mapKg : &p.mapVg; strided = false;
+      y = (j - w.n_band) * kTileN;
+    }
+  } else {
+    const int kt = w.kt0 + j;
+    if (p.etc && kt < gt_src) {
+      m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
+    } else {
+      m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
+      y = (kt - (p.etc ? gt_src : 0)) * kTileN;
+    }
+  }
 }
 
 template <int D>
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
   if (warp == 0 || warp == 2) {
-    // ------------------------------------------------------------ TMA producers
+    // ------------------------------------------------------------ K and V producers
     // Warp 0 loads the K ring, warp 2 the V ring, over all units of this CTA
     // (one global tile counter, so a ring never drains between units).
     if (lane == 0) {
@@ -297,23 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           const CUtensorMap* m;
           bool strided;
           int y;
-          if (!w.grow) {
-            if (j < w.n_band) {
-              m = is_k ? &p.mapK[w.slot] : &p.mapV[w.slot]; strided = true;
-              y = w.c + w.d * (w.band_lo + j * kTileN);
-            } else {
-              m = is_k ? &p.mapKg : &p.mapVg; strided = false;
-              y = (j - w.n_band) * kTileN;
-            }
-          } else {
-            const int kt = w.kt0 + j;
-            if (p.etc && kt < gt_src) {
-              m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
-            } else {
-              m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
-              y = (kt - (p.etc ? gt_src : 0)) * kTileN;
-            }
-          }
+          tile_source(p, w, j, is_k, gt_src, m, strided, y);
           const int st = g % S;
           if (g >= S && !mbar_wait(bar(b_empty + st), ((g / S) - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
           mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
@@ -328,94 +319,117 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     }
   } else {
     // ------------------------------------------------------------ MMA issuers
-    // One issuing thread per query tile (warp 1: tile 0, warp 3: tile 1), so
-    // each tile's QK -> softmax -> PV chain waits only on its own barriers
-    // and one thread's waits overlap the other's MMAs.  The chains continue
-    // from one unit to the next: the issuer reloads its Q slot as soon as its
-    // last QK of a unit has completed, and a unit's first PV (which
-    // overwrites O) waits until the softmax warpgroup has read the previous
-    // unit's O.  Every descriptor is precomputed: a K-major step adds 32 B (2
-    // in 16-B units) inside a 128-B row and 16 KB per 64-column block, an
-    // MN-major V step adds 2 KB, a stage adds one tile; shared-memory
-    // addresses stay below 256 KB, so the additions never carry out of the
-    // 14-bit address field.  A K or V stage is released by both issuers: the
-    // user after its MMAs (commit), the other once the stage holds the tile.
-    if (lane == 0) {
-      const int q = warp >> 1;
-      constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, true);
-      constexpr uint64_t kStage = C::kTileBytes >> 4;
-      const uint64_t dQ = sdesc_sw128(sQ + q * C::kTileBytes, 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
-      const uint32_t tS = tmem + C::kColS + q * 128;
-      const uint32_t tO = tmem + C::kColO + q * D;
-      int g = 0;            // key tiles seen (all units of this CTA)
-      int ns = 0;           // QKs issued
-      int npv = 0;          // PVs issued
-      int nact = 0;         // units in which this query tile was active
-      int q_loads = 0, q_seen = 0;
-      bool ok = true;
-      if (u0 < n_units) { load_q(q, decode_unit(p, u0)); ++q_loads; }
-      for (int u = u0; u < n_units && ok; u += ustep) {
-        const Unit w = decode_unit(p, u);
-        const TileView tv = tile_view(w, q), tvo = tile_view(w, 1 - q);
-        const int T = w.n_tiles;
-        int last = -1;
-        for (int j = T - 1; j >= 0; --j)
-          if (tv.uses(j)) { last = j; break; }
-        if (!mbar_wait(bar(B_QFULL + q), q_seen & 1, abort_flag, cap)) { fail(); ok = false; break; }
-        ++q_seen;
-        const int un = u + ustep;
-        int pend = -1, pend_g = 0;
-        bool first_pv = true;
-        // O += P V_pend with P read from TMEM (the first 64 columns of S).
-        auto issue_pv = [&]() -> bool {
-          const int vs = pend_g % VS;
-          if (!mbar_wait(bar(B_PFULL + q), npv & 1, abort_flag, cap)) return false;
-          if (first_pv && nact > 0 && !mbar_wait(bar(B_OFREE + q), (nact - 1) & 1, abort_flag, cap)) return false;
-          if (!mbar_wait(bar(B_VFULL + vs), (pend_g / VS) & 1, abort_flag, cap)) return false;
-          tc_fence_after();
-          const uint64_t dv = dV0 + vs * kStage;
-          umma_bf16_ts(tO, tS, dv, kIdPV, first_pv ? 0u : 1u);
+    // Warp 1 issues the MMAs of query tile 0, warp 3 those of tile 1.  Each
+    // issuing warp runs its loop converged (every lane waits, so the loop
+    // state stays warp-uniform) and one elected lane issues every MMA, commit,
+    // arrival and Q load (the same lane throughout: tcgen05 ordering and
+    // commit tracking are per thread).  Per key tile j a tile's group is
+    // PV_q(j-1) then QK_q(j).  The groups alternate between the tiles on key
+    // tiles both use (tile 1's group for j after tile 0's, tile 0's group for
+    // j + 1 after tile 1's), so one tile's softmax overlaps the other tile's
+    // MMAs.  An issuer first waits for its K and V tiles, the O slot and its
+    // Q tile, then for its turn (a monotonic counter in shared memory, so no
+    // phase can alias), and for its P last, which is usually the latest, so
+    // little is left between P and the first MMA.  Every K/V full phase is
+    // observed by both issuers in order (a parity wait is only sound once the
+    // barrier's previous phase has been seen); a tile an issuer does not use
+    // is released by it at once, a used one after its MMAs (commit).  The
+    // issuer reloads its Q slot for the next unit as soon as its last QK of
+    // the unit has completed, and a unit's first PV (which overwrites O)
+    // waits until the softmax warpgroup has read the previous unit's O.
+    // Every descriptor is precomputed: a K-major step adds 32 B (2 in 16-B
+    // units) inside a 128-B row and 16 KB per 64-column block, an MN-major V
+    // step adds 2 KB, a stage adds one tile; shared-memory addresses stay
+    // below 256 KB, so the additions never carry out of the 14-bit address
+    // field.
+    static_assert((VS & (VS - 1)) == 0, "V ring depth must be a power of two");
+    constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, true);
+    constexpr uint64_t kStage = C::kTileBytes >> 4;
+    const int q = warp >> 1;
+    const bool leader = elect_one();
+    const uint64_t dQ = sdesc_sw128(sQ + q * C::kTileBytes, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
+    const uint32_t tS = tmem + C::kColS + q * 128;
+    const uint32_t tO = tmem + C::kColO + q * D;
+    int g = 0, ks = 0, kph = 0;   // key tiles seen (all units), K stage of tile g and its phase parity
+    int ns = 0;                   // QKs issued
+    int npv = 0;                  // PVs issued
+    int nact = 0;                 // units in which this query tile was active
+    int q_loads = 0, q_seen = 0;
+    bool ok = true;
+    auto wait_or_fail = [&](int b, int parity) -> bool {
+      if (__all_sync(0xffffffffu, mbar_wait(bar(b), parity, abort_flag, cap))) return true;
+      if (leader) fail();
+      ok = false;
+      return false;
+    };
+    if (u0 < n_units) {
+      if (leader) load_q(q, decode_unit(p, u0));
+      __syncwarp();
+      ++q_loads;
+    }
+    for (int u = u0; u < n_units && ok; u += ustep) {
+      const Unit w = decode_unit(p, u);
+      const TileView tv = tile_view(w, q), tvo = tile_view(w, 1 - q);
+      int last = -1;
+      for (int j = w.n_tiles - 1; j >= 0; --j)
+        if (tv.uses(j)) { last = j; break; }
+      const int un = u + ustep;
+      int pend = -1, pend_g = 0;
+      bool first_pv = true, q_ready = false;
+      // What the pending PV needs besides its P: its V stage and the O slot
+      // (first PV of a unit).  P comes last: it is usually the latest.
+      auto pv_waits = [&]() -> bool {
+        if (!wait_or_fail(B_VFULL + (pend_g & (VS - 1)), (pend_g / VS) & 1)) return false;
+        return !(first_pv && nact > 0) || wait_or_fail(B_OFREE + q, (nact - 1) & 1);
+      };
+      // O_q += P_q V(pend), P read from TMEM (the first 64 columns of S_q); leader only.
+      auto pv_mmas = [&]() {
+        const int vs = pend_g & (VS - 1);
+        const uint64_t dv = dV0 + vs * kStage;
+        umma_bf16_ts(tO, tS, dv, kIdPV, first_pv ? 0u : 1u);
 #pragma unroll
-          for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
-          first_pv = false;
-          ++npv;
-          if (pend == last) umma_commit(bar(B_ODONE + q));
-          umma_commit(bar(B_VEMPTY + vs));
-          pend = -1;
-          return true;
-        };
-        for (int j = 0; j < T && ok; ++j, ++g) {
-          // Every K/V full phase is observed in order (a parity wait is only
-          // sound once the barrier's previous phase has been seen): a tile this
-          // query tile does not use is waited for and released at once.
-          const int ks = g % KS;
-          if (!mbar_wait(bar(B_KFULL + ks), (g / KS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-          if (!tv.uses(j)) {
-            mbar_arrive(bar(B_KEMPTY + ks));
-            const int vs = g % VS;
-            if (!mbar_wait(bar(B_VFULL + vs), (g / VS) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-            mbar_arrive(bar(B_VEMPTY + vs));
-            continue;
+        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
+        if (pend == last) umma_commit(bar(B_ODONE + q));
+        umma_commit(bar(B_VEMPTY + vs));
+      };
+      for (int j = 0; j < w.n_tiles; ++j, ++g) {
+        if (!wait_or_fail(B_KFULL + ks, kph)) break;
+        if (!tv.uses(j)) {
+          if (leader) mbar_arrive(bar(B_KEMPTY + ks));
+          __syncwarp();
+          const int vs = g & (VS - 1);
+          if (!wait_or_fail(B_VFULL + vs, (g / VS) & 1)) break;
+          if (leader) mbar_arrive(bar(B_VEMPTY + vs));
+          __syncwarp();
+          if (++ks == KS) { ks = 0; kph ^= 1; }
+          continue;
+        }
+        if (pend >= 0 && !pv_waits()) break;
+        if (!q_ready) {
+          if (!wait_or_fail(B_QFULL + q, q_seen & 1)) break;
+          ++q_seen;
+          q_ready = true;
+        }
+        const bool turn = (q == 0) ? ((j >= 1) & tv.uses(j - 1) & tvo.uses(j - 1)) : tvo.uses(j);
+        const int need_other = q == 0 ? g - 1 : g;
+        if (turn && issued[1 - q] < need_other) {
+          const long long t0 = clock64();
+          while (issued[1 - q] < need_other) {
+            if (*abort_flag || clock64() - t0 > cap) { ok = false; break; }
           }
-          // Ping-pong on key tiles both query tiles use: tile 1's group (PV of
-          // its previous tile + QK of this one) goes after tile 0's, and tile
-          // 0's next group after tile 1's, so one tile's softmax overlaps the
-          // other's MMAs instead of both running at once.  Monotonic counters
-          // (not barrier phases), so no phase can alias.
-          const int need_other = (q == 0) ? ((j >= 1 && tv.uses(j - 1) && tvo.uses(j - 1)) ? g - 1 : -2)
-                                          : (tvo.uses(j) ? g : -2);
-          if (need_other >= -1 && issued[1 - q] < need_other) {
-            const long long t0 = clock64();
-            while (issued[1 - q] < need_other) {
-              if (*abort_flag || clock64() - t0 > cap) { fail(); ok = false; break; }
-            }
-            if (!ok) break;
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (leader) fail();
+            ok = false;
+            break;
           }
-          if (pend >= 0 && !issue_pv()) { fail(); ok = false; break; }
-          tc_fence_after();
+        }
+        if (pend >= 0 && !wait_or_fail(B_PFULL + q, npv & 1)) break;
+        tc_fence_after();
+        if (leader) {
+          if (pend >= 0) pv_mmas();
           const uint64_t dk = dK0 + ks * kStage;
           umma_bf16_ss(tS, dQ, dk, kIdQK, 0u);
 #pragma unroll
@@ -426,26 +440,49 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           umma_commit(bar(B_SFULL + q));
           umma_commit(bar(B_KEMPTY + ks));
           issued[q] = g;
-          ++ns;
-          pend = j;
-          pend_g = g;
-          if (j == last && un < n_units) {
-            // The Q slot is free once this QK has completed: load the next unit's tile.
-            if (!mbar_wait(bar(B_SFULL + q), (ns - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
-            load_q(q, decode_unit(p, un));
+        }
+        __syncwarp();
+        if (pend >= 0) {
+          first_pv = false;
+          ++npv;
+        }
+        ++ns;
+        pend = j;
+        pend_g = g;
+        if (++ks == KS) { ks = 0; kph ^= 1; }
+        if (j == last && un < n_units) {
+          // The Q slot is free once this QK has completed: load the next unit's tile.
+          if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
+          if (leader) load_q(q, decode_unit(p, un));
+          __syncwarp();
+          ++q_loads;
+        }
+      }
+      if (ok && pend >= 0 && pv_waits() && wait_or_fail(B_PFULL + q, npv & 1)) {
+        tc_fence_after();
+        if (leader) pv_mmas();
+        __syncwarp();
+        ++npv;
+      }
+      if (ok && last < 0) {
+        // No key tile for this query tile: its Q load is consumed unused.
+        if (wait_or_fail(B_QFULL + q, q_seen & 1)) {
+          ++q_seen;
+          if (un < n_units) {
+            if (leader) load_q(q, decode_unit(p, un));
+            __syncwarp();
             ++q_loads;
           }
         }
-        if (ok && pend >= 0 && !issue_pv()) { fail(); ok = false; }
-        if (ok && last < 0 && un < n_units) { load_q(q, decode_unit(p, un)); ++q_loads; }
-        if (last >= 0) ++nact;
       }
-      // Drain: a Q load issued for a unit never started has landed, and
-      // every MMA issued here has completed before TMEM is released.
-      if (q_loads > q_seen) mbar_wait(bar(B_QFULL + q), q_seen & 1, nullptr, cap);
-      umma_commit(bar(B_FIN + q));
-      mbar_wait(bar(B_FIN + q), 0, nullptr, cap);
+      if (last >= 0) ++nact;
     }
+    // Drain: a Q load issued for a unit never started has landed, and every
+    // MMA issued here has completed before TMEM is released.
+    if (q_loads > q_seen) mbar_wait(bar(B_QFULL + q), q_seen & 1, nullptr, cap);
+    if (leader) umma_commit(bar(B_FIN + q));
+    __syncwarp();
+    mbar_wait(bar(B_FIN + q), 0, nullptr, cap);
   }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
