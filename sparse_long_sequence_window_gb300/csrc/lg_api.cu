@@ -92,10 +92,11 @@ GrowPlan grow_plan(int n_glob, int key_tiles) {
 }
 
 struct WsLayout {
-  size_t qg = 0, kg = 0, vg = 0, acc = 0, ml = 0, total = kStatusBytes;
+  size_t qg = 0, kg = 0, vg = 0, cnt = 0, acc = 0, ml = 0, total = kStatusBytes;
 };
 
-WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather) {
+// gather (Longformer): gathered global rows and the gcount table of N + 1 ints.
+WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N) {
   WsLayout w;
   size_t off = kStatusBytes;
   if (n_glob > 0) {
@@ -104,6 +105,7 @@ WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather) {
       w.qg = off; off += gbytes;
       w.kg = off; off += gbytes;
       w.vg = off; off += gbytes;
+      w.cnt = off; off += round_up((static_cast<size_t>(N) + 1) * 4, 256);
     }
     w.acc = off; off += round_up(static_cast<size_t>(BH) * n_glob * n_splits * D * 4, 256);
     w.ml = off; off += round_up(static_cast<size_t>(BH) * n_glob * n_splits * 2 * 4, 256);
@@ -177,14 +179,14 @@ size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_d
   if (B < 1 || H < 1 || N < 1 || D < 1 || n_global < 0 || n_global > N || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(n_global, cdiv(N, kTileN));
-  return ws_layout(B * H, n_global, D, g.n_parts, true).total;
+  return ws_layout(B * H, n_global, D, g.n_parts, true, N).total;
 }
 
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || G < 1 || D < 1 || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  return ws_layout(B * H, G, D, g.n_parts, false).total;
+  return ws_layout(B * H, G, D, g.n_parts, false, 0).total;
 }
 
 lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
@@ -240,7 +242,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   // ---- bf16 tensor-core path
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(n_global, cdiv(N, kTileN));
-  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true);
+  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true, N);
   __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(ws + lay.qg);
   __nv_bfloat16* kg = reinterpret_cast<__nv_bfloat16*>(ws + lay.kg);
   __nv_bfloat16* vg = reinterpret_cast<__nv_bfloat16*>(ws + lay.vg);
@@ -250,6 +252,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     pp.q = static_cast<const __nv_bfloat16*>(q); pp.k = static_cast<const __nv_bfloat16*>(k);
     pp.v = static_cast<const __nv_bfloat16*>(v);
     pp.qg = qg; pp.kg = kg; pp.vg = vg;
+    pp.gcount = reinterpret_cast<int*>(ws + lay.cnt);
     if ((e = launch_prep(pp, stream)) != cudaSuccess) return LG_ERR_CUDA;
   }
 
@@ -301,7 +304,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.out = out; tp.lse = lse;
     tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
     tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
-    tp.gidx = global_idx; tp.status = status; tp.wait_cap = wait_cap_cycles();
+    tp.gidx = global_idx; tp.gcount = n_global > 0 ? reinterpret_cast<const int*>(ws + lay.cnt) : nullptr;
+    tp.status = status; tp.wait_cap = wait_cap_cycles();
     tp.scale_log2 = s * 1.4426950408889634f;
     tp.BH = BH; tp.H = H; tp.N = N; tp.D = D; tp.wl = wl; tp.wr = wr; tp.n_glob = n_global; tp.etc = 0;
     tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
@@ -363,7 +367,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
 
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false);
+  const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0);
   static TcParams tp;
   tp = TcParams{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||

@@ -1,8 +1,11 @@
 // Support kernels of the bf16 path:
 //  * prep: checks that the global positions are strictly increasing and inside
 //    [0, N) (a bad list sets a status bit; nothing outside the tensors is
-//    touched) and gathers the global tokens' q, k, v rows into contiguous
-//    [BH, g, D] buffers that the tensor-core kernel reads with TMA.
+//    touched), gathers the global tokens' q, k, v rows into contiguous
+//    [BH, g, D] buffers that the tensor-core kernel reads with TMA, and
+//    tabulates gcount[x] = number of global positions below x for x in
+//    [0, N] (one binary search per entry), so that a query row finds the
+//    global keys inside its band with two loads.
 //  * merge: combines the partial softmax statistics of the global-query rows
 //    over the key splits.  With m = max_p m_p: l = sum_p 2^{m_p - m} l_p,
 //    O = sum_p 2^{m_p - m} acc_p / l, LSE = (m + log2 l) ln 2 (statistics are
@@ -27,6 +30,16 @@ __global__ void prep_kernel(const PrepParams p) {
     bool bad = pos < 0 || pos >= p.N;
     if (r > 0 && p.gidx[r - 1] >= pos) bad = true;
     if (bad) atomicOr(p.status, ST_GLOBAL_IDX);
+  }
+  if (p.gcount != nullptr) {
+    for (int x = tid; x <= p.N; x += nthreads) {
+      int lo = 0, hi = p.n_glob;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (p.gidx[mid] < x) lo = mid + 1; else hi = mid;
+      }
+      p.gcount[x] = lo;
+    }
   }
   if (p.q == nullptr) return;
   const int lane = threadIdx.x & 31;
@@ -103,6 +116,7 @@ __global__ void merge_kernel(const MergeParams p, int bf16_out) {
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   if (p.n_glob <= 0) return cudaSuccess;
   long long work = p.q ? static_cast<long long>(p.BH) * p.n_glob * 32 : p.n_glob;
+  if (p.gcount != nullptr && work < static_cast<long long>(p.N) + 1) work = static_cast<long long>(p.N) + 1;
   long long nb = (work + 255) / 256;
   int blocks = static_cast<int>(nb < 4096 ? nb : 4096);
   if (blocks < 1) blocks = 1;

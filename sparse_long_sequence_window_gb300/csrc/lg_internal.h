@@ -55,6 +55,7 @@ struct TcParams {
   float* part_acc;                // [BH, n_glob, n_parts, D] unnormalised partial outputs
   float* part_ml;                 // [BH, n_glob, n_parts, 2] partial (max, sum), max in log2 units
   const int* gidx;                // Longformer global positions (device), for band de-duplication
+  const int* gcount;              // Longformer: gcount[x] = number of global positions < x, x in [0, N]
   int* status;
   long long wait_cap;             // clock64 cycles a bounded wait may spin
   float scale_log2;               // scale * log2(e)
@@ -85,6 +86,7 @@ struct PrepParams {
   const int* gidx; int n_glob; int N;
   const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;  // NULL: validate only
   __nv_bfloat16* qg; __nv_bfloat16* kg; __nv_bfloat16* vg;                 // [BH, g, D]
+  int* gcount;                                                              // [N + 1] or NULL
   int BH, D;
   int* status;
 };

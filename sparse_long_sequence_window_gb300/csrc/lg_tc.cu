@@ -48,7 +48,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only whe
 constexpr float kLn2 = 0.6931471805599453f;
 
 #ifndef LG_TC_KSTAGES128
-#define LG_TC_KSTAGES128 3
+#define LG_TC_KSTAGES128 2
 #endif
 #ifndef LG_TC_POLY_SHIFT
 #define LG_TC_POLY_SHIFT 0   // one exp2 in 2^shift columns runs on the FMA pipe (0: none)
@@ -184,16 +184,6 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   if (a > b) return 0u;
   const uint32_t upper = (b >= 31) ? 0xFFFFFFFFu : ((1u << (b + 1)) - 1u);
   return upper & ~((1u << a) - 1u);
-}
-
-// First index in the sorted list g[0..n) whose value is >= x.
-__device__ __forceinline__ int lower_bound_dev(const int* g, int n, long long x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (static_cast<long long>(__ldg(g + mid)) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -514,12 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       // Global keys (Longformer) already inside this row's band are masked in
       // the global tiles, so they count once.  The global list is sorted, so
       // they have list indices in [g_a, g_b): the positions in [pos_q -
-      // d*w_left, pos_q + d*w_right]; for d > 1 only those on the row's stride
-      // lattice.
+      // d*w_left, pos_q + d*w_right] (for d > 1 only those on the row's
+      // stride lattice); gcount[x] = number of global positions below x.
       int g_a = 0, g_b = 0;
       if (!w.grow && !p.etc && p.n_glob > 0 && row_valid) {
-        g_a = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl);
-        g_b = lower_bound_dev(p.gidx, p.n_glob, static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1);
+        const long long a = static_cast<long long>(pos_q) - static_cast<long long>(w.d) * p.wl;
+        const long long b = static_cast<long long>(pos_q) + static_cast<long long>(w.d) * p.wr + 1;
+        g_a = __ldg(p.gcount + (a < 0 ? 0 : (a > p.N ? p.N : a)));
+        g_b = __ldg(p.gcount + (b < 0 ? 0 : (b > p.N ? p.N : b)));
       }
       for (int j = 0; j < T; ++j) {
         if (!tv.uses(j)) continue;
