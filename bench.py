@@ -173,11 +173,12 @@ def launches_per_call(w):
     if w.dtype == "f32":
         return 2 if (not w.is_etc and (w.global_positions or w.n_random_global)) else 1
     if w.is_etc:
-        return 2  # tensor-core kernel + merge
+        return 3  # unit table + tensor-core kernel + merge
     dil = [d for d in set(w.dilations()) if d != 1]
     groups = max(1, -(-len(dil) // 3))
     has_g = bool(w.global_positions) or w.n_random_global > 0
-    return groups + (2 if has_g else 0)
+    # per dilation group: unit table + tensor-core kernel; globals: prep + merge
+    return 2 * groups + (2 if has_g else 0)
 
 
 # ---------------------------------------------------------------------- rank bookkeeping

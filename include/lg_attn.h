@@ -78,9 +78,11 @@ const char* lg_version(void);
 
 /*
  * Bytes of device workspace lg_attn_fwd needs for these sizes.  The workspace
- * holds the device status word, the gathered global-token rows (bf16) and the
- * partial softmax statistics of the global-query rows.  It must be 256-byte
- * aligned.  Returns 0 if the sizes are invalid.
+ * holds the device status word and, for bf16, the gathered global-token rows,
+ * a table of global-position counts (N + 1 ints), the partial softmax
+ * statistics of the global-query rows and a table of work-unit records (64
+ * bytes per unit, written by the call itself).  It must be 256-byte aligned.
+ * Returns 0 if the sizes are invalid.
  */
 size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_dtype dt);
 

@@ -92,11 +92,19 @@ GrowPlan grow_plan(int n_glob, int key_tiles) {
 }
 
 struct WsLayout {
-  size_t qg = 0, kg = 0, vg = 0, cnt = 0, acc = 0, ml = 0, total = kStatusBytes;
+  size_t qg = 0, kg = 0, vg = 0, cnt = 0, acc = 0, ml = 0, units = 0, max_units = 0, total = kStatusBytes;
 };
 
+// Work units of one tensor-core launch, at most: band units (per head at most
+// ceil(rows / 256) plus one per residue class) and the global-row units.
+long long max_units(int BH, int rows, int max_dil, const GrowPlan& g) {
+  return static_cast<long long>(BH) * (cdiv(rows, 2 * kTileM) + max_dil) +
+         static_cast<long long>(BH) * g.n_gtiles * g.n_splits;
+}
+
 // gather (Longformer): gathered global rows and the gcount table of N + 1 ints.
-WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N) {
+// Then the partial sums of the global rows and the unit table (16 ints per unit).
+WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N, long long units) {
   WsLayout w;
   size_t off = kStatusBytes;
   if (n_glob > 0) {
@@ -110,6 +118,9 @@ WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N) 
     w.acc = off; off += round_up(static_cast<size_t>(BH) * n_glob * n_splits * D * 4, 256);
     w.ml = off; off += round_up(static_cast<size_t>(BH) * n_glob * n_splits * 2 * 4, 256);
   }
+  w.units = off;
+  w.max_units = static_cast<size_t>(units);
+  off += round_up(static_cast<size_t>(units) * 64, 256);
   w.total = off;
   return w;
 }
@@ -179,14 +190,14 @@ size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_d
   if (B < 1 || H < 1 || N < 1 || D < 1 || n_global < 0 || n_global > N || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(n_global, cdiv(N, kTileN));
-  return ws_layout(B * H, n_global, D, g.n_parts, true, N).total;
+  return ws_layout(B * H, n_global, D, g.n_parts, true, N, max_units(B * H, N, LG_MAX_BF16_DILATION, g)).total;
 }
 
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || G < 1 || D < 1 || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
   const GrowPlan g = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  return ws_layout(B * H, G, D, g.n_parts, false, 0).total;
+  return ws_layout(B * H, G, D, g.n_parts, false, 0, max_units(B * H, L, 1, g)).total;
 }
 
 lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
@@ -242,7 +253,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   // ---- bf16 tensor-core path
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(n_global, cdiv(N, kTileN));
-  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true, N);
+  const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true, N, max_units(BH, N, LG_MAX_BF16_DILATION, gp));
   __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(ws + lay.qg);
   __nv_bfloat16* kg = reinterpret_cast<__nv_bfloat16*>(ws + lay.kg);
   __nv_bfloat16* vg = reinterpret_cast<__nv_bfloat16*>(ws + lay.vg);
@@ -313,6 +324,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.n_grow_units = (grp == 0 && n_global > 0) ? BH * gp.n_gtiles * gp.n_splits : 0;
     const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
     if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
+    if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
+    tp.units = ws + lay.units;
     if ((e = prof_mark(stream, true)) != cudaSuccess) return LG_ERR_CUDA;
     if ((e = launch_tc(tp, static_cast<int>(units), stream)) != cudaSuccess) return LG_ERR_CUDA;
     if ((e = prof_mark(stream, false)) != cudaSuccess) return LG_ERR_CUDA;
@@ -367,7 +380,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
 
   if (!encode_fn()) return LG_ERR_CUDA;
   const GrowPlan gp = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
-  const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0);
+  const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0, max_units(BH, L, 1, gp));
   static TcParams tp;
   tp = TcParams{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
@@ -396,6 +409,8 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.n_grow_units = BH * gp.n_gtiles * gp.n_splits;
   const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * tp.band_units_per_batch;
   if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
+  if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
+  tp.units = ws + lay.units;
   if ((e = prof_mark(stream, true)) != cudaSuccess) return LG_ERR_CUDA;
   if ((e = launch_tc(tp, static_cast<int>(units), stream)) != cudaSuccess) return LG_ERR_CUDA;
   if ((e = prof_mark(stream, false)) != cudaSuccess) return LG_ERR_CUDA;

@@ -54,6 +54,7 @@ struct TcParams {
   float* lse;                     // [BH, N]
   float* part_acc;                // [BH, n_glob, n_parts, D] unnormalised partial outputs
   float* part_ml;                 // [BH, n_glob, n_parts, 2] partial (max, sum), max in log2 units
+  void* units;                    // [n_units, 16] int unit records (workspace), written before the kernel
   const int* gidx;                // Longformer global positions (device), for band de-duplication
   const int* gcount;              // Longformer: gcount[x] = number of global positions < x, x in [0, N]
   int* status;

@@ -88,7 +88,9 @@ struct Unit {
   int active[2];
 };
 
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+// Unit u from its index (the arithmetic behind the unit table: a scan over
+// heads and residue classes, with divisions; run once per unit per call).
+__device__ Unit decode_unit_slow(const TcParams& p, int u) {
   Unit w{};
   if (u < p.n_grow_units) {
     w.grow = 1;
@@ -134,6 +136,45 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     w.first[q] = (klo - w.band_lo) / kTileN;
     w.last[q] = (khi - w.band_lo) / kTileN;
   }
+  return w;
+}
+
+// Unit records: 16 ints per unit, built once per launch by unit_table_kernel,
+// so that a CTA reads a unit with four 16-byte loads.
+__global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_units) {
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+    const Unit w = decode_unit_slow(p, u);
+    int4* rec = reinterpret_cast<int4*>(p.units) + 4 * static_cast<size_t>(u);
+    const int flags = w.grow | (w.slot << 1) | (w.active[0] << 4) | (w.active[1] << 5) | (w.d << 8) | (w.c << 16);
+    rec[0] = make_int4(w.bh, flags, w.t0, w.n_c);
+    rec[1] = make_int4(w.band_lo, w.n_band, w.kt0, w.grow0);
+    rec[2] = make_int4(w.n_tiles, w.first[0], w.first[1], w.last[0]);
+    rec[3] = make_int4(w.last[1], 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+  const int4* rec = reinterpret_cast<const int4*>(p.units) + 4 * static_cast<size_t>(u);
+  const int4 a = __ldg(rec), b = __ldg(rec + 1), c = __ldg(rec + 2), d = __ldg(rec + 3);
+  Unit w;
+  w.bh = a.x;
+  w.grow = a.y & 1;
+  w.slot = (a.y >> 1) & 7;
+  w.active[0] = (a.y >> 4) & 1;
+  w.active[1] = (a.y >> 5) & 1;
+  w.d = (a.y >> 8) & 255;
+  w.c = (a.y >> 16) & 255;
+  w.t0 = a.z;
+  w.n_c = a.w;
+  w.band_lo = b.x;
+  w.n_band = b.y;
+  w.kt0 = b.z;
+  w.grow0 = b.w;
+  w.n_tiles = c.x;
+  w.first[0] = c.y;
+  w.first[1] = c.z;
+  w.last[0] = c.w;
+  w.last[1] = d.x;
   return w;
 }
 
@@ -714,6 +755,7 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       attr_done[0] = true;
     }
+    unit_table_kernel<<<(n_units + 255) / 256, 256, 0, s>>>(p, n_units);
     tc_attn_kernel<64><<<grid_for(n_units), kThreads, Cfg<64>::kSmem, s>>>(p, n_units);
   } else {
     if (!attr_done[1]) {
@@ -721,6 +763,7 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       attr_done[1] = true;
     }
+    unit_table_kernel<<<(n_units + 255) / 256, 256, 0, s>>>(p, n_units);
     tc_attn_kernel<128><<<grid_for(n_units), kThreads, Cfg<128>::kSmem, s>>>(p, n_units);
   }
   return cudaGetLastError();
