@@ -64,6 +64,20 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int rows, int BH, int d
   return r == CUDA_SUCCESS;
 }
 
+// bf16 output viewed as {D, rows, BH} for tiled stores of 32 rows x 64 columns.
+bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Band work units of one head: pairs of 128-step query tiles in each residue class.
 int band_units_for(int N, int d) {
   int units = 0;
@@ -292,6 +306,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
       tp.slot_dil[sl] = 1;
       tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0];
     }
+    if (!encode_store_map(&tp.mapO, out, D, N, BH)) return LG_ERR_CUDA;
     if (n_global > 0) {
       if (!encode_map(&tp.mapQg, qg, D, n_global, BH, 0) || !encode_map(&tp.mapKg, kg, D, n_global, BH, 0) ||
           !encode_map(&tp.mapVg, vg, D, n_global, BH, 0))
@@ -385,7 +400,8 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp = TcParams{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
       !encode_map(&tp.mapV[0], v_l, D, L, BH, 1) || !encode_map(&tp.mapQg, q_g, D, G, BH, 0) ||
-      !encode_map(&tp.mapKg, k_g, D, G, BH, 0) || !encode_map(&tp.mapVg, v_g, D, G, BH, 0))
+      !encode_map(&tp.mapKg, k_g, D, G, BH, 0) || !encode_map(&tp.mapVg, v_g, D, G, BH, 0) ||
+      !encode_store_map(&tp.mapO, out_l, D, L, BH))
     return LG_ERR_CUDA;
   for (int sl = 1; sl < kMaxSlots; ++sl) {
     tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.slot_dil[sl] = 1;

@@ -62,7 +62,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;                        // two query tiles
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffMisc = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // output staging, 4 KB per softmax warp
+  static constexpr int kOffMisc = kOffStage + 8 * 4096;
   static constexpr int kMiscBytes = 1024;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
   static constexpr uint32_t kColS = 0;                   // S_q at q * 128
@@ -677,8 +678,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         mbar_arrive(bar(B_OFREE + q));                  // O may be overwritten by the next unit
         ++nact;
         if (!w.grow) {
-          if (row_valid) {
-            const float inv_l = 1.f / l_run;
+          const float inv_l = row_valid ? 1.f / l_run : 0.f;
+          if (w.d == 1) {
+            // Consecutive rows: each warp stages its 32 rows, 64 columns at a
+            // time, in shared memory (128-byte swizzle, conflict-free) and
+            // writes them with one TMA store per 64 columns; rows past the
+            // end of the sequence are clipped by the store.
+            const uint32_t stage = sbase + C::kOffStage + (warp - 4) * 4096;
+            const int row0 = w.c + w.t0 + q * kTileM + 32 * (warp & 3);
+#pragma unroll
+            for (int half = 0; half < D / 64; ++half) {
+              if (lane == 0) bulk_wait_read_all();   // this buffer's previous store has read it
+              __syncwarp();
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float* v = o + half * 64 + 8 * c;
+                st_shared_v4(stage + lane * 128 + ((c ^ (lane & 7)) << 4), pack_bf16x2(v[0] * inv_l, v[1] * inv_l),
+                             pack_bf16x2(v[2] * inv_l, v[3] * inv_l), pack_bf16x2(v[4] * inv_l, v[5] * inv_l),
+                             pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&p.mapO, stage, half * 64, row0, w.bh);
+                bulk_commit_group();
+              }
+            }
+          } else if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
                                                   (static_cast<size_t>(w.bh) * p.N + pos_q) * D);
 #pragma unroll
@@ -690,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
               val.w = pack_bf16x2(o[8 * k + 6] * inv_l, o[8 * k + 7] * inv_l);
               dst[k] = val;
             }
-            p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
           }
+          if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
         } else if (row_valid) {
           const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;   // partial slot of this warpgroup
           const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
@@ -709,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     }
   }
 
+  if (warp >= 4 && lane == 0) bulk_wait_all();   // output stores issued by this warp have completed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
