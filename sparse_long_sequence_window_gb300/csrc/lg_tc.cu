@@ -445,8 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           ++q_seen;
           q_ready = true;
         }
-        const bool turn = (q == 0) ? ((j >= 1) & tv.uses(j - 1) & tvo.uses(j - 1)) : tvo.uses(j);
-        const int need_other = q == 0 ? g - 1 : g;
+        // Band units: both tiles use the same key tiles; global-row units: the
+        // tiles take alternate key tiles, and each follows the other's previous one.
+        const bool turn = w.grow ? (j >= 1)
+                                 : ((q == 0) ? ((j >= 1) & tv.uses(j - 1) & tvo.uses(j - 1)) : tvo.uses(j));
+        const int need_other = (w.grow || q == 0) ? g - 1 : g;
         if (turn && issued[1 - q] < need_other) {
           const long long t0 = clock64();
           while (issued[1 - q] < need_other) {
