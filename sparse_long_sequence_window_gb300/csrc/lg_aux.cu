@@ -12,9 +12,7 @@
 //    kept in log2 units).  This is the softmax-denominator weighting of
 //    "LONGNET: Scaling Transformers to 1,000,000,000 Tokens", section 3.4,
 //    "Mixture of Dilated Attentions", which equals one joint softmax over the
-//    union of the key splits.  One warp per global row: lanes split the
-//    partials for the max and the sum (shuffle reductions) and the
-//    dimensions for the output.
+//    union of the key splits.  One block per global row (see merge_kernel).
 #include <math.h>
 
 #include "lg_internal.h"
@@ -61,54 +59,82 @@ __global__ void prep_kernel(const PrepParams p) {
   }
 }
 
+// One block of 128 threads per global row.  Pass 1: the row's maximum and
+// sum over the partials (threads stride over the partials, block
+// reductions).  Pass 2: the weights 2^(m_p - m) of a chunk of partials go to
+// shared memory and each thread accumulates one output column over the
+// chunk (for D = 64, two groups of threads take alternate partials and add
+// up at the end), so the loads of consecutive partials are independent.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeChunk = 1024;
+
 template <int D>
-__global__ void merge_kernel(const MergeParams p, int bf16_out) {
-  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= static_cast<long long>(p.BH) * p.n_glob) return;
-  const int bh = static_cast<int>(wid / p.n_glob);
-  const int r = static_cast<int>(wid % p.n_glob);
-  const size_t base = static_cast<size_t>(wid) * p.n_splits;
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p, int bf16_out) {
+  constexpr int G = kMergeThreads / D;  // thread groups over the partials
+  __shared__ float wgt[kMergeChunk];
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float part[G > 1 ? G * D : 1];
+  const long long row_id = blockIdx.x;
+  const int bh = static_cast<int>(row_id / p.n_glob);
+  const int r = static_cast<int>(row_id % p.n_glob);
+  const int tid = threadIdx.x, lane = tid & 31, wrp = tid >> 5;
+  const size_t base = static_cast<size_t>(row_id) * p.n_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base;
 
   float m = -INFINITY;
-  for (int s = lane; s < p.n_splits; s += 32) m = fmaxf(m, ml[s].x);
+  for (int s = tid; s < p.n_splits; s += kMergeThreads) m = fmaxf(m, ml[s].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[wrp] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
   float l = 0.f;
-  for (int s = lane; s < p.n_splits; s += 32) {
+  for (int s = tid; s < p.n_splits; s += kMergeThreads) {
     const float2 v = ml[s];
     if (v.x != -INFINITY) l += exp2f(v.x - m) * v.y;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if (lane == 0) red[wrp] = l;
+  __syncthreads();
+  l = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) l += red[w];
 
-  constexpr int PER = D / 32;
-  float acc[PER];
+  const int col = tid % D, grp = tid / D;
+  float acc = 0.f;
+  for (int c0 = 0; c0 < p.n_splits; c0 += kMergeChunk) {
+    const int n = min(kMergeChunk, p.n_splits - c0);
+    __syncthreads();
+    for (int s = tid; s < n; s += kMergeThreads) {
+      const float2 v = ml[c0 + s];
+      wgt[s] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - m);  // empty partials hold no sums
+    }
+    __syncthreads();
+    const float* a = p.part_acc + (base + c0) * D + col;
+#pragma unroll 4
+    for (int s = grp; s < n; s += G) {
+      const float wv = wgt[s];
+      if (wv != 0.f) acc = fmaf(wv, a[static_cast<size_t>(s) * D], acc);
+    }
+  }
+  if (G > 1) {
+    part[grp * D + col] = acc;
+    __syncthreads();
+    if (grp != 0) return;
 #pragma unroll
-  for (int t = 0; t < PER; ++t) acc[t] = 0.f;
-  for (int s = 0; s < p.n_splits; ++s) {
-    const float2 v = ml[s];
-    if (v.x == -INFINITY) continue;
-    const float wgt = exp2f(v.x - m);
-    const float* a = p.part_acc + (base + s) * D;
-#pragma unroll
-    for (int t = 0; t < PER; ++t) acc[t] = fmaf(wgt, a[lane + 32 * t], acc[t]);
+    for (int g2 = 1; g2 < G; ++g2) acc += part[g2 * D + col];
   }
   const int row = p.gidx ? p.gidx[r] : r;
   if (row < 0 || row >= p.N_out) return;
   const float inv_l = 1.f / l;
   const size_t orow = (static_cast<size_t>(bh) * p.N_out + row) * D;
-  if (bf16_out) {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + orow;
-#pragma unroll
-    for (int t = 0; t < PER; ++t) o[lane + 32 * t] = __float2bfloat16_rn(acc[t] * inv_l);
-  } else {
-    float* o = reinterpret_cast<float*>(p.out) + orow;
-#pragma unroll
-    for (int t = 0; t < PER; ++t) o[lane + 32 * t] = acc[t] * inv_l;
-  }
-  if (lane == 0) p.lse[static_cast<size_t>(bh) * p.N_out + row] = (m + log2f(l)) * 0.6931471805599453f;
+  if (bf16_out) reinterpret_cast<__nv_bfloat16*>(p.out)[orow + col] = __float2bfloat16_rn(acc * inv_l);
+  else reinterpret_cast<float*>(p.out)[orow + col] = acc * inv_l;
+  if (col == 0) p.lse[static_cast<size_t>(bh) * p.N_out + row] = (m + log2f(l)) * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -125,11 +151,12 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s) {
-  const long long warps = static_cast<long long>(p.BH) * p.n_glob;
-  if (warps <= 0) return cudaSuccess;
-  const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
-  if (p.D == 64) merge_kernel<64><<<blocks, 256, 0, s>>>(p, bf16_out);
-  else if (p.D == 128) merge_kernel<128><<<blocks, 256, 0, s>>>(p, bf16_out);
+  const long long rows = static_cast<long long>(p.BH) * p.n_glob;
+  if (rows <= 0) return cudaSuccess;
+  if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned blocks = static_cast<unsigned>(rows);
+  if (p.D == 64) merge_kernel<64><<<blocks, kMergeThreads, 0, s>>>(p, bf16_out);
+  else if (p.D == 128) merge_kernel<128><<<blocks, kMergeThreads, 0, s>>>(p, bf16_out);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

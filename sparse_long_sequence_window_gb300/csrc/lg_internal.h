@@ -21,7 +21,7 @@ enum : int {
 constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace
 constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;              // keys per tile
-constexpr int kGrowSplitTiles = 16;      // key tiles per split of a global-query row block (two partials)
+constexpr int kGrowSplitTiles = 32;      // key tiles per split of a global-query row block (two partials)
 constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
 
 // ---------------------------------------------------------------- fp32 CUDA-core path
