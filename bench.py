@@ -354,7 +354,7 @@ def sweep(lg, torch, dev):
 
 
 def committed_traffic(w):
-    """DRAM bytes per launch from a committed ncu capture of the current kernel source, else None."""
+    """DRAM bytes per launch from a committed ncu capture of the current kernel sources, else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -362,8 +362,10 @@ def committed_traffic(w):
         import hashlib
         with open(path) as f:
             rec = json.load(f)
-        src = os.path.join(ROOT, "sparse_long_sequence_window_gb300", "csrc", "lg_tc.cu")
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for name in ("lg_tc.cu", "lg_internal.h", "lg_ptx.cuh"):
+            h.update(open(os.path.join(ROOT, "sparse_long_sequence_window_gb300", "csrc", name), "rb").read())
+        digest = h.hexdigest()[:16]
         ent = rec.get(w.name)
         if ent and ent.get("kernel_sha") == digest:
             return ent.get("dram_bytes_per_launch")
