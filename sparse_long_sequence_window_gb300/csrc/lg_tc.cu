@@ -66,8 +66,15 @@ struct Cfg {
   static constexpr int kOffMisc = kOffStage + 8 * 4096;
   static constexpr int kMiscBytes = 1024;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
-  static constexpr uint32_t kColS = 0;                   // S_q at q * 128
-  static constexpr uint32_t kColO = 256;                 // O_q at 256 + q * D
+  // TMEM columns.  D = 128: S_q at 128 q (P_q over its first 64 columns), O_q
+  // at 256 + 128 q.  D = 64: S_q at 128 q, P_q in its own 64 columns at
+  // 256 + 64 q, O_q at 384 + 64 q, so QK_q of the next key tile can run while
+  // the softmax of the current one is still writing P.
+  static constexpr bool kSplitP = (D == 64);
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColP = kSplitP ? 256 : 0;
+  static constexpr uint32_t kPStride = kSplitP ? 64 : 128;
+  static constexpr uint32_t kColO = kSplitP ? 384 : 256;
 };
 
 // Rows one strided TMA box delivers for a dilation d (box height R*d <= 256).
@@ -270,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int B_QFULL = 0, B_KFULL = 2, B_KEMPTY = B_KFULL + KS, B_VFULL = B_KEMPTY + KS,
                 B_VEMPTY = B_VFULL + VS, B_SFULL = B_VEMPTY + VS, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-                B_OFREE = B_ODONE + 2, B_FIN = B_OFREE + 2, NBARS = B_FIN + 2;
+                B_OFREE = B_ODONE + 2, B_FIN = B_OFREE + 2, B_SEMPTY = B_FIN + 2, B_PEMPTY = B_SEMPTY + 2,
+                NBARS = B_PEMPTY + 2;
   static_assert(NBARS * 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -285,7 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     issued[1] = -1;
     for (int i = 0; i < NBARS; ++i) {
       uint32_t count = 1;
-      if (i == B_PFULL || i == B_PFULL + 1 || i == B_OFREE || i == B_OFREE + 1) count = 128;
+      if (i == B_PFULL || i == B_PFULL + 1 || i == B_OFREE || i == B_OFREE + 1 || i == B_SEMPTY ||
+          i == B_SEMPTY + 1)
+        count = 128;
       // K/V stages are released by both MMA issuers (one arrival each).
       if ((i >= B_KEMPTY && i < B_KEMPTY + KS) || (i >= B_VEMPTY && i < B_VEMPTY + VS)) count = 2;
       mbar_init(bar(i), count);
@@ -384,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
     const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
     const uint32_t tS = tmem + C::kColS + q * 128;
+    const uint32_t tP = tmem + C::kColP + q * C::kPStride;
     const uint32_t tO = tmem + C::kColO + q * D;
     int g = 0, ks = 0, kph = 0;   // key tiles seen (all units), K stage of tile g and its phase parity
     int ns = 0;                   // QKs issued
@@ -417,15 +428,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         if (!wait_or_fail(B_VFULL + (pend_g & (VS - 1)), (pend_g / VS) & 1)) return false;
         return !(first_pv && nact > 0) || wait_or_fail(B_OFREE + q, (nact - 1) & 1);
       };
-      // O_q += P_q V(pend), P read from TMEM (the first 64 columns of S_q); leader only.
+      // O_q += P_q V(pend), P read from TMEM; leader only.
       auto pv_mmas = [&]() {
         const int vs = pend_g & (VS - 1);
         const uint64_t dv = dV0 + vs * kStage;
-        umma_bf16_ts(tO, tS, dv, kIdPV, first_pv ? 0u : 1u);
+        umma_bf16_ts(tO, tP, dv, kIdPV, first_pv ? 0u : 1u);
 #pragma unroll
-        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tS + kk * 8, dv + kk * 128, kIdPV, 1u);
+        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tP + kk * 8, dv + kk * 128, kIdPV, 1u);
         if (pend == last) umma_commit(bar(B_ODONE + q));
         umma_commit(bar(B_VEMPTY + vs));
+        if (C::kSplitP) umma_commit(bar(B_PEMPTY + q));   // P_q may be rewritten, O_q rescaled
+      };
+      // S_q = Q_q K(g)^T; leader only.
+      auto qk_mmas = [&]() {
+        const uint64_t dk = dK0 + ks * kStage;
+        umma_bf16_ss(tS, dQ, dk, kIdQK, 0u);
+#pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (kTileM * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tS, dQ + o, dk + o, kIdQK, 1u);
+        }
+        umma_commit(bar(B_SFULL + q));
+        umma_commit(bar(B_KEMPTY + ks));
       };
       for (int j = 0; j < w.n_tiles; ++j, ++g) {
         if (!wait_or_fail(B_KFULL + ks, kph)) break;
@@ -437,6 +461,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           if (leader) mbar_arrive(bar(B_VEMPTY + vs));
           __syncwarp();
           if (++ks == KS) { ks = 0; kph ^= 1; }
+          continue;
+        }
+        if (C::kSplitP) {
+          // QK_q(j) as soon as the softmax has read the previous S_q, then the
+          // pending PV once its P is written.
+          if (ns > 0 && !wait_or_fail(B_SEMPTY + q, (ns - 1) & 1)) break;
+          if (!q_ready) {
+            if (!wait_or_fail(B_QFULL + q, q_seen & 1)) break;
+            ++q_seen;
+            q_ready = true;
+          }
+          tc_fence_after();
+          if (leader) qk_mmas();
+          __syncwarp();
+          ++ns;
+          if (pend >= 0) {
+            if (!pv_waits() || !wait_or_fail(B_PFULL + q, npv & 1)) break;
+            tc_fence_after();
+            if (leader) pv_mmas();
+            __syncwarp();
+            first_pv = false;
+            ++npv;
+          }
+          pend = j;
+          pend_g = g;
+          if (++ks == KS) { ks = 0; kph ^= 1; }
+          if (j == last && un < n_units) {
+            if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
+            if (leader) load_q(q, decode_unit(p, un));
+            __syncwarp();
+            ++q_loads;
+          }
           continue;
         }
         if (pend >= 0 && !pv_waits()) break;
@@ -465,15 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         tc_fence_after();
         if (leader) {
           if (pend >= 0) pv_mmas();
-          const uint64_t dk = dK0 + ks * kStage;
-          umma_bf16_ss(tS, dQ, dk, kIdQK, 0u);
-#pragma unroll
-          for (int kk = 1; kk < D / 16; ++kk) {
-            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (kTileM * 128) + (kk & 3) * 32) >> 4);
-            umma_bf16_ss(tS, dQ + o, dk + o, kIdQK, 1u);
-          }
-          umma_commit(bar(B_SFULL + q));
-          umma_commit(bar(B_KEMPTY + ks));
+          qk_mmas();
           issued[q] = g;
         }
         __syncwarp();
@@ -526,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     const int r = threadIdx.x & 127;                    // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS + q * 128;
+    const uint32_t tP = tmem + lane_off + C::kColP + q * C::kPStride;
     const uint32_t tO = tmem + lane_off + C::kColO + q * D;
     const float sl2 = p.scale_log2;
     int ns = 0;                                         // tiles processed (all units)
@@ -579,11 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
                                                  : p.N - (kt - (p.etc ? gt_src : 0)) * kTileN;
         hi = min(kTileN, limit) - 1;
       }
-      uint32_t keep[4];
+      // In-band global columns [ca, cb) of a Longformer global tile.
+      const int ca = jj0 >= 0 ? max(g_a - jj0, 0) : 0, cb = jj0 >= 0 ? min(g_b - jj0, kTileN) : 0;
+      // Most tiles need no mask in any row of the warp: decided from lo, hi and
+      // [ca, cb) before any per-column work.
+      const bool need_mask = __any_sync(0xffffffffu, (lo > 0) | (hi < kTileN - 1) | (ca < cb));
+      uint32_t keep[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+      if (need_mask) {
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) keep[wd] = range_bits(lo, hi, 32 * wd);
-      if (jj0 >= 0) {
-        const int ca = max(g_a - jj0, 0), cb = min(g_b - jj0, kTileN);  // in-band columns [ca, cb)
+        for (int wd = 0; wd < 4; ++wd) keep[wd] = range_bits(lo, hi, 32 * wd);
         if (ca < cb) {
           if (w.d == 1) {
 #pragma unroll
@@ -601,18 +654,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           }
         }
       }
-      const bool full = (keep[0] & keep[1] & keep[2] & keep[3]) == 0xFFFFFFFFu;
-      const bool need_mask = __any_sync(0xffffffffu, !full);
 
       if (!wait_all(bar(B_SFULL + q), ns & 1)) { fail(); ok = false; break; }
       tc_fence_after();
       float s[kTileN];
       tmem_ld128(tS, s);
+      if (C::kSplitP) {
+        tc_fence_before();
+        mbar_arrive(bar(B_SEMPTY + q));                 // S_q may take the next QK
+      }
 
       if (need_mask) {
+        // Per 32-column word: nothing to do when every row of the warp keeps
+        // it, a per-column select otherwise.
 #pragma unroll
-        for (int col = 0; col < kTileN; ++col)
-          s[col] = ((keep[col >> 5] >> (col & 31)) & 1u) ? s[col] : -INFINITY;
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint32_t kw = keep[wd];
+          if (!__all_sync(0xffffffffu, kw == 0xFFFFFFFFu)) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) s[32 * wd + c] = ((kw >> c) & 1u) ? s[32 * wd + c] : -INFINITY;
+          }
+        }
       }
       float mx[8];
 #pragma unroll
@@ -650,9 +712,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const float psum = (a0 + a1) + (b0 + b1);
       l_run = l_run * corr + psum;
       m_run = m_new;
-      // O_q is idle here: PV_q of the previous tile finished before QK_q of
-      // this one (same issuing thread, in order), and PV_q of this tile waits
-      // for P_q below.
+      // O_q is idle here: PV_q of the previous tile has finished (D = 128:
+      // it was issued before QK_q of this tile by the same thread; D = 64: its
+      // commit is waited for below, which also frees P_q), and PV_q of this
+      // tile waits for P_q.
+      if (C::kSplitP && ns > 0) {
+        if (!wait_all(bar(B_PEMPTY + q), (ns - 1) & 1)) { fail(); ok = false; break; }
+        tc_fence_after();
+      }
       if (__any_sync(0xffffffffu, need_rescale)) {
         const float f = need_rescale ? corr : 1.f;
 #pragma unroll 1
@@ -664,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           tmem_st32(tO + cc * 32, o);
         }
       }
-      tmem_st64(tS, pk);                                 // P_q over the first 64 columns of S_q
+      tmem_st64(tP, pk);
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + q));
       ++ns;
