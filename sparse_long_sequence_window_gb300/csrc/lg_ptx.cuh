@@ -273,24 +273,6 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64
       : "memory");
 }
 
-// 2^x on the FMA/ALU pipes only (no conversion instructions), for -125 <= x
-// <= 8 (smaller x gives about 2^-125).  Range reduction by the round-to-
-// nearest trick: adding 1.5 * 2^23 leaves n = rint(x) in the low mantissa
-// bits, so t - 1.5 * 2^23 = n and bits(t) << 23 = n << 23 (mod 2^32); f = x - n
-// lies in [-1/2, 1/2].  2^f = e^(f ln 2) by its Taylor series to degree 4:
-// the relative error is below (ln2 / 2)^5 / 5! / 2^(-1/2) = 6e-5.  The result
-// is assembled by adding n to the exponent field of 2^f.
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -125.0f);
-  const float t = x + 12582912.0f;
-  const float f = x - (t - 12582912.0f);
-  float p = fmaf(0.009618129107628477f, f, 0.05550410866482158f);
-  p = fmaf(p, f, 0.2402265069591007f);
-  p = fmaf(p, f, 0.6931471805599453f);
-  p = fmaf(p, f, 1.0f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 // Register budget of a warpgroup (all four warps execute it).
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {

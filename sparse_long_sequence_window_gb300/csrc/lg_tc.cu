@@ -50,9 +50,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 #ifndef LG_TC_KSTAGES128
 #define LG_TC_KSTAGES128 2
 #endif
-#ifndef LG_TC_POLY_SHIFT
-#define LG_TC_POLY_SHIFT 0   // one exp2 in 2^shift columns runs on the FMA pipe (0: none)
-#endif
 
 template <int D>
 struct Cfg {
@@ -219,12 +216,6 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, bool strided, 
                   y0 + piece * R * (strided ? d : 1), bh);
     }
   }
-}
-
-// Columns of the 128-wide tile whose exp2 goes to the FMA pipe (one in
-// 2^LG_TC_POLY_SHIFT), the rest to the MUFU.
-__host__ __device__ constexpr bool poly_col(int col) {
-  return LG_TC_POLY_SHIFT > 0 && (col & ((1 << LG_TC_POLY_SHIFT) - 1)) == (1 << LG_TC_POLY_SHIFT) - 1;
 }
 
 // Bits of the columns [lo, hi] that fall in the 32-column word starting at `base`.
@@ -701,8 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       for (int i = 0; i < kTileN / 2; ++i) {
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
-        const float p0 = poly_col(2 * i) ? exp2_poly(x0) : ex2_approx(x0);
-        const float p1 = poly_col(2 * i + 1) ? exp2_poly(x1) : ex2_approx(x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
