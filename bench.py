@@ -353,6 +353,20 @@ def sweep(lg, torch, dev):
     return res
 
 
+def kernel_source_digest():
+    """Hash of the tensor-core kernel's sources with comments and blank lines removed."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in ("lg_tc.cu", "lg_internal.h", "lg_ptx.cuh"):
+        text = open(os.path.join(ROOT, "sparse_long_sequence_window_gb300", "csrc", name)).read()
+        for line in text.splitlines():
+            code = re.sub(r"//.*", "", line).rstrip()
+            if code.strip():
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def committed_traffic(w):
     """DRAM bytes per launch from a committed ncu capture of the current kernel sources, else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -362,10 +376,7 @@ def committed_traffic(w):
         import hashlib
         with open(path) as f:
             rec = json.load(f)
-        h = hashlib.sha256()
-        for name in ("lg_tc.cu", "lg_internal.h", "lg_ptx.cuh"):
-            h.update(open(os.path.join(ROOT, "sparse_long_sequence_window_gb300", "csrc", name), "rb").read())
-        digest = h.hexdigest()[:16]
+        digest = kernel_source_digest()
         ent = rec.get(w.name)
         if ent and ent.get("kernel_sha") == digest:
             return ent.get("dram_bytes_per_launch")

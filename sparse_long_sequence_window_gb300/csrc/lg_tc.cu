@@ -7,8 +7,10 @@
 // "ETC: Encoding Long and Structured Inputs in Transformers", section 3.4
 // ("Global-Local Attention", "Softmax unification").
 //
-// One CTA handles one work unit with two 128-row query tiles (q = 0, 1), each
-// owned by its own softmax warpgroup, against a list of 128-key tiles:
+// The kernel is persistent: one CTA per SM walks the work units blockIdx.x,
+// blockIdx.x + gridDim.x, ... of a table built before the launch.  A unit has
+// two 128-row query tiles (q = 0, 1), each owned by its own softmax
+// warpgroup, against a list of 128-key tiles:
 //  * Band unit: query steps t0 .. t0+255 of one dilation residue class c
 //    (positions c + d*t).  Inside a class the dilated window is the contiguous
 //    step range [t - w_left, t + w_right]; the key tiles are the contiguous
@@ -19,18 +21,19 @@
 //    The global-key tiles follow; a global key already inside a row's band is
 //    masked there (it counts once).
 //  * Global-row unit: 128 global queries against one split of all keys; the
-//    two warpgroups take alternate key tiles and each writes partial softmax
-//    statistics that a merge kernel combines.
+//    two query tiles hold the same rows and take alternate key tiles, and
+//    each writes partial softmax statistics that a merge kernel combines.
 // Warp roles (384 threads): warp 0 issues the K loads, warp 2 the V loads
 // (TMA); warp 1 owns TMEM and issues the MMAs and Q loads of query tile 0,
 // warp 3 those of tile 1; warps 4..7 and 8..11 are the two softmax
-// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128 fp32 columns, reused for
-// P_q as packed bf16) and O_q (D columns) for both tiles.  The MMA order per
-// key tile j is PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j), so the tensor core
-// works on one tile while the other tile's softmax runs.  Because the MMAs
-// of one thread execute in order, the completion of QK_q(j) also means
-// PV_q(j-1) is done: the softmax may then rescale O_q and overwrite S_q with
-// P_q without further waits.
+// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128
+// fp32 columns), P_q (packed bf16, over the first 64 columns of S_q for
+// D = 128, in its own columns for D = 64) and O_q (D columns) for both tiles.
+// For D = 128 the MMA order per key tile j is PV_0(j-1), QK_0(j), PV_1(j-1),
+// QK_1(j), so the tensor core works on one tile while the other tile's
+// softmax runs; because the MMAs of one thread execute in order, the
+// completion of QK_q(j) also means PV_q(j-1) is done, and the softmax may
+// rescale O_q and overwrite S_q with P_q without further waits.
 #include "lg_internal.h"
 #include "lg_ptx.cuh"
 
@@ -369,7 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     // is released by it at once, a used one after its MMAs (commit).  The
     // issuer reloads its Q slot for the next unit as soon as its last QK of
     // the unit has completed, and a unit's first PV (which overwrites O)
-    // waits until the softmax warpgroup has read the previous unit's O.
+    // waits until the softmax warpgroup has read the previous unit's O.  For
+    // D = 64 (P in its own columns) a tile's QK_q(j) goes first, as soon as
+    // the softmax has read S_q(j-1), and PV_q(j-1) follows once P_q(j-1) is
+    // written; the tiles do not take turns there.
     // Every descriptor is precomputed: a K-major step adds 32 B (2 in 16-B
     // units) inside a 128-B row and 16 KB per 64-column block, an MN-major V
     // step adds 2 KB, a stage adds one tile; shared-memory addresses stay
