@@ -142,6 +142,44 @@ lg_status lg_attn_fwd_noalloc(const void* q, const void* k, const void* v, void*
                               int w_left, int w_right, const int32_t* dilation, int causal,
                               const int32_t* global_idx, int n_global, float scale, lg_stream_t stream);
 
+/*
+ * lg_attn_fwd on inputs and outputs in host memory, with the host<->device
+ * copies overlapped with the computation.  (Not a step of the method: the
+ * paper has no counterpart; this serves callers whose tensors live in host
+ * memory.)
+ *
+ * The (batch, head) slices are processed in n_groups groups of consecutive
+ * slices (more if a group would exceed LG_MAX_HEADS slices).  Group c's q, k,
+ * v are copied to q_d, k_d, v_d on a copy stream, its attention runs on
+ * `stream` (one lg_attn_fwd call on that group, viewed as B = 1), and its
+ * out and lse are copied back on a second copy stream, so copies of one
+ * group overlap the kernels of another.
+ *
+ *  q_h, k_h, v_h  HOST, [B, H, N, D], dtype dt, read only; should be
+ *                 page-locked (pageable memory works, without overlap).
+ *  out_h, lse_h   HOST, [B, H, N, D] and fp32 [B, H, N], written.
+ *  q_d .. lse_d   DEVICE buffers of the same shapes, owned by the caller,
+ *                 used as staging; their contents on return are unspecified.
+ *  global_idx     DEVICE pointer, as for lg_attn_fwd.
+ *  n_groups       >= 1; 1 means no overlap.
+ *  workspace      device, >= lg_attn_fwd_workspace_size(B, H, N, D, ...)
+ *                 bytes (the groups use it one after another).
+ *  Other arguments as for lg_attn_fwd.
+ *
+ * Asynchronous: returns once everything is queued; `stream` completes after
+ * the last copy back.  The library creates two CUDA streams per device on
+ * first use and keeps them.  Argument errors return before anything is
+ * queued; an error returned after that leaves out_h and lse_h unspecified.
+ * lg_query_status on the workspace reports the last group's device status (a
+ * bad global list is found by every group).
+ */
+lg_status lg_attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* out_h, float* lse_h,
+                           void* q_d, void* k_d, void* v_d, void* out_d, float* lse_d,
+                           lg_dtype dt, int B, int H, int N, int D,
+                           int w_left, int w_right, const int32_t* dilation, int causal,
+                           const int32_t* global_idx, int n_global, float scale,
+                           void* workspace, size_t workspace_bytes, int n_groups, lg_stream_t stream);
+
 /* Bytes of device workspace lg_etc_attn_fwd needs; 0 if the sizes are invalid. */
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt);
 

@@ -16,7 +16,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "LgError", "load", "attn_fwd", "etc_attn_fwd", "attn_fwd_workspace_size",
+    "LgError", "load", "attn_fwd", "attn_fwd_host", "etc_attn_fwd", "attn_fwd_workspace_size",
     "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
     "profile_begin", "profile_end", "status_string", "LIB_PATH",
 ]
@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.lg_attn_fwd.restype = i32
     lib.lg_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32,
                                 vp, sz, vp]
+    lib.lg_attn_fwd_host.restype = i32
+    lib.lg_attn_fwd_host.argtypes = [vp] * 10 + [i32] * 7 + [vp, i32, vp, i32, f32, vp, sz, i32, vp]
     lib.lg_etc_attn_fwd.restype = i32
     lib.lg_etc_attn_fwd.argtypes = [vp] * 10 + [i32] * 7 + [f32, vp, sz, vp]
     lib.lg_query_status.restype = i32
@@ -153,6 +155,46 @@ def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int
     _check(st, "lg_attn_fwd")
     attn_fwd.last_workspace = ws
     return out, lse
+
+
+def attn_fwd_host(q_h, k_h, v_h, w_left: int, w_right: int, dilation: Optional[Sequence[int]] = None,
+                  causal: bool = False, global_idx=None, scale: Optional[float] = None,
+                  out_h=None, lse_h=None, staging=None, workspace=None, n_groups: int = 4, stream=None):
+    """attn_fwd on host tensors: q_h, k_h, v_h [B, H, N, D] in (preferably pinned)
+    host memory; the library copies them in and out/lse back, overlapping the
+    copies of one group of heads with the kernels of another.  staging: the
+    device buffers (q, k, v, out, lse) it may use (allocated here if None).
+    global_idx: int32 CUDA tensor (or None).  Asynchronous on the current
+    stream; returns (out_h, lse_h).
+    """
+    import torch
+    lib = load()
+    B, H, N, D = q_h.shape
+    dil = np.ascontiguousarray(np.asarray(dilation if dilation is not None else [1] * H, dtype=np.int32))
+    if dil.size != H:
+        raise ValueError("dilation needs H entries")
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    if global_idx is not None and (global_idx.dtype != torch.int32 or not global_idx.is_cuda):
+        raise TypeError("global_idx must be an int32 CUDA tensor")
+    dt = _dtype_code(q_h)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if out_h is None:
+        out_h = torch.empty(q_h.shape, dtype=q_h.dtype, pin_memory=True)
+    if lse_h is None:
+        lse_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    if staging is None:
+        staging = tuple(torch.empty(q_h.shape, dtype=q_h.dtype, device=dev) for _ in range(4)) + (
+            torch.empty((B, H, N), dtype=torch.float32, device=dev),)
+    need = attn_fwd_workspace_size(B, H, N, D, n_global, dt)
+    ws = _workspace(need, dev, workspace)
+    st = lib.lg_attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(out_h), _ptr(lse_h),
+                              *(_ptr(x) for x in staging), dt, B, H, N, D, int(w_left), int(w_right),
+                              dil.ctypes.data, int(bool(causal)), _ptr(global_idx) if n_global else None, n_global,
+                              float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(), int(n_groups),
+                              _stream(stream))
+    _check(st, "lg_attn_fwd_host")
+    attn_fwd_host.last_workspace = ws
+    return out_h, lse_h
 
 
 def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius: int, scale: Optional[float] = None,

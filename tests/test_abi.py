@@ -137,3 +137,23 @@ def test_count_pairs_rejects_bad_lists(lib):
         lg.count_pairs(10, 1, 1, 1, False, [3, 3])
     with pytest.raises(ValueError):
         lg.count_pairs(10, 1, 1, 1, False, [11])
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    """lg_attn_fwd_host checks its arguments before queueing anything (no GPU needed)."""
+    dil = (ctypes.c_int32 * 2)(1, 1)
+
+    def call(**over):
+        a = dict(ptrs=[FAKE] * 10, dt=lg.LG_BF16, B=1, H=2, N=256, D=64, wl=8, wr=8, dil=dil, causal=0,
+                 gidx=None, ng=0, scale=0.0, ws=FAKE, wsb=1 << 30, groups=2)
+        a.update(over)
+        return lib.lg_attn_fwd_host(*a["ptrs"], a["dt"], a["B"], a["H"], a["N"], a["D"], a["wl"], a["wr"],
+                                    a["dil"], a["causal"], a["gidx"], a["ng"], a["scale"], a["ws"], a["wsb"],
+                                    a["groups"], None)
+
+    assert call(ptrs=[FAKE] * 9 + [None]) == lg.LG_ERR_INVALID_ARG
+    assert call(groups=0) == lg.LG_ERR_INVALID_ARG
+    assert call(N=0) == lg.LG_ERR_INVALID_ARG
+    assert call(dil=(ctypes.c_int32 * 2)(1, 0)) == lg.LG_ERR_INVALID_ARG
+    assert call(wsb=64) == lg.LG_ERR_WORKSPACE
+    assert call(ws=None) == lg.LG_ERR_WORKSPACE

@@ -144,3 +144,22 @@ def test_repeat_calls_are_deterministic(cuda_lib):
     o2, l2 = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, g)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("groups", [1, 4])
+def test_host_entry_matches_device_entry(cuda_lib, groups):
+    """lg_attn_fwd_host (host tensors, groups of heads overlapped with the copies)
+    gives the same bits as lg_attn_fwd on the same inputs, and both match the oracle."""
+    lg = cuda_lib
+    w = W("host entry", "bf16", 2, 3, 900, 128, 70, 40, (1, 2, 3), False, (0, 11, 500, 899))
+    inp = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    g = torch.from_numpy(inp["global_idx"]).to(dev)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o_ref, l_ref = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, g)
+    qh, kh, vh = (inp[n].pin_memory() for n in ("q", "k", "v"))
+    o_h, l_h = lg.attn_fwd_host(qh, kh, vh, w.w_left, w.w_right, w.dilations(), False, g, n_groups=groups)
+    torch.cuda.synchronize()
+    assert lg.query_status(lg.attn_fwd_host.last_workspace) == 0
+    assert torch.equal(o_h, o_ref.cpu()) and torch.equal(l_h, l_ref.cpu())
+    pu.run_longformer(cuda_lib, w)
