@@ -410,7 +410,17 @@ def committed_traffic(w):
 
 # ---------------------------------------------------------------------- CPU oracle
 
-def cpu_sample(w, budget_s, seed=1234):
+def cpu_inputs(w, seed=1234):
+    """One head's inputs for the CPU oracle (drawn once per run)."""
+    rng = np.random.default_rng(seed)
+    D, N = w.D, w.N
+    if w.is_etc:
+        G = w.etc_G
+        return [rng.standard_normal((1, 1, n, D), dtype=np.float32) for n in (N, N, N, G, G, G)]
+    return [rng.standard_normal((1, 1, N, D), dtype=np.float32) for _ in range(3)]
+
+
+def cpu_sample(w, budget_s, seed=1234, arrs=None):
     """Runs the CPU oracle on uniformly sampled rows of one head for about budget_s seconds.
 
     Returns (useful FLOPs computed, seconds, rows).
@@ -418,9 +428,10 @@ def cpu_sample(w, budget_s, seed=1234):
     from oracle import lg_oracle
     rng = np.random.default_rng(seed)
     D, N = w.D, w.N
+    if arrs is None:
+        arrs = cpu_inputs(w, seed)
     if w.is_etc:
         G = w.etc_G
-        arrs = [rng.standard_normal((1, 1, n, D), dtype=np.float32) for n in (N, N, N, G, G, G)]
         flops = 0.0; rows = 0
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < budget_s:
@@ -432,7 +443,7 @@ def cpu_sample(w, budget_s, seed=1234):
         return flops, time.perf_counter() - t0, rows
     g = workloads.global_positions(w)
     gflags = np.zeros(N, bool); gflags[g] = True
-    q, k, v = (rng.standard_normal((1, 1, N, D), dtype=np.float32) for _ in range(3))
+    q, k, v = arrs
     d = w.dilations()[0]
     flops = 0.0; rows = 0
     t0 = time.perf_counter()
@@ -455,12 +466,13 @@ def cpu_baseline(w, budget_s=15.0):
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step a bounded sample of the workload's rows."""
     w = workloads.PRESETS[args.workload]
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))  # whole run about 2.5 min
+    arrs = cpu_inputs(w)
     for _ in range(args.warmup):
-        cpu_sample(w, per_step, seed=99)
+        cpu_sample(w, per_step, seed=99, arrs=arrs)
     total_f, total_s, total_rows = 0.0, 0.0, 0
     for s in range(args.steps):
-        fl, sec, rows = cpu_sample(w, per_step, seed=1000 + s)
+        fl, sec, rows = cpu_sample(w, per_step, seed=1000 + s, arrs=arrs)
         total_f += fl; total_s += sec; total_rows += rows
     value = total_f / total_s / 1e12
     sample = (f"{total_rows} uniformly drawn query rows of one head of {w.name} over {args.steps} steps "
