@@ -288,6 +288,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
       others.push_back(dilation[h]);
   std::sort(others.begin(), others.end());
   const int n_groups = std::max(1, cdiv(static_cast<long long>(others.size()), kMaxSlots - 1));
+  static_assert(1 + (LG_MAX_HEADS + kMaxSlots - 2) / (kMaxSlots - 1) <= static_cast<int>(kStatusBytes / sizeof(int)),
+                "one unit counter per launch fits in the status area");
 
   static TcParams tp;  // large parameter block; filled per launch
   for (int grp = 0; grp < n_groups; ++grp) {
@@ -332,6 +334,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
     tp.gidx = global_idx; tp.gcount = n_global > 0 ? reinterpret_cast<const int*>(ws + lay.cnt) : nullptr;
     tp.status = status; tp.wait_cap = wait_cap_cycles();
+    tp.unit_counter = status + 1 + grp;   // one zeroed word of the status area per launch
     tp.scale_log2 = s * 1.4426950408889634f;
     tp.BH = BH; tp.H = H; tp.N = N; tp.D = D; tp.wl = wl; tp.wr = wr; tp.n_glob = n_global; tp.etc = 0;
     tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
@@ -418,6 +421,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
   tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
   tp.gidx = nullptr; tp.status = status; tp.wait_cap = wait_cap_cycles();
+  tp.unit_counter = status + 1;
   tp.scale_log2 = s * 1.4426950408889634f;
   tp.BH = BH; tp.H = H; tp.N = L; tp.D = D; tp.wl = r; tp.wr = r; tp.n_glob = G; tp.etc = 1;
   tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;

@@ -59,6 +59,7 @@ struct TcParams {
   const int* gidx;                // Longformer global positions (device), for band de-duplication
   const int* gcount;              // Longformer: gcount[x] = number of global positions < x, x in [0, N]
   int* status;
+  int* unit_counter;              // units claimed so far (zeroed before the launch)
   long long wait_cap;             // clock64 cycles a bounded wait may spin
   float scale_log2;               // scale * log2(e)
   int BH, H, N, D;                // N = L for ETC

@@ -7,8 +7,8 @@
 // "ETC: Encoding Long and Structured Inputs in Transformers", section 3.4
 // ("Global-Local Attention", "Softmax unification").
 //
-// The kernel is persistent: one CTA per SM walks the work units blockIdx.x,
-// blockIdx.x + gridDim.x, ... of a table built before the launch.  A unit has
+// The kernel is persistent: one CTA per SM claims the work units of a table
+// built before the launch one at a time from a global counter.  A unit has
 // two 128-row query tiles (q = 0, 1), each owned by its own softmax
 // warpgroup, against a list of 128-key tiles:
 //  * Band unit: query steps t0 .. t0+255 of one dilation residue class c
@@ -44,10 +44,13 @@ constexpr int kThreads = 384;
 // Register split between the warpgroups (setmaxnreg): the producer/MMA
 // warpgroup gives registers to the two softmax warpgroups.  The launch holds
 // kThreads x (registers per thread at launch); the split must fit in it.
-constexpr int kRegsControl = 64;
+constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsLaunchMin = (128 * kRegsControl + 256 * kRegsSoftmax + kThreads - 1) / kThreads;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only when the max grows more
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kUnitSlots = 4;              // ring of claimed unit indices
+constexpr int kTailRounds = 2;             // rounds of units claimed dynamically at the end
+constexpr int kUnitReaders = 11;           // V producer + two issuing warps + eight softmax warps  // log2 units; O is rescaled only when the max grows more
 constexpr float kLn2 = 0.6931471805599453f;
 
 #ifndef LG_TC_KSTAGES128
@@ -272,11 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   constexpr int B_QFULL = 0, B_KFULL = 2, B_KEMPTY = B_KFULL + KS, B_VFULL = B_KEMPTY + KS,
                 B_VEMPTY = B_VFULL + VS, B_SFULL = B_VEMPTY + VS, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                 B_OFREE = B_ODONE + 2, B_FIN = B_OFREE + 2, B_SEMPTY = B_FIN + 2, B_PEMPTY = B_SEMPTY + 2,
-                NBARS = B_PEMPTY + 2;
-  static_assert(NBARS * 8 <= 256, "barrier area");
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
-  volatile int* issued = reinterpret_cast<volatile int*>(misc + 264);  // last key tile each issuer issued a QK for
+                B_UFULL = B_PEMPTY + 2, B_UEMPTY = B_UFULL + kUnitSlots, NBARS = B_UEMPTY + kUnitSlots;
+  static_assert(NBARS * 8 <= 512, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
+  volatile int* issued = reinterpret_cast<volatile int*>(misc + 520);  // last key tile each issuer issued a QK for
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(misc + 528);  // claimed unit indices
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -292,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         count = 128;
       // K/V stages are released by both MMA issuers (one arrival each).
       if ((i >= B_KEMPTY && i < B_KEMPTY + KS) || (i >= B_VEMPTY && i < B_VEMPTY + VS)) count = 2;
+      // A unit slot is read by the V producer, both issuing warps and the eight softmax warps.
+      if (i >= B_UEMPTY && i < B_UEMPTY + kUnitSlots) count = kUnitReaders;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -307,7 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
   const long long cap = p.wait_cap;
   const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
-  const int u0 = blockIdx.x, ustep = gridDim.x;   // this CTA's units: u0, u0 + ustep, ...
+
+  // Work units (cost-ordered: global-row units first).  Turns k < k_static
+  // take the fixed unit blockIdx.x + k * gridDim.x; the units of the last
+  // rounds are claimed one at a time from a global counter, so CTAs that drew
+  // short units take more of them and the CTAs end together.  The K producer
+  // picks; the unit of a CTA's k-th turn goes to slot k % 4 of a ring in
+  // shared memory (UFULL: written; UEMPTY: every reader has it).  A slot holds
+  // -1 once the units are exhausted.  Every reader takes the slots in order,
+  // so a parity wait on a slot always refers to its latest phase.  Waits on a
+  // slot: all lanes of the calling warp (or the single thread).
+  const int k_static = max(0, n_units / static_cast<int>(gridDim.x) - kTailRounds);
+  auto slot_wait = [&](int k) -> bool {
+    return mbar_wait(bar(B_UFULL + (k % kUnitSlots)), (k / kUnitSlots) & 1, abort_flag, cap);
+  };
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -334,7 +353,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const uint32_t ring = is_k ? sK : sV;
       int g = 0, issued = 0;
       bool ok = true;
-      for (int u = u0; u < n_units && ok; u += ustep) {
+      // The K producer picks the units and publishes them; the V producer reads them.
+      auto claim = [&](int k) -> int {
+        if (k < k_static) return static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        const int c = k_static * static_cast<int>(gridDim.x) + atomicAdd(p.unit_counter, 1);
+        return c < n_units ? c : -1;
+      };
+      auto publish = [&](int k, int v) -> bool {
+        const int sl = k % kUnitSlots;
+        if (k >= kUnitSlots && !mbar_wait(bar(B_UEMPTY + sl), ((k / kUnitSlots) - 1) & 1, abort_flag, cap))
+          return false;
+        unit_ring[sl] = v;
+        mbar_arrive(bar(B_UFULL + sl));
+        return true;
+      };
+      auto take = [&](int k, int& v) -> bool {
+        if (!slot_wait(k)) return false;
+        v = unit_ring[k % kUnitSlots];
+        mbar_arrive(bar(B_UEMPTY + k % kUnitSlots));
+        return true;
+      };
+      int u = -1;
+      ok = is_k ? publish(0, u = claim(0)) : take(0, u);
+      if (!ok) fail();
+      for (int k = 0; ok && u >= 0; ++k) {
+        int un = -1;
+        if (is_k && !publish(k + 1, un = claim(k + 1))) { fail(); ok = false; break; }
         const Unit w = decode_unit(p, u);
         for (int j = 0; j < w.n_tiles; ++j, ++g) {
           const CUtensorMap* m;
@@ -347,6 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
           issued = g + 1;
         }
+        if (ok && !is_k && !take(k + 1, un)) { fail(); ok = false; }
+        u = un;
       }
       // Drain: every load issued here has landed before the CTA exits (these
       // waits ignore the abort flag and are bounded by the cap alone).
@@ -405,18 +451,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       ok = false;
       return false;
     };
-    if (u0 < n_units) {
-      if (leader) load_q(q, decode_unit(p, u0));
+    // The unit of this CTA's k-th turn (all lanes wait on the slot; -1 after a failed wait).
+    auto unit_in_slot = [&](int k) -> int {
+      if (!wait_or_fail(B_UFULL + (k % kUnitSlots), (k / kUnitSlots) & 1)) return -1;
+      const int v = unit_ring[k % kUnitSlots];
+      __syncwarp();
+      if (leader) mbar_arrive(bar(B_UEMPTY + k % kUnitSlots));   // this warp has read slot k
+      return v;
+    };
+    int u = unit_in_slot(0);
+    if (u >= 0) {
+      if (leader) load_q(q, decode_unit(p, u));
       __syncwarp();
       ++q_loads;
     }
-    for (int u = u0; u < n_units && ok; u += ustep) {
+    for (int k = 0; ok && u >= 0; ++k) {
+      // The next unit is published before this unit's first K tile is loaded.
+      const int un = unit_in_slot(k + 1);
+      if (!ok) break;
       const Unit w = decode_unit(p, u);
       const TileView tv = tile_view(w, q), tvo = tile_view(w, 1 - q);
       int last = -1;
       for (int j = w.n_tiles - 1; j >= 0; --j)
         if (tv.uses(j)) { last = j; break; }
-      const int un = u + ustep;
       int pend = -1, pend_g = 0;
       bool first_pv = true, q_ready = false;
       // What the pending PV needs besides its P: its V stage and the O slot
@@ -484,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           pend = j;
           pend_g = g;
           if (++ks == KS) { ks = 0; kph ^= 1; }
-          if (j == last && un < n_units) {
+          if (j == last && un >= 0) {
             if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
             if (leader) load_q(q, decode_unit(p, un));
             __syncwarp();
@@ -530,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         pend = j;
         pend_g = g;
         if (++ks == KS) { ks = 0; kph ^= 1; }
-        if (j == last && un < n_units) {
+        if (j == last && un >= 0) {
           // The Q slot is free once this QK has completed: load the next unit's tile.
           if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
           if (leader) load_q(q, decode_unit(p, un));
@@ -548,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         // No key tile for this query tile: its Q load is consumed unused.
         if (wait_or_fail(B_QFULL + q, q_seen & 1)) {
           ++q_seen;
-          if (un < n_units) {
+          if (un >= 0) {
             if (leader) load_q(q, decode_unit(p, un));
             __syncwarp();
             ++q_loads;
@@ -556,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         }
       }
       if (last >= 0) ++nact;
+      u = un;
     }
     // Drain: a Q load issued for a unit never started has landed, and every
     // MMA issued here has completed before TMEM is released.
@@ -583,7 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const bool got = mbar_wait(b, parity, abort_flag, cap);
       return __all_sync(0xffffffffu, got);
     };
-    for (int u = u0; u < n_units && ok; u += ustep) {
+    // The unit of this CTA's ut-th turn, read by every lane from slot ut % 4.
+    auto unit_in_slot = [&](int ut, int& v) -> bool {
+      if (!wait_all(bar(B_UFULL + ut % kUnitSlots), (ut / kUnitSlots) & 1)) {
+        fail();
+        ok = false;
+        return false;
+      }
+      v = unit_ring[ut % kUnitSlots];
+      return true;
+    };
+    int u = -1;
+    unit_in_slot(0, u);
+    for (int ut = 0; ok && u >= 0; ++ut) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_UEMPTY + ut % kUnitSlots));   // this warp has read slot ut
       const Unit w = decode_unit(p, u);
       const TileView tv = tile_view(w, q);
       const int T = w.n_tiles;
@@ -798,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
         reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(-INFINITY, 0.f);
       }
+      if (!unit_in_slot(ut + 1, u)) break;
     }
   }
 
@@ -826,7 +899,7 @@ cudaError_t prepare_kernel() {
 }
 
 // Persistent grid: one CTA per SM (shared memory allows no second one), each
-// walking units blockIdx.x, blockIdx.x + gridDim.x, ...
+// claiming units until the table is exhausted.
 int grid_for(int n_units) {
   static int sms[64] = {0};
   int dev = 0;
