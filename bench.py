@@ -204,13 +204,22 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float)
 # ---------------------------------------------------------------------- native arm
 
 def time_steps(torch, f, steps, flush):
-    """Per-step CUDA-event times (ms) on the current stream; L2 flushed between steps if asked."""
+    """Per-step CUDA-event times (ms) on the current stream; L2 flushed between steps if asked.
+
+    The flush writes a buffer of twice the L2 size and then reads another one
+    of the same size: the write evicts every line the previous step left in
+    L2, and the read writes those dirty lines back before the timed region, so
+    a step starts with no input in L2 and no write-back of the flush data to
+    pay for.
+    """
     stream = torch.cuda.current_stream()
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    reader = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
     times = []
     for _ in range(steps):
         if scratch is not None:
             scratch.zero_()
+            reader.sum()
         a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
         a.record(stream); f(); b.record(stream)
         times.append((a, b))
@@ -336,7 +345,7 @@ def run_native(args, rank, world):
         "dtype": w.dtype, "data": "synthetic iid N(0,1), seeded",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
                    "useful_pairs": pairs, "useful_flops_per_step": flops,
-                   "l2": "flushed between steps" if flush else "inputs larger than L2",
+                   "l2": "flushed between steps (write, then read, 2x L2)" if flush else "inputs larger than L2",
                    "parallelism": f"replicas x{world}"},
         "pct_bf16_peak": round(100 * value / world / (roofline["peak"] if roofline else FALLBACK_BF16_TFLOPS), 2),
         "e2e": e2e,
