@@ -88,21 +88,45 @@ int band_units_for(int N, int d) {
   return units;
 }
 
-// Global-query rows: 128-row tiles against splits of kGrowSplitTiles key
-// tiles; the two warpgroups of a unit take alternate key tiles, so each split
-// leaves two partial slots per row.
+// Global-query rows: 128-row tiles against splits of the key tiles; the two
+// warpgroups of a unit take alternate key tiles, so each split leaves two
+// partial slots per row.
 struct GrowPlan {
-  int n_gtiles = 0, n_key_tiles = 0, n_splits = 0, n_parts = 0;
+  int n_gtiles = 0, n_key_tiles = 0, n_splits = 0, n_parts = 0, split = 0;
 };
 
-GrowPlan grow_plan(int n_glob, int key_tiles) {
+// Fewest key tiles per split the workspace is sized for: rows of up to 64 key
+// tiles may be split into 8-tile pieces, up to 256 into 16, longer rows keep
+// 32-tile splits.
+int min_grow_split(int key_tiles) { return key_tiles <= 64 ? 8 : key_tiles <= 256 ? 16 : kGrowSplitMax; }
+
+// The splits of a row of key_tiles key tiles into pieces of about `split`
+// tiles (clamped to [min_grow_split, kGrowSplitMax]), evened out so that the
+// pieces differ by at most two tiles.  split = 0 gives the finest plan, the
+// one the workspace is sized for; any other plan has no more splits.
+GrowPlan grow_plan(int n_glob, int key_tiles, int split) {
   GrowPlan g;
   if (n_glob <= 0) return g;
+  split = std::max(min_grow_split(key_tiles), std::min(kGrowSplitMax, split));
   g.n_gtiles = cdiv(n_glob, kTileM);
   g.n_key_tiles = key_tiles;
-  g.n_splits = cdiv(key_tiles, kGrowSplitTiles);
+  const int n = cdiv(key_tiles, split);
+  g.split = std::min(kGrowSplitMax, 2 * cdiv(cdiv(key_tiles, n), 2));
+  g.n_splits = cdiv(key_tiles, g.split);
   g.n_parts = 2 * g.n_splits;
   return g;
+}
+
+// Key tiles per split for a launch: a global-row unit (split / 2 key tiles per
+// warpgroup) should take no longer than a band unit (band_tiles key tiles per
+// query tile) or than an SM's average share of the launch, whichever is
+// longer, so that the few global-row units do not end after everything else.
+int choose_grow_split(long long band_units, int band_tiles, long long grow_blocks, int key_tiles) {
+  const double work = static_cast<double>(band_units) * band_tiles +
+                      static_cast<double>(grow_blocks) * key_tiles / 2.0;   // in key tiles per warpgroup
+  const double per_sm = work / std::max(1, device_sm_count());
+  const double len = std::max(static_cast<double>(band_tiles), per_sm);
+  return static_cast<int>(std::min(2.0 * len, static_cast<double>(kGrowSplitMax)));
 }
 
 struct WsLayout {
@@ -203,14 +227,14 @@ const char* lg_version(void) { return "0.1.0 sm_103a"; }
 size_t lg_attn_fwd_workspace_size(int B, int H, int N, int D, int n_global, lg_dtype dt) {
   if (B < 1 || H < 1 || N < 1 || D < 1 || n_global < 0 || n_global > N || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
-  const GrowPlan g = grow_plan(n_global, cdiv(N, kTileN));
+  const GrowPlan g = grow_plan(n_global, cdiv(N, kTileN), 0);
   return ws_layout(B * H, n_global, D, g.n_parts, true, N, max_units(B * H, N, LG_MAX_BF16_DILATION, g)).total;
 }
 
 size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || G < 1 || D < 1 || !valid_dt(dt)) return 0;
   if (dt == LG_F32) return kStatusBytes;
-  const GrowPlan g = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
+  const GrowPlan g = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN), 0);
   return ws_layout(B * H, G, D, g.n_parts, false, 0, max_units(B * H, L, 1, g)).total;
 }
 
@@ -266,7 +290,16 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
 
   // ---- bf16 tensor-core path
   if (!encode_fn()) return LG_ERR_CUDA;
-  const GrowPlan gp = grow_plan(n_global, cdiv(N, kTileN));
+  GrowPlan gp;
+  if (n_global > 0) {
+    long long band_units = 0;
+    for (int h = 0; h < H; ++h) band_units += band_units_for(N, dilation[h]);
+    band_units *= B;
+    const int band_tiles = std::min(cdiv(static_cast<long long>(wl) + wr + kTileM, kTileN) + 1, cdiv(N, kTileN)) + cdiv(n_global, kTileN);
+    gp = grow_plan(n_global, cdiv(N, kTileN),
+                   choose_grow_split(band_units, band_tiles, static_cast<long long>(BH) * cdiv(n_global, kTileM),
+                                     cdiv(N, kTileN)));
+  }
   const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true, N, max_units(BH, N, LG_MAX_BF16_DILATION, gp));
   __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(ws + lay.qg);
   __nv_bfloat16* kg = reinterpret_cast<__nv_bfloat16*>(ws + lay.kg);
@@ -338,14 +371,15 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.scale_log2 = s * 1.4426950408889634f;
     tp.BH = BH; tp.H = H; tp.N = N; tp.D = D; tp.wl = wl; tp.wr = wr; tp.n_glob = n_global; tp.etc = 0;
     tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
-    tp.n_key_tiles_grow = gp.n_key_tiles;
+    tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
     tp.n_grow_units = (grp == 0 && n_global > 0) ? BH * gp.n_gtiles * gp.n_splits : 0;
     const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
     if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
     if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
     tp.units = ws + lay.units;
     if ((e = prof_mark(stream, true)) != cudaSuccess) return LG_ERR_CUDA;
-    if ((e = launch_tc(tp, static_cast<int>(units), stream)) != cudaSuccess) return LG_ERR_CUDA;
+    // A later group's table may not overwrite the table the previous group's kernel reads.
+    if ((e = launch_tc(tp, static_cast<int>(units), stream, grp == 0)) != cudaSuccess) return LG_ERR_CUDA;
     if ((e = prof_mark(stream, false)) != cudaSuccess) return LG_ERR_CUDA;
   }
   if (n_global > 0) {
@@ -397,7 +431,11 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   }
 
   if (!encode_fn()) return LG_ERR_CUDA;
-  const GrowPlan gp = grow_plan(G, cdiv(G, kTileN) + cdiv(L, kTileN));
+  const int key_tiles_g = cdiv(G, kTileN) + cdiv(L, kTileN);
+  const int band_tiles = std::min(cdiv(2LL * r + kTileM, kTileN) + 1, cdiv(L, kTileN)) + cdiv(G, kTileN);
+  const GrowPlan gp = grow_plan(G, key_tiles_g,
+                                choose_grow_split(static_cast<long long>(BH) * band_units_for(L, 1), band_tiles,
+                                                  static_cast<long long>(BH) * cdiv(G, kTileM), key_tiles_g));
   const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0, max_units(BH, L, 1, gp));
   static TcParams tp;
   tp = TcParams{};
@@ -425,14 +463,14 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.scale_log2 = s * 1.4426950408889634f;
   tp.BH = BH; tp.H = H; tp.N = L; tp.D = D; tp.wl = r; tp.wr = r; tp.n_glob = G; tp.etc = 1;
   tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
-    tp.n_key_tiles_grow = gp.n_key_tiles;
+  tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
   tp.n_grow_units = BH * gp.n_gtiles * gp.n_splits;
   const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * tp.band_units_per_batch;
   if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
   if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
   tp.units = ws + lay.units;
   if ((e = prof_mark(stream, true)) != cudaSuccess) return LG_ERR_CUDA;
-  if ((e = launch_tc(tp, static_cast<int>(units), stream)) != cudaSuccess) return LG_ERR_CUDA;
+  if ((e = launch_tc(tp, static_cast<int>(units), stream, true)) != cudaSuccess) return LG_ERR_CUDA;
   if ((e = prof_mark(stream, false)) != cudaSuccess) return LG_ERR_CUDA;
   MergeParams mp{};
   mp.part_acc = reinterpret_cast<const float*>(ws + lay.acc);

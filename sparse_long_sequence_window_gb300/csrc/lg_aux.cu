@@ -21,6 +21,7 @@ namespace lg {
 namespace {
 
 __global__ void prep_kernel(const PrepParams p) {
+  grid_dep_launch();   // the next kernel of the call may start
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int nthreads = gridDim.x * blockDim.x;
   for (int r = tid; r < p.n_glob; r += nthreads) {
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const int bh = static_cast<int>(row_id / p.n_glob);
   const int r = static_cast<int>(row_id % p.n_glob);
   const int tid = threadIdx.x, lane = tid & 31, wrp = tid >> 5;
+  grid_dep_wait();     // the partials are written by the tensor-core kernel before this one
   const size_t base = static_cast<size_t>(row_id) * p.n_splits;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base;
 
@@ -155,10 +157,9 @@ cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = static_cast<unsigned>(rows);
-  if (p.D == 64) merge_kernel<64><<<blocks, kMergeThreads, 0, s>>>(p, bf16_out);
-  else if (p.D == 128) merge_kernel<128><<<blocks, kMergeThreads, 0, s>>>(p, bf16_out);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (p.D == 64) return launch_kernel(merge_kernel<64>, dim3(blocks), dim3(kMergeThreads), 0, s, true, p, bf16_out);
+  if (p.D == 128) return launch_kernel(merge_kernel<128>, dim3(blocks), dim3(kMergeThreads), 0, s, true, p, bf16_out);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace lg

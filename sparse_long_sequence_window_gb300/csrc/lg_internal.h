@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/lg_attn.h"
 
 namespace lg {
@@ -21,8 +23,38 @@ enum : int {
 constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace
 constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;              // keys per tile
-constexpr int kGrowSplitTiles = 32;      // key tiles per split of a global-query row block (two partials)
+constexpr int kGrowSplitMax = 32;        // most key tiles per split of a global-query row block (two partials)
 constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
+
+// ---------------------------------------------------------------- launch chaining
+// The kernels of one call run back to back on one stream.  A kernel launched
+// with programmatic stream serialization may start while its predecessor is
+// still running (its prologue overlaps the predecessor's tail and the launch
+// latency); it calls grid_dep_wait() before it touches anything the
+// predecessor writes, and that wait returns once the predecessor has completed
+// and its memory is visible.  A chained kernel also waits before it exits, so
+// that its completion implies its predecessors'.  grid_dep_launch() lets the
+// successor launch early.  Both are no-ops when there is no such predecessor
+// or successor.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch on stream s, chained to the stream's previous kernel when `chained`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool chained,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- fp32 CUDA-core path
 
@@ -60,6 +92,7 @@ struct TcParams {
   const int* gcount;              // Longformer: gcount[x] = number of global positions < x, x in [0, N]
   int* status;
   int* unit_counter;              // units claimed so far (zeroed before the launch)
+  int grow_split;                 // key tiles per split of a global-query row block
   long long wait_cap;             // clock64 cycles a bounded wait may spin
   float scale_log2;               // scale * log2(e)
   int BH, H, N, D;                // N = L for ETC
@@ -96,9 +129,13 @@ struct PrepParams {
 
 // Host-side launchers (each defined next to its kernel).
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
-cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s);
+// The unit-table kernel and the tensor-core kernel; the table kernel is
+// chained to the stream's previous kernel when chain_table (not when that
+// kernel may still read the unit table), the tensor-core kernel always is.
+cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table);
 cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 size_t tc_smem_bytes(int D);
+int device_sm_count();  // SMs of the current device (cached per device)
 
 }  // namespace lg

@@ -109,8 +109,8 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u) {
     const int r = u / p.n_splits;
     w.grow0 = (r % p.n_gtiles) * kTileM;
     w.bh = r / p.n_gtiles;
-    w.kt0 = split * kGrowSplitTiles;
-    w.n_tiles = min(kGrowSplitTiles, p.n_key_tiles_grow - w.kt0);
+    w.kt0 = split * p.grow_split;
+    w.n_tiles = min(p.grow_split, p.n_key_tiles_grow - w.kt0);
     w.slot = 0; w.d = 1;
     w.active[0] = 1; w.active[1] = w.n_tiles > 1;
     return w;
@@ -153,6 +153,7 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u) {
 // Unit records: 16 ints per unit, built once per launch by unit_table_kernel,
 // so that a CTA reads a unit with four 16-byte loads.
 __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_units) {
+  grid_dep_launch();   // the tensor-core kernel may start its prologue
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
     const Unit w = decode_unit_slow(p, u);
     int4* rec = reinterpret_cast<int4*>(p.units) + 4 * static_cast<size_t>(u);
@@ -162,6 +163,7 @@ __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_unit
     rec[2] = make_int4(w.n_tiles, w.first[0], w.first[1], w.last[0]);
     rec[3] = make_int4(w.last[1], 0, 0, 0);
   }
+  grid_dep_wait();     // complete only after the call's earlier kernels
 }
 
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
@@ -311,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel; the unit table, the unit
+  // counter and the gathered global rows are read only after it completes.
+  grid_dep_wait();
+  grid_dep_launch();
   const long long cap = p.wait_cap;
   const int gt_src = (p.n_glob + kTileN - 1) / kTileN;
 
@@ -857,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           }
           if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
         } else if (row_valid) {
-          const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;   // partial slot of this warpgroup
+          const int slot = (w.kt0 / p.grow_split) * 2 + q;   // partial slot of this warpgroup
           const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
           float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D);
 #pragma unroll
@@ -866,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         }
       } else if (w.grow && row_valid) {
         // A warpgroup with no key tile in this split leaves an empty partial.
-        const int slot = (w.kt0 / kGrowSplitTiles) * 2 + q;
+        const int slot = (w.kt0 / p.grow_split) * 2 + q;
         const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
         reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(-INFINITY, 0.f);
       }
@@ -901,6 +907,27 @@ cudaError_t prepare_kernel() {
 // Persistent grid: one CTA per SM (shared memory allows no second one), each
 // claiming units until the table is exhausted.
 int grid_for(int n_units) {
+  const int sms = device_sm_count();
+  return n_units < sms ? n_units : sms;
+}
+
+cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table) {
+  if (n_units <= 0) return cudaSuccess;
+  static bool attr_done[2] = {false, false};
+  const int i = p.D == 64 ? 0 : 1;
+  if (!attr_done[i]) {
+    cudaError_t e = i == 0 ? prepare_kernel<64>() : prepare_kernel<128>();
+    if (e != cudaSuccess) return e;
+    attr_done[i] = true;
+  }
+  cudaError_t e = launch_kernel(unit_table_kernel, dim3((n_units + 255) / 256), dim3(256), 0, s, chain_table, p, n_units);
+  if (e != cudaSuccess) return e;
+  if (i == 0)
+    return launch_kernel(tc_attn_kernel<64>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<64>::kSmem, s, true, p, n_units);
+  return launch_kernel(tc_attn_kernel<128>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<128>::kSmem, s, true, p, n_units);
+}
+
+int device_sm_count() {
   static int sms[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -909,30 +936,7 @@ int grid_for(int n_units) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
     sms[dev] = v;
   }
-  return n_units < sms[dev] ? n_units : sms[dev];
-}
-
-cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s) {
-  if (n_units <= 0) return cudaSuccess;
-  static bool attr_done[2] = {false, false};
-  if (p.D == 64) {
-    if (!attr_done[0]) {
-      cudaError_t e = prepare_kernel<64>();
-      if (e != cudaSuccess) return e;
-      attr_done[0] = true;
-    }
-    unit_table_kernel<<<(n_units + 255) / 256, 256, 0, s>>>(p, n_units);
-    tc_attn_kernel<64><<<grid_for(n_units), kThreads, Cfg<64>::kSmem, s>>>(p, n_units);
-  } else {
-    if (!attr_done[1]) {
-      cudaError_t e = prepare_kernel<128>();
-      if (e != cudaSuccess) return e;
-      attr_done[1] = true;
-    }
-    unit_table_kernel<<<(n_units + 255) / 256, 256, 0, s>>>(p, n_units);
-    tc_attn_kernel<128><<<grid_for(n_units), kThreads, Cfg<128>::kSmem, s>>>(p, n_units);
-  }
-  return cudaGetLastError();
+  return sms[dev];
 }
 
 int tc_rows_per_load(int d) { return rows_per_load(d); }
