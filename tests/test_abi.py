@@ -105,6 +105,10 @@ def test_workspace_sizes(lib):
     a = lg.attn_fwd_workspace_size(1, 16, 8192, 128, 128, lg.LG_BF16)
     b = lg.attn_fwd_workspace_size(1, 16, 32768, 128, 128, lg.LG_BF16)
     assert b > a
+    # the partials have room for the finest split a launch may choose: rows of
+    # up to 64 key tiles may be cut into 8-tile pieces, two partials per piece
+    # of D + 2 floats (acc and (m, l)) for every (head, global row)
+    assert with_g - base >= 12 * 65 * (2 * (4096 // 128 // 8)) * (64 + 2) * 4
     assert lg.attn_fwd_workspace_size(0, 1, 1, 64, 0, lg.LG_BF16) == 0
     assert lg.etc_attn_fwd_workspace_size(2, 12, 4096, 256, 64, lg.LG_BF16) > 256
 

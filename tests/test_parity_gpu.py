@@ -70,6 +70,8 @@ BF16_CASES = [
       tuple(range(100, 400, 3))),
     W("bf16 globals in causal dilated bands D128", "bf16", 1, 3, 900, 128, 70, 0, (2, 4, 7), True,
       tuple(range(0, 900, 7))),
+    # one head, short window: the global-query rows are split into 8-tile pieces (16 partials)
+    W("bf16 fine global-row splits D128", "bf16", 1, 1, 8192, 128, 64, 64, (), False, None, 128),
 ]
 
 
