@@ -39,7 +39,9 @@
  *    launched.  Errors found on the device (bad global indices, a bounded
  *    wait that ran out) are recorded in the workspace's status word and
  *    returned by lg_query_status.  Each call clears that word first.
- *  - Calls that share a workspace must not overlap on the device.
+ *  - Calls that share a workspace must not overlap on the device.  Calls with
+ *    their own workspaces may come from several host threads at once
+ *    (lg_profile_* and lg_attn_fwd_noalloc excepted, as stated there).
  */
 #ifndef LG_ATTN_H
 #define LG_ATTN_H
@@ -128,7 +130,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
  * Arguments are those of lg_attn_fwd minus the workspace.  The caller still
  * owns and passes inputs and outputs.  Returns LG_ERR_WORKSPACE, before any
  * CUDA call, when lg_attn_fwd_workspace_size(...) exceeds the fixed size
- * (for bf16 with global tokens the scratch grows with B*H*g*N/2048).  The
+ * (for bf16 with global tokens the scratch grows with B*H*g*N/512 for
+ * N <= 8192, B*H*g*N/1024 up to N = 32768 and B*H*g*N/2048 beyond).  The
  * first call on a device looks up the array's device address (once, with
  * that device current); make it before any stream capture.  All calls share
  * the one array: calls that overlap on the GPU (other streams, other host

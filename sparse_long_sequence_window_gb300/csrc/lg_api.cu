@@ -324,7 +324,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   static_assert(1 + (LG_MAX_HEADS + kMaxSlots - 2) / (kMaxSlots - 1) <= static_cast<int>(kStatusBytes / sizeof(int)),
                 "one unit counter per launch fits in the status area");
 
-  static TcParams tp;  // large parameter block; filled per launch
+  TcParams tp;  // filled per launch (a few KB; calls from several host threads keep their own)
   for (int grp = 0; grp < n_groups; ++grp) {
     tp = TcParams{};
     int slot_d[kMaxSlots] = {1, 0, 0, 0};
@@ -437,8 +437,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
                                 choose_grow_split(static_cast<long long>(BH) * band_units_for(L, 1), band_tiles,
                                                   static_cast<long long>(BH) * cdiv(G, kTileM), key_tiles_g));
   const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0, max_units(BH, L, 1, gp));
-  static TcParams tp;
-  tp = TcParams{};
+  TcParams tp{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
       !encode_map(&tp.mapV[0], v_l, D, L, BH, 1) || !encode_map(&tp.mapQg, q_g, D, G, BH, 0) ||
       !encode_map(&tp.mapKg, k_g, D, G, BH, 0) || !encode_map(&tp.mapVg, v_g, D, G, BH, 0) ||
