@@ -117,6 +117,16 @@ GrowPlan grow_plan(int n_glob, int key_tiles, int split) {
   return g;
 }
 
+// Band units at the end of a launch of `units` units to split in two
+// one-tile units each: the last round of a persistent launch (units mod grid
+// units) when splitting it still leaves at most one item per CTA; 0 otherwise.
+long long tail_split(long long units, long long band_units) {
+  const long long grid = std::min<long long>(units, device_sm_count());
+  if (grid <= 0 || units <= grid) return 0;
+  const long long last = units % grid;
+  return (last > 0 && last <= grid - last && last <= band_units) ? last : 0;
+}
+
 // Key tiles per split for a launch: a global-row unit (split / 2 key tiles per
 // warpgroup) should take no longer than a band unit (band_tiles key tiles per
 // query tile) or than an SM's average share of the launch, whichever is
@@ -157,8 +167,8 @@ WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N, 
     w.ml = off; off += round_up(static_cast<size_t>(BH) * n_glob * n_splits * 2 * 4, 256);
   }
   w.units = off;
-  w.max_units = static_cast<size_t>(units);
-  off += round_up(static_cast<size_t>(units) * 64, 256);
+  w.max_units = static_cast<size_t>(units) + static_cast<size_t>(units) / 2;   // room for the tail split
+  off += round_up(w.max_units * 64, 256);
   w.total = off;
   return w;
 }
@@ -373,7 +383,9 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
     tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
     tp.n_grow_units = (grp == 0 && n_global > 0) ? BH * gp.n_gtiles * gp.n_splits : 0;
-    const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
+    const long long base_units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
+    tp.n_tail_split = static_cast<int>(tail_split(base_units, static_cast<long long>(B) * start));
+    const long long units = base_units + tp.n_tail_split;
     if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
     if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
     tp.units = ws + lay.units;
@@ -464,7 +476,9 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
   tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
   tp.n_grow_units = BH * gp.n_gtiles * gp.n_splits;
-  const long long units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * tp.band_units_per_batch;
+  const long long band_units = static_cast<long long>(B) * tp.band_units_per_batch;
+  tp.n_tail_split = static_cast<int>(tail_split(static_cast<long long>(tp.n_grow_units) + band_units, band_units));
+  const long long units = static_cast<long long>(tp.n_grow_units) + band_units + tp.n_tail_split;
   if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
   if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
   tp.units = ws + lay.units;

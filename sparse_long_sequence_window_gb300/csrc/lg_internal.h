@@ -93,6 +93,7 @@ struct TcParams {
   int* status;
   int* unit_counter;              // units claimed so far (zeroed before the launch)
   int grow_split;                 // key tiles per split of a global-query row block
+  int n_tail_split;               // last band units split into two one-tile units each
   long long wait_cap;             // clock64 cycles a bounded wait may spin
   float scale_log2;               // scale * log2(e)
   int BH, H, N, D;                // N = L for ETC

@@ -99,10 +99,20 @@ struct Unit {
   int active[2];
 };
 
-// Unit u from its index (the arithmetic behind the unit table: a scan over
-// heads and residue classes, with divisions; run once per unit per call).
-__device__ Unit decode_unit_slow(const TcParams& p, int u) {
+// Unit u of a launch of n_units from its index (the arithmetic behind the
+// unit table: a scan over heads and residue classes, with divisions; run once
+// per unit per call).  The last n_tail_split band units are each split into
+// two one-tile units, which come last (u = n_full + 2 i + h: rows t0 + 128 h
+// of band unit n_full + i, worked by query tile 0), so that the last round of
+// a launch can spread over more CTAs.
+__device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
   Unit w{};
+  const int n_full = n_units - 2 * p.n_tail_split;
+  int half = -1;
+  if (u >= n_full) {
+    half = (u - n_full) & 1;
+    u = n_full + ((u - n_full) >> 1);
+  }
   if (u < p.n_grow_units) {
     w.grow = 1;
     const int split = u % p.n_splits;
@@ -131,8 +141,10 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u) {
     if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
     rem -= units;
   }
-  if (w.n_c <= 0) { w.n_tiles = 0; return w; }
-  const int t_last = min(w.t0 + 2 * kTileM - 1, w.n_c - 1);
+  const int span = half >= 0 ? 1 : 2;                 // query tiles of this unit
+  if (half > 0) w.t0 += kTileM;
+  if (w.n_c <= 0 || w.t0 >= w.n_c) { w.n_tiles = 0; return w; }
+  const int t_last = min(w.t0 + span * kTileM - 1, w.n_c - 1);
   w.band_lo = max(0, w.t0 - p.wl);
   const int band_hi = min(w.n_c - 1, t_last + p.wr);
   w.n_band = (band_hi - w.band_lo + kTileN) / kTileN;
@@ -140,7 +152,7 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u) {
   w.n_tiles = w.n_band + n_gt;
   for (int q = 0; q < 2; ++q) {
     const int a = w.t0 + q * kTileM;
-    w.active[q] = a < w.n_c;
+    w.active[q] = q < span && a < w.n_c;
     if (!w.active[q]) { w.first[q] = 1; w.last[q] = 0; continue; }
     const int b_ = min(a + kTileM - 1, w.n_c - 1);
     const int klo = max(0, a - p.wl), khi = min(w.n_c - 1, b_ + p.wr);
@@ -155,7 +167,7 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u) {
 __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_units) {
   grid_dep_launch();   // the tensor-core kernel may start its prologue
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
-    const Unit w = decode_unit_slow(p, u);
+    const Unit w = decode_unit_slow(p, u, n_units);
     int4* rec = reinterpret_cast<int4*>(p.units) + 4 * static_cast<size_t>(u);
     const int flags = w.grow | (w.slot << 1) | (w.active[0] << 4) | (w.active[1] << 5) | (w.d << 8) | (w.c << 16);
     rec[0] = make_int4(w.bh, flags, w.t0, w.n_c);
