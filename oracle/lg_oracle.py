@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for window + dilation + global sparse self-attention (forward).
+"""fp64 CPU oracle for window + dilation + global sparse self-attention
+(forward; and its backward, the next row after the forward).
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check in
 ``__graft_entry__.smoke`` and the CPU-baseline leg of ``bench.py`` may import
@@ -364,3 +365,79 @@ def merge_partials(ms, ls, accs):
     l = (w * ls).sum(axis=0)
     out = (w[:, :, None] * accs).sum(axis=0) / l[:, None]
     return out, m + np.log(l)
+
+
+# --------------------------------------------------------------------------
+# Backward pass (the row after the forward: gradients of the same function)
+# --------------------------------------------------------------------------
+
+def masked_attention_bwd(q, k, v, mask, scale, dout, dlse=None):
+    """dQ, dK, dV of one head of ``masked_attention`` for upstream gradients dO (and dLSE).
+
+    The pages train with this attention and take gradients through it
+    (Longformer page, "Autoregressive Language Modeling Configuration":
+    activations recomputed in the backward pass; LongNet page, "Distributed
+    Training Algorithm": the gradients with respect to the keys and values),
+    so the backward pass is the derivative of the forward definition above,
+    written out by the chain rule in float64:
+      P = softmax over the allowed keys of scale * q k^T,  O = P v,
+      dV = P^T dO,   dP = dO v^T,
+      dS_ij = P_ij (dP_ij - sum_j' P_ij' dP_ij') + P_ij dLSE_i,
+      dQ = scale * dS k,   dK = scale * dS^T q.
+    Disallowed pairs have P = 0 and so contribute nothing.  q, dout: [n_q, D];
+    k, v: [n_k, D]; mask: [n_q, n_k] bool; dlse: [n_q] or None.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    _, _, p = masked_attention(q, k, v, mask, scale)
+    dv = p.T @ dout
+    dp = dout @ v.T
+    delta = (p * dp).sum(axis=1, keepdims=True)
+    ds = p * (dp - delta)
+    if dlse is not None:
+        ds = ds + p * np.asarray(dlse, np.float64)[:, None]
+    return scale * (ds @ k), scale * (ds.T @ q), dv
+
+
+def attn_bwd(q, k, v, dout, w_left, w_right, dilation, causal, global_idx, scale=None, dlse=None):
+    """Dense-mask backward of ``attn_fwd``: dQ, dK, dV [B, H, N, D] (float64).
+
+    Same mask as the forward (``allowed_mask`` per head); dout: [B, H, N, D];
+    dlse: [B, H, N] or None.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    B, H, N, D = q.shape
+    s = default_scale(D, scale)
+    dq = np.empty_like(q); dk = np.empty_like(k); dv = np.empty_like(v)
+    for h in range(H):
+        mask = allowed_mask(N, w_left, w_right, int(dilation[h]), bool(causal), global_idx)
+        for b in range(B):
+            dl = None if dlse is None else np.asarray(dlse, np.float64)[b, h]
+            dq[b, h], dk[b, h], dv[b, h] = masked_attention_bwd(q[b, h], k[b, h], v[b, h], mask, s,
+                                                                dout[b, h], dl)
+    return dq, dk, dv
+
+
+def etc_attn_bwd(q_l, k_l, v_l, q_g, k_g, v_g, radius, dout_l, dout_g, scale=None):
+    """Dense-mask backward of ``etc_attn_fwd``: gradients of the long and global inputs.
+
+    The [global; long] sequence with the ``etc_mask`` of the forward; returns
+    (dq_l, dk_l, dv_l, dq_g, dk_g, dv_g), each shaped like its input.
+    """
+    q_l = np.asarray(q_l, np.float64); k_l = np.asarray(k_l, np.float64); v_l = np.asarray(v_l, np.float64)
+    q_g = np.asarray(q_g, np.float64); k_g = np.asarray(k_g, np.float64); v_g = np.asarray(v_g, np.float64)
+    B, H, L, D = q_l.shape
+    G = q_g.shape[2]
+    s = default_scale(D, scale)
+    mask = etc_mask(L, G, radius)
+    out = [np.empty_like(x) for x in (q_l, k_l, v_l, q_g, k_g, v_g)]
+    for b in range(B):
+        for h in range(H):
+            q = np.concatenate([q_g[b, h], q_l[b, h]]); k = np.concatenate([k_g[b, h], k_l[b, h]])
+            v = np.concatenate([v_g[b, h], v_l[b, h]])
+            do = np.concatenate([np.asarray(dout_g, np.float64)[b, h], np.asarray(dout_l, np.float64)[b, h]])
+            dq, dk, dv = masked_attention_bwd(q, k, v, mask, s, do)
+            for i, (x, part) in enumerate(((dq, 1), (dk, 1), (dv, 1), (dq, 0), (dk, 0), (dv, 0))):
+                out[i][b, h] = x[G:] if part else x[:G]
+    return tuple(out)

@@ -259,9 +259,94 @@ def pin_merge(O, seed=14):
         assert np.abs(lse - full_l).max() < 1e-12
 
 
+# ---------------------------------------------------------------- backward
+
+def _loss(O, q, k, v, args, dout, dlse):
+    """Scalar L = sum(dO * O) + sum(dLSE * LSE); its gradients are the backward pass."""
+    out, lse = O.attn_fwd(q, k, v, *args)
+    return float((dout * out).sum() + (dlse * lse).sum())
+
+
+def pin_bwd_finite_differences(O, seed=15):
+    """Central differences of the forward oracle reproduce dQ, dK, dV (incl. a dLSE term)."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 2, 11, 3
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    dout, dlse = _rand(rng, B, H, N, D), _rand(rng, B, H, N)
+    for args in ((2, 1, [1, 2], False, [4]), (3, 0, [2, 1], True, [])):
+        dq, dk, dv = O.attn_bwd(q, k, v, dout, *args, dlse=dlse)
+        eps = 1e-6
+        for x, g in ((q, dq), (k, dk), (v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + eps; up = _loss(O, q, k, v, args, dout, dlse)
+                x[idx] = old - eps; dn = _loss(O, q, k, v, args, dout, dlse)
+                x[idx] = old
+                num[idx] = (up - dn) / (2 * eps)
+            assert np.abs(num - g).max() < 1e-6 * (1 + np.abs(g).max())
+
+
+def pin_bwd_autograd(O, seed=16):
+    """torch autograd of a masked fp64 softmax attention (library routine) gives the same gradients."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 2, 19, 8
+    q, k, v = _rand(rng, B, H, N, D), _rand(rng, B, H, N, D), _rand(rng, B, H, N, D)
+    dout, dlse = _rand(rng, B, H, N, D), _rand(rng, B, H, N)
+    wl, wr, dil, causal, g = 3, 2, [1, 3], False, [0, 9]
+    masks = torch.from_numpy(np.stack([O.allowed_mask(N, wl, wr, d, causal, g) for d in dil]))[None]
+    qt, kt, vt = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+    s = 1 / np.sqrt(D)
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=masks, scale=s)
+    logits = (s * qt @ kt.transpose(-1, -2)).masked_fill(~masks, float("-inf"))
+    loss = (out * torch.from_numpy(dout)).sum() + (torch.logsumexp(logits, dim=-1) * torch.from_numpy(dlse)).sum()
+    loss.backward()
+    dq, dk, dv = O.attn_bwd(q, k, v, dout, wl, wr, dil, causal, g, dlse=dlse)
+    for mine, ref in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        assert np.abs(mine - ref.numpy()).max() < 1e-11
+
+
+def pin_bwd_invariants(O, seed=17):
+    """Shifting every key leaves O unchanged, so sum_j dK_j = 0; rows of P sum to 1, so sum_j dV_j = sum_i dO_i."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 3, 40, 6
+    q, k, v, dout = (_rand(rng, B, H, N, D) for _ in range(4))
+    dq, dk, dv = O.attn_bwd(q, k, v, dout, 5, 4, [1, 2, 3], True, [7, 30])
+    assert np.abs(dk.sum(axis=2)).max() < 1e-11
+    assert np.abs(dv.sum(axis=2) - dout.sum(axis=2)).max() < 1e-11
+    # identity window (w = 0, no globals): O = V, so dV = dO and dQ = dK = 0
+    dq, dk, dv = O.attn_bwd(q, k, v, dout, 0, 0, [1, 1, 1], False, [])
+    assert np.abs(dv - dout).max() < 1e-14 and np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+
+
+def pin_etc_bwd_finite_differences(O, seed=18):
+    """Central differences of the ETC forward reproduce the gradients of the long and global inputs."""
+    rng = np.random.default_rng(seed)
+    B, H, L, G, D, r = 1, 1, 7, 2, 3, 1
+    xs = [_rand(rng, B, H, L, D) for _ in range(3)] + [_rand(rng, B, H, G, D) for _ in range(3)]
+    dl, dg = _rand(rng, B, H, L, D), _rand(rng, B, H, G, D)
+
+    def loss():
+        ol, og, _, _ = O.etc_attn_fwd(*xs, r)
+        return float((dl * ol).sum() + (dg * og).sum())
+
+    grads = O.etc_attn_bwd(*xs, r, dl, dg)
+    eps = 1e-6
+    for x, g in zip(xs, grads):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps; up = loss()
+            x[idx] = old - eps; dn = loss()
+            x[idx] = old
+            num[idx] = (up - dn) / (2 * eps)
+        assert np.abs(num - g).max() < 1e-6 * (1 + np.abs(g).max())
+
+
 ALL_PINS = [
     pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
     pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
     pin_identity_window, pin_dilation_residues, pin_key_shift, pin_constant_values,
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
+    pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
 ]

@@ -111,9 +111,42 @@ def mut_merge_no_rescale(O):
     O.merge_partials = merge_partials
 
 
+def _bwd_mutant(O, variant):
+    def masked_attention_bwd(q, k, v, mask, scale, dout, dlse=None):
+        q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+        _, _, p = O.masked_attention(q, k, v, mask, scale)
+        dp = dout @ v.T
+        delta = 0.0 if variant == "no_delta" else (p * dp).sum(axis=1, keepdims=True)
+        ds = p * (dp - delta)
+        if dlse is not None:
+            ds = ds + p * np.asarray(dlse)[:, None]
+        dv = p @ dout if variant == "dv_untransposed" else p.T @ dout
+        sc = 1.0 if variant == "no_scale" else scale
+        dk = sc * (ds @ q) if variant == "dk_untransposed" else sc * (ds.T @ q)
+        return sc * (ds @ k), dk, dv
+    O.masked_attention_bwd = masked_attention_bwd
+
+
+def mut_bwd_no_delta(O):
+    _bwd_mutant(O, "no_delta")
+
+
+def mut_bwd_no_scale(O):
+    _bwd_mutant(O, "no_scale")
+
+
+def mut_bwd_dk_untransposed(O):
+    _bwd_mutant(O, "dk_untransposed")
+
+
+def mut_bwd_dv_untransposed(O):
+    _bwd_mutant(O, "dv_untransposed")
+
+
 MUTANTS = [mut_swap_sides, mut_ignore_dilation, mut_span_not_steps, mut_causal_keeps_right,
            mut_no_global_columns, mut_no_scale, mut_transposed_logits, mut_lse_log2,
-           mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale]
+           mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale,
+           mut_bwd_no_delta, mut_bwd_no_scale, mut_bwd_dk_untransposed, mut_bwd_dv_untransposed]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
