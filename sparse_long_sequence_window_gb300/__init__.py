@@ -99,6 +99,20 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+def _same(ref, what, *ts):
+    """Every tensor in ts has ref's shape, dtype and device (the library trusts the sizes it is given)."""
+    for t in ts:
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError(f"{what}: expected {tuple(ref.shape)} {ref.dtype} on {ref.device}, "
+                             f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+def _check_out(t, shape, dtype, device, what):
+    if t.shape != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{what}: expected {tuple(shape)} {dtype} on {device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
 def _stream(stream) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -116,10 +130,16 @@ def etc_attn_fwd_workspace_size(B, H, L, G, D, dtype_code) -> int:
 def _workspace(nbytes: int, device, workspace):
     import torch
     if workspace is not None:
+        if workspace.device != device or not workspace.is_contiguous():
+            raise ValueError(f"workspace must be a contiguous tensor on {device}")
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError("workspace too small")
         return workspace
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
 
 
 def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int]] = None,
@@ -134,24 +154,30 @@ def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int
     """
     import torch
     lib = load()
+    if q.dim() != 4 or not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor [B, H, N, D]")
+    _same(q, "k", k)
+    _same(q, "v", v)
     B, H, N, D = q.shape
     dil = np.ascontiguousarray(np.asarray(dilation if dilation is not None else [1] * H, dtype=np.int32))
     if dil.size != H:
         raise ValueError("dilation needs H entries")
     n_global = 0 if global_idx is None else int(global_idx.numel())
-    if global_idx is not None and global_idx.dtype != torch.int32:
-        raise TypeError("global_idx must be int32")
+    if global_idx is not None and (global_idx.dtype != torch.int32 or global_idx.device != q.device):
+        raise TypeError("global_idx must be an int32 tensor on q's device")
     dt = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
+    _check_out(out, q.shape, q.dtype, q.device, "out")
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
     need = attn_fwd_workspace_size(B, H, N, D, n_global, dt)
     ws = _workspace(need, q.device, workspace)
     st = lib.lg_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), dt, B, H, N, D,
                          int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
                          _ptr(global_idx) if n_global else None, n_global,
-                         float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(), _stream(stream))
+                         float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
     _check(st, "lg_attn_fwd")
     attn_fwd.last_workspace = ws
     return out, lse
@@ -169,6 +195,10 @@ def attn_fwd_host(q_h, k_h, v_h, w_left: int, w_right: int, dilation: Optional[S
     """
     import torch
     lib = load()
+    if q_h.dim() != 4 or q_h.is_cuda:
+        raise ValueError("q_h must be a host tensor [B, H, N, D]")
+    _same(q_h, "k_h", k_h)
+    _same(q_h, "v_h", v_h)
     B, H, N, D = q_h.shape
     dil = np.ascontiguousarray(np.asarray(dilation if dilation is not None else [1] * H, dtype=np.int32))
     if dil.size != H:
@@ -182,15 +212,22 @@ def attn_fwd_host(q_h, k_h, v_h, w_left: int, w_right: int, dilation: Optional[S
         out_h = torch.empty(q_h.shape, dtype=q_h.dtype, pin_memory=True)
     if lse_h is None:
         lse_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    _check_out(out_h, q_h.shape, q_h.dtype, q_h.device, "out_h")
+    _check_out(lse_h, (B, H, N), torch.float32, q_h.device, "lse_h")
     if staging is None:
         staging = tuple(torch.empty(q_h.shape, dtype=q_h.dtype, device=dev) for _ in range(4)) + (
             torch.empty((B, H, N), dtype=torch.float32, device=dev),)
+    if len(staging) != 5:
+        raise ValueError("staging holds five device tensors: q, k, v, out, lse")
+    for t, name in zip(staging[:4], ("q", "k", "v", "out")):
+        _check_out(t, q_h.shape, q_h.dtype, dev, f"staging {name}")
+    _check_out(staging[4], (B, H, N), torch.float32, dev, "staging lse")
     need = attn_fwd_workspace_size(B, H, N, D, n_global, dt)
     ws = _workspace(need, dev, workspace)
     st = lib.lg_attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(out_h), _ptr(lse_h),
                               *(_ptr(x) for x in staging), dt, B, H, N, D, int(w_left), int(w_right),
                               dil.ctypes.data, int(bool(causal)), _ptr(global_idx) if n_global else None, n_global,
-                              float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(), int(n_groups),
+                              float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), int(n_groups),
                               _stream(stream))
     _check(st, "lg_attn_fwd_host")
     attn_fwd_host.last_workspace = ws
@@ -202,18 +239,30 @@ def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius: int, scale: Optional[floa
     """ETC-style global-local attention forward.  Returns (out_l, out_g, lse_l, lse_g)."""
     import torch
     lib = load()
+    if q_l.dim() != 4 or q_g.dim() != 4 or not q_l.is_cuda:
+        raise ValueError("q_l, q_g must be CUDA tensors [B, H, L, D] and [B, H, G, D]")
+    _same(q_l, "k_l", k_l)
+    _same(q_l, "v_l", v_l)
+    _same(q_g, "k_g", k_g)
+    _same(q_g, "v_g", v_g)
     B, H, L, D = q_l.shape
     G = q_g.shape[2]
+    if q_g.shape[:2] != q_l.shape[:2] or q_g.shape[3] != D or q_g.dtype != q_l.dtype or q_g.device != q_l.device:
+        raise ValueError("q_g must match q_l in B, H, D, dtype and device")
     dt = _dtype_code(q_l)
     out_l = torch.empty_like(q_l) if out_l is None else out_l
     out_g = torch.empty_like(q_g) if out_g is None else out_g
     lse_l = torch.empty((B, H, L), dtype=torch.float32, device=q_l.device) if lse_l is None else lse_l
     lse_g = torch.empty((B, H, G), dtype=torch.float32, device=q_l.device) if lse_g is None else lse_g
+    _check_out(out_l, q_l.shape, q_l.dtype, q_l.device, "out_l")
+    _check_out(out_g, q_g.shape, q_g.dtype, q_l.device, "out_g")
+    _check_out(lse_l, (B, H, L), torch.float32, q_l.device, "lse_l")
+    _check_out(lse_g, (B, H, G), torch.float32, q_l.device, "lse_g")
     need = etc_attn_fwd_workspace_size(B, H, L, G, D, dt)
     ws = _workspace(need, q_l.device, workspace)
     st = lib.lg_etc_attn_fwd(_ptr(q_l), _ptr(k_l), _ptr(v_l), _ptr(q_g), _ptr(k_g), _ptr(v_g),
                              _ptr(out_l), _ptr(out_g), _ptr(lse_l), _ptr(lse_g), dt, B, H, L, G, D,
-                             int(radius), float(scale) if scale else 0.0, ws.data_ptr(), ws.numel(),
+                             int(radius), float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws),
                              _stream(stream))
     _check(st, "lg_etc_attn_fwd")
     etc_attn_fwd.last_workspace = ws

@@ -161,3 +161,19 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert call(dil=(ctypes.c_int32 * 2)(1, 0)) == lg.LG_ERR_INVALID_ARG
     assert call(wsb=64) == lg.LG_ERR_WORKSPACE
     assert call(ws=None) == lg.LG_ERR_WORKSPACE
+
+
+def test_binding_checks_tensors_before_the_library(lib):
+    """The binding refuses tensors whose sizes the library would trust blindly."""
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lg.attn_fwd(q, q, q, 4, 4)                  # host tensors on the device entry point
+    k_bad = torch.zeros(1, 2, 7, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lg.attn_fwd_host(q, k_bad, q, 4, 4)         # k shorter than q
+    v_bad = torch.zeros(1, 2, 8, 64, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        lg.attn_fwd_host(q, q, v_bad, 4, 4)         # v of another dtype
+    with pytest.raises(ValueError):
+        lg.etc_attn_fwd(q, q, q, q, q, q, 2)        # host tensors on the device entry point
