@@ -23,7 +23,8 @@ from __future__ import annotations
 
 import os
 
-# The CPU oracle is timed single-threaded; set before numpy loads its BLAS.
+# The CPU oracle runs one single-threaded process per host core (a spawned
+# pool); set before numpy loads its BLAS, so every worker inherits it.
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -356,8 +357,9 @@ def run_native(args, rank, world):
     }
     if per_config:
         line["per_config"] = per_config
+        line["linear_in_n_slope"] = linear_in_n_slope(per_config)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if dist:
         dist.destroy_process_group()
     return line
@@ -465,27 +467,87 @@ def cpu_sample(w, budget_s, seed=1234, arrs=None):
     return flops, time.perf_counter() - t0, rows
 
 
-def cpu_baseline(w, budget_s=15.0):
-    flops, secs, rows = cpu_sample(w, budget_s)
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+# The oracle over all host cores: one spawned worker process per core (spawn,
+# not fork: the parent may already hold a CUDA context), each single-threaded,
+# each drawing the same one-head inputs once and evaluating its own uniformly
+# drawn rows.  The throughput is the sum of the workers' useful FLOPs over the
+# wall time of the parallel section.
+_WORKER = {}
+
+
+def _pool_init(preset):
+    w = workloads.PRESETS[preset]
+    _WORKER["w"] = w
+    _WORKER["arrs"] = cpu_inputs(w)
+
+
+def _pool_task(args):
+    budget_s, seed = args
+    return cpu_sample(_WORKER["w"], budget_s, seed=seed, arrs=_WORKER["arrs"])
+
+
+class OraclePool:
+    def __init__(self, preset, workers=None):
+        import multiprocessing as mp
+        self.workers = max(1, workers or os.cpu_count() or 1)
+        self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_pool_init, initargs=(preset,))
+        # every worker has its inputs before anything is timed
+        self.pool.map(_pool_task, [(0.0, i) for i in range(self.workers)], chunksize=1)
+
+    def sample(self, budget_s, seed):
+        """Useful FLOPs, wall seconds and rows of one parallel sample of about budget_s seconds."""
+        t0 = time.perf_counter()
+        res = self.pool.map(_pool_task, [(budget_s, seed * 1000 + i) for i in range(self.workers)], chunksize=1)
+        secs = time.perf_counter() - t0
+        return sum(r[0] for r in res), secs, sum(r[2] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(preset, budget_s=15.0):
+    w = workloads.PRESETS[preset]
+    pool = OraclePool(preset)
+    try:
+        flops, secs, rows = pool.sample(budget_s, seed=1)
+    finally:
+        pool.close()
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": pool.workers, "kind": "oracle",
+            "host_cpu_count": os.cpu_count(),
             "sample": f"{rows} uniformly drawn query rows of one head of {w.name}, fp64 numpy, "
-                      f"{secs:.1f} s, one thread"}
+                      f"{secs:.1f} s wall on {pool.workers} single-threaded worker processes"}
+
+
+def linear_in_n_slope(per_config):
+    """Least-squares slope of log(ms per call) against log(N) over the long-scale sweep (1 = linear)."""
+    pts = [(workloads.PRESETS[n].N, per_config[n]["ms"]) for n in ("long_8k", "long_32k", "long_128k")
+           if n in per_config]
+    if len(pts) < 2:
+        return None
+    x = np.log([p[0] for p in pts]); y = np.log([p[1] for p in pts])
+    slope = float(np.polyfit(x, y, 1)[0])
+    return {"slope": round(slope, 4), "points_N_ms": [[int(a), b] for a, b in pts],
+            "workload": "long_scale bf16 B1 H16 D128 w512/512 G=128 random"}
 
 
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step a bounded sample of the workload's rows."""
     w = workloads.PRESETS[args.workload]
     per_step = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))  # whole run about 2.5 min
-    arrs = cpu_inputs(w)
-    for _ in range(args.warmup):
-        cpu_sample(w, per_step, seed=99, arrs=arrs)
-    total_f, total_s, total_rows = 0.0, 0.0, 0
-    for s in range(args.steps):
-        fl, sec, rows = cpu_sample(w, per_step, seed=1000 + s, arrs=arrs)
-        total_f += fl; total_s += sec; total_rows += rows
+    pool = OraclePool(args.workload)
+    try:
+        for i in range(args.warmup):
+            pool.sample(per_step, seed=90 + i)
+        total_f, total_s, total_rows = 0.0, 0.0, 0
+        for s in range(args.steps):
+            fl, sec, rows = pool.sample(per_step, seed=1000 + s)
+            total_f += fl; total_s += sec; total_rows += rows
+    finally:
+        pool.close()
     value = total_f / total_s / 1e12
     sample = (f"{total_rows} uniformly drawn query rows of one head of {w.name} over {args.steps} steps "
-              f"of ~{per_step:.1f} s each, fp64 numpy, one thread")
+              f"of ~{per_step:.1f} s each, fp64 numpy, {pool.workers} single-threaded worker processes")
     return {
         "impl": "reference",
         "metric": "sparse attn fwd TFLOP/s (in-band pairs) & % bf16 tensor peak, N=512-128K",
@@ -493,7 +555,8 @@ def run_reference(args, rank, world):
         "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic iid N(0,1), seeded",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": pool.workers, "kind": "oracle",
+                         "host_cpu_count": os.cpu_count(), "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -225,6 +225,29 @@ int64_t lg_count_pairs(int N, int w_left, int w_right, int dilation, int causal,
 int64_t lg_etc_count_pairs(int L, int G, int radius);
 
 /*
+ * Testing aid for the device-side timeout path.  (Not a step of the method:
+ * the paper has no counterpart.)
+ *
+ * Every wait of the tensor-core kernel is bounded: when a wait for a tile, a
+ * score block or a work unit runs out, the kernel records a timeout in the
+ * workspace's status word, every role stops taking new work, waits (with a
+ * fixed bound of about two seconds that nothing here shortens) until the TMA
+ * loads and MMAs it has already issued have completed, releases its tensor
+ * memory and returns; lg_query_status then reports LG_ERR_TIMEOUT and the
+ * outputs are undefined.  This call makes that path testable without a fault:
+ *
+ *  withhold         1: later bf16 calls issue no TMA load and no MMA in the
+ *                   tensor-core kernel, so its first wait for a tile runs out
+ *                   with nothing in flight; 0: normal operation.
+ *  wait_cap_cycles  cap of the work waits in SM clock cycles; <= 0 restores
+ *                   the default (about one second).
+ *
+ * Process-wide, applies to calls made after it returns; not for concurrent
+ * use with other calls.  Returns LG_ERR_INVALID_ARG if withhold is not 0 or 1.
+ */
+lg_status lg_debug_timeout_test(int withhold, long long wait_cap_cycles);
+
+/*
  * Kernel timing of the dominant attention kernel.  After lg_profile_begin,
  * each launch of that kernel is bracketed by CUDA events on its stream;
  * lg_profile_end synchronises those events and returns the summed elapsed

@@ -18,7 +18,7 @@ import numpy as np
 __all__ = [
     "LgError", "load", "attn_fwd", "attn_fwd_host", "etc_attn_fwd", "attn_fwd_workspace_size",
     "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
-    "profile_begin", "profile_end", "status_string", "LIB_PATH",
+    "profile_begin", "profile_end", "status_string", "debug_timeout_test", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblg_attn.so")
@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
     lib.lg_count_pairs.argtypes = [i32, i32, i32, i32, i32, vp, i32]
     lib.lg_etc_count_pairs.restype = ctypes.c_int64
     lib.lg_etc_count_pairs.argtypes = [i32, i32, i32]
+    lib.lg_debug_timeout_test.restype = i32
+    lib.lg_debug_timeout_test.argtypes = [i32, ctypes.c_longlong]
     lib.lg_profile_begin.restype = i32
     lib.lg_profile_begin.argtypes = []
     lib.lg_profile_end.restype = i32
@@ -117,6 +119,18 @@ def _stream(stream) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def _keep_for(stream, *tensors):
+    """Tensors allocated here but used by work queued on another stream than the
+    current one: tell the caching allocator, so that their memory is not handed
+    out again before that work has completed."""
+    import torch
+    if stream is None or stream == torch.cuda.current_stream(stream.device):
+        return
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            t.record_stream(stream)
 
 
 def attn_fwd_workspace_size(B, H, N, D, n_global, dtype_code) -> int:
@@ -179,6 +193,8 @@ def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int
                          _ptr(global_idx) if n_global else None, n_global,
                          float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
     _check(st, "lg_attn_fwd")
+    if workspace is None:
+        _keep_for(stream, ws)
     attn_fwd.last_workspace = ws
     return out, lse
 
@@ -214,7 +230,8 @@ def attn_fwd_host(q_h, k_h, v_h, w_left: int, w_right: int, dilation: Optional[S
         lse_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
     _check_out(out_h, q_h.shape, q_h.dtype, q_h.device, "out_h")
     _check_out(lse_h, (B, H, N), torch.float32, q_h.device, "lse_h")
-    if staging is None:
+    own_staging = staging is None
+    if own_staging:
         staging = tuple(torch.empty(q_h.shape, dtype=q_h.dtype, device=dev) for _ in range(4)) + (
             torch.empty((B, H, N), dtype=torch.float32, device=dev),)
     if len(staging) != 5:
@@ -230,6 +247,14 @@ def attn_fwd_host(q_h, k_h, v_h, w_left: int, w_right: int, dilation: Optional[S
                               float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), int(n_groups),
                               _stream(stream))
     _check(st, "lg_attn_fwd_host")
+    # The library queues work on its own copy streams too, all joined into
+    # `stream`; buffers allocated here must outlive that stream's work.
+    s = stream if stream is not None else torch.cuda.current_stream()
+    if own_staging:
+        for t in staging:
+            t.record_stream(s)
+    if workspace is None:
+        ws.record_stream(s)
     attn_fwd_host.last_workspace = ws
     return out_h, lse_h
 
@@ -265,6 +290,8 @@ def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius: int, scale: Optional[floa
                              int(radius), float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws),
                              _stream(stream))
     _check(st, "lg_etc_attn_fwd")
+    if workspace is None:
+        _keep_for(stream, ws)
     etc_attn_fwd.last_workspace = ws
     return out_l, out_g, lse_l, lse_g
 
@@ -289,6 +316,14 @@ def etc_count_pairs(L, G, radius) -> int:
     if r < 0:
         raise ValueError("invalid arguments to lg_etc_count_pairs")
     return int(r)
+
+
+def debug_timeout_test(withhold: bool, wait_cap_cycles: int = 0):
+    """Testing aid of the timeout path: with withhold, later bf16 calls issue no
+    loads or MMAs, so their first bounded wait runs out (after wait_cap_cycles
+    SM cycles; <= 0 restores the default cap) and lg_query_status reports
+    LG_ERR_TIMEOUT.  debug_timeout_test(False) restores normal operation."""
+    _check(load().lg_debug_timeout_test(int(bool(withhold)), int(wait_cap_cycles)), "lg_debug_timeout_test")
 
 
 def profile_begin():

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -25,14 +26,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-long long wait_cap_cycles() {
-  static long long cap = [] {
-    const char* e = getenv("LG_WAIT_CAP_CYCLES");
-    long long v = e ? atoll(e) : 0;
-    return v > 0 ? v : 2000000000LL;  // about one second at the SM clock
-  }();
-  return cap;
-}
+// Cap of the bounded work waits and the timeout-test switch (lg_debug_timeout_test).
+std::atomic<long long> g_wait_cap_override{0};
+std::atomic<int> g_withhold{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -248,16 +244,29 @@ size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtyp
   return ws_layout(B * H, G, D, g.n_parts, false, 0, max_units(B * H, L, 1, g)).total;
 }
 
-lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
-                      int H, int N, int D, int w_left, int w_right, const int32_t* dilation, int causal,
-                      const int32_t* global_idx, int n_global, float scale, void* workspace,
-                      size_t workspace_bytes, lg_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  // ---- argument checks (nothing is launched on failure)
+}  // extern "C"
+
+namespace lg {
+
+long long wait_cap_cycles() {
+  const long long v = g_wait_cap_override.load(std::memory_order_relaxed);
+  return v > 0 ? v : 2000000000LL;  // about one second at the SM clock
+}
+
+int withhold_for_test() { return g_withhold.load(std::memory_order_relaxed); }
+
+// Every argument check of lg_attn_fwd, on sizes and pointers only (no CUDA
+// call).  max_heads_per_call: the head count one kernel call may hold
+// (lg_attn_fwd: LG_MAX_HEADS; the host-memory entry point splits larger
+// problems into groups of at most that many slices).
+lg_status validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right, const int32_t* dilation,
+                       int causal, const int32_t* global_idx, int n_global, const void* workspace,
+                       size_t workspace_bytes, bool per_call_head_limit) {
   if (!valid_dt(dt) || B < 1 || H < 1 || N < 1 || w_left < 0 || w_right < 0 || (causal != 0 && causal != 1) ||
       n_global < 0 || n_global > N || dilation == nullptr)
     return LG_ERR_INVALID_ARG;
-  if (H > LG_MAX_HEADS) return LG_ERR_UNSUPPORTED;
+  if (per_call_head_limit && H > LG_MAX_HEADS) return LG_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * N > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !lse) return LG_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
@@ -271,7 +280,24 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     for (int h = 0; h < H; ++h)
       if (dilation[h] > LG_MAX_BF16_DILATION) return LG_ERR_UNSUPPORTED;
   const size_t need = lg_attn_fwd_workspace_size(B, H, N, D, n_global, dt);
+  if (need == 0) return LG_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return LG_ERR_WORKSPACE;
+  return LG_OK;
+}
+
+}  // namespace lg
+
+extern "C" {
+
+lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
+                      int H, int N, int D, int w_left, int w_right, const int32_t* dilation, int causal,
+                      const int32_t* global_idx, int n_global, float scale, void* workspace,
+                      size_t workspace_bytes, lg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // ---- argument checks (nothing is launched on failure)
+  lg_status st = validate_fwd(q, k, v, out, lse, dt, B, H, N, D, w_left, w_right, dilation, causal, global_idx,
+                              n_global, workspace, workspace_bytes, true);
+  if (st != LG_OK) return st;
 
   const int BH = B * H;
   const int wl = std::min(w_left, N);
@@ -376,7 +402,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
     tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
     tp.gidx = global_idx; tp.gcount = n_global > 0 ? reinterpret_cast<const int*>(ws + lay.cnt) : nullptr;
-    tp.status = status; tp.wait_cap = wait_cap_cycles();
+    tp.status = status; tp.wait_cap = wait_cap_cycles(); tp.withhold = withhold_for_test();
     tp.unit_counter = status + 1 + grp;   // one zeroed word of the status area per launch
     tp.scale_log2 = s * 1.4426950408889634f;
     tp.BH = BH; tp.H = H; tp.N = N; tp.D = D; tp.wl = wl; tp.wr = wr; tp.n_glob = n_global; tp.etc = 0;
@@ -469,7 +495,7 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.out = out_l; tp.lse = lse_l;
   tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
   tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
-  tp.gidx = nullptr; tp.status = status; tp.wait_cap = wait_cap_cycles();
+  tp.gidx = nullptr; tp.status = status; tp.wait_cap = wait_cap_cycles(); tp.withhold = withhold_for_test();
   tp.unit_counter = status + 1;
   tp.scale_log2 = s * 1.4426950408889634f;
   tp.BH = BH; tp.H = H; tp.N = L; tp.D = D; tp.wl = r; tp.wr = r; tp.n_glob = G; tp.etc = 1;
@@ -548,6 +574,13 @@ int64_t lg_etc_count_pairs(int L, int G, int radius) {
     band += hi - lo + 1;
   }
   return band + static_cast<int64_t>(L) * G + static_cast<int64_t>(G) * (G + L);
+}
+
+lg_status lg_debug_timeout_test(int withhold, long long wait_cap_cycles) {
+  if (withhold != 0 && withhold != 1) return LG_ERR_INVALID_ARG;
+  g_withhold.store(withhold, std::memory_order_relaxed);
+  g_wait_cap_override.store(wait_cap_cycles > 0 ? wait_cap_cycles : 0, std::memory_order_relaxed);
+  return LG_OK;
 }
 
 lg_status lg_profile_begin(void) {

@@ -55,15 +55,13 @@ extern "C" lg_status lg_attn_fwd_host(const void* q_h, const void* k_h, const vo
                                       int n_global, float scale, void* workspace, size_t workspace_bytes,
                                       int n_groups, lg_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (!q_h || !k_h || !v_h || !out_h || !lse_h || !q_d || !k_d || !v_d || !out_d || !lse_d || !dilation)
-    return LG_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || D < 1 || n_groups < 1 || (dt != LG_F32 && dt != LG_BF16)) return LG_ERR_INVALID_ARG;
-  // The full problem's checks (sizes, dilations, workspace) before anything is queued.
-  const size_t need = lg_attn_fwd_workspace_size(B, H, N, D, n_global, dt);
-  if (need == 0) return LG_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < need) return LG_ERR_WORKSPACE;
-  for (int h = 0; h < H; ++h)
-    if (dilation[h] < 1) return LG_ERR_INVALID_ARG;
+  // The whole problem's checks before anything is queued: the host pointers,
+  // the group count, and every check lg_attn_fwd makes (on the device staging
+  // buffers, which share the host tensors' shapes).
+  if (!q_h || !k_h || !v_h || !out_h || !lse_h || n_groups < 1) return LG_ERR_INVALID_ARG;
+  lg_status st = lg::validate_fwd(q_d, k_d, v_d, out_d, lse_d, dt, B, H, N, D, w_left, w_right, dilation, causal,
+                                  global_idx, n_global, workspace, workspace_bytes, false);
+  if (st != LG_OK) return st;
 
   const long long BH = static_cast<long long>(B) * H;
   long long groups = std::min<long long>(n_groups, BH);
@@ -73,7 +71,7 @@ extern "C" lg_status lg_attn_fwd_host(const void* q_h, const void* k_h, const vo
   const size_t lse_slice = static_cast<size_t>(N) * sizeof(float);
 
   cudaStream_t s_in, s_out;
-  lg_status st = copy_streams(&s_in, &s_out);
+  st = copy_streams(&s_in, &s_out);
   if (st != LG_OK) return st;
   Events evs;
   cudaEvent_t start;
@@ -83,39 +81,44 @@ extern "C" lg_status lg_attn_fwd_host(const void* q_h, const void* k_h, const vo
     return LG_ERR_CUDA;
 
   std::vector<int32_t> dil;
-  for (long long c = 0; c < groups; ++c) {
+  for (long long c = 0; c < groups && st == LG_OK; ++c) {
     const long long bh0 = c * BH / groups, bh1 = (c + 1) * BH / groups;
     const int nh = static_cast<int>(bh1 - bh0);
     const size_t off = static_cast<size_t>(bh0) * slice, bytes = static_cast<size_t>(nh) * slice;
     const size_t loff = static_cast<size_t>(bh0) * lse_slice, lbytes = static_cast<size_t>(nh) * lse_slice;
     cudaEvent_t in_done, comp_done;
-    if (evs.make(&in_done) != cudaSuccess || evs.make(&comp_done) != cudaSuccess) return LG_ERR_CUDA;
+    if (evs.make(&in_done) != cudaSuccess || evs.make(&comp_done) != cudaSuccess) { st = LG_ERR_CUDA; break; }
     if (cudaMemcpyAsync(static_cast<char*>(q_d) + off, static_cast<const char*>(q_h) + off, bytes,
                         cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
         cudaMemcpyAsync(static_cast<char*>(k_d) + off, static_cast<const char*>(k_h) + off, bytes,
                         cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
         cudaMemcpyAsync(static_cast<char*>(v_d) + off, static_cast<const char*>(v_h) + off, bytes,
                         cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
-        cudaEventRecord(in_done, s_in) != cudaSuccess || cudaStreamWaitEvent(stream, in_done, 0) != cudaSuccess)
-      return LG_ERR_CUDA;
+        cudaEventRecord(in_done, s_in) != cudaSuccess || cudaStreamWaitEvent(stream, in_done, 0) != cudaSuccess) {
+      st = LG_ERR_CUDA;
+      break;
+    }
     dil.resize(nh);
     for (int i = 0; i < nh; ++i) dil[i] = dilation[(bh0 + i) % H];
     st = lg_attn_fwd(static_cast<const char*>(q_d) + off, static_cast<const char*>(k_d) + off,
                      static_cast<const char*>(v_d) + off, static_cast<char*>(out_d) + off,
                      reinterpret_cast<float*>(reinterpret_cast<char*>(lse_d) + loff), dt, 1, nh, N, D, w_left, w_right,
                      dil.data(), causal, global_idx, n_global, scale, workspace, workspace_bytes, stream_);
-    if (st != LG_OK) return st;
+    if (st != LG_OK) break;
     if (cudaEventRecord(comp_done, stream) != cudaSuccess || cudaStreamWaitEvent(s_out, comp_done, 0) != cudaSuccess ||
         cudaMemcpyAsync(static_cast<char*>(out_h) + off, static_cast<const char*>(out_d) + off, bytes,
                         cudaMemcpyDeviceToHost, s_out) != cudaSuccess ||
         cudaMemcpyAsync(reinterpret_cast<char*>(lse_h) + loff, reinterpret_cast<const char*>(lse_d) + loff, lbytes,
                         cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
-      return LG_ERR_CUDA;
+      st = LG_ERR_CUDA;
   }
-  // The caller's stream completes after the last copy back.
-  cudaEvent_t all_out;
-  if (evs.make(&all_out) != cudaSuccess || cudaEventRecord(all_out, s_out) != cudaSuccess ||
-      cudaStreamWaitEvent(stream, all_out, 0) != cudaSuccess)
+  // On every path from here, success or not, the caller's stream completes
+  // only after everything queued on the two copy streams, so a caller that
+  // synchronises `stream` after an error may free its buffers safely.
+  cudaEvent_t all_in, all_out;
+  if (evs.make(&all_in) != cudaSuccess || evs.make(&all_out) != cudaSuccess ||
+      cudaEventRecord(all_in, s_in) != cudaSuccess || cudaEventRecord(all_out, s_out) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, all_in, 0) != cudaSuccess || cudaStreamWaitEvent(stream, all_out, 0) != cudaSuccess)
     return LG_ERR_CUDA;
-  return LG_OK;
+  return st;
 }

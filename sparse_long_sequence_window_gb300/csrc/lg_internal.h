@@ -95,6 +95,7 @@ struct TcParams {
   int grow_split;                 // key tiles per split of a global-query row block
   int n_tail_split;               // last band units split into two one-tile units each
   long long wait_cap;             // clock64 cycles a bounded wait may spin
+  int withhold;                   // test of the timeout path: issue no TMA load and no MMA
   float scale_log2;               // scale * log2(e)
   int BH, H, N, D;                // N = L for ETC
   int wl, wr;                     // wr already 0 when causal
@@ -137,6 +138,17 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain
 cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 size_t tc_smem_bytes(int D);
+// Cap of the bounded work waits (clock64 cycles) and the timeout-test switch,
+// as set by lg_debug_timeout_test (default: about one second, no withholding).
+long long wait_cap_cycles();
+int withhold_for_test();
+// Every argument check of lg_attn_fwd (sizes, values, pointers, workspace),
+// without any CUDA call.  per_call_head_limit: also refuse H > LG_MAX_HEADS
+// (one kernel call); the host-memory entry point splits larger problems.
+lg_status validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right, const int32_t* dilation,
+                       int causal, const int32_t* global_idx, int n_global, const void* workspace,
+                       size_t workspace_bytes, bool per_call_head_limit);
 int device_sm_count();  // SMs of the current device (cached per device)
 
 }  // namespace lg

@@ -34,6 +34,9 @@
 // softmax runs; because the MMAs of one thread execute in order, the
 // completion of QK_q(j) also means PV_q(j-1) is done, and the softmax may
 // rescale O_q and overwrite S_q with P_q without further waits.
+#include <atomic>
+#include <mutex>
+
 #include "lg_internal.h"
 #include "lg_ptx.cuh"
 
@@ -52,6 +55,11 @@ constexpr int kUnitSlots = 4;              // ring of claimed unit indices
 constexpr int kTailRounds = 2;             // rounds of units claimed dynamically at the end
 constexpr int kUnitReaders = 11;           // V producer + two issuing warps + eight softmax warps  // log2 units; O is rescaled only when the max grows more
 constexpr float kLn2 = 0.6931471805599453f;
+// Bound of the drain waits, which hold a CTA until the TMA loads and MMAs it
+// has already issued complete (always finite) before TMEM and shared memory
+// are released: fixed, about two seconds, and independent of the cap of the
+// work waits (which a caller may shorten).
+constexpr long long kDrainCap = 4000000000LL;
 
 #ifndef LG_TC_KSTAGES128
 #define LG_TC_KSTAGES128 2
@@ -398,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         int un = -1;
         if (is_k && !publish(k + 1, un = claim(k + 1))) { fail(); ok = false; break; }
         const Unit w = decode_unit(p, u);
-        for (int j = 0; j < w.n_tiles; ++j, ++g) {
+        // (p.withhold: a test of the timeout path; no load is issued, so the
+        // consumers' first wait runs out with nothing in flight.)
+        for (int j = 0; j < w.n_tiles && !p.withhold; ++j, ++g) {
           const CUtensorMap* m;
           bool strided;
           int y;
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       // Drain: every load issued here has landed before the CTA exits (these
       // waits ignore the abort flag and are bounded by the cap alone).
       for (int x = max(0, issued - S); x < issued; ++x)
-        mbar_wait(bar(b_full + x % S), (x / S) & 1, nullptr, cap);
+        mbar_wait(bar(b_full + x % S), (x / S) & 1, nullptr, kDrainCap);
     }
   } else {
     // ------------------------------------------------------------ MMA issuers
@@ -478,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       return v;
     };
     int u = unit_in_slot(0);
-    if (u >= 0) {
+    if (u >= 0 && !p.withhold) {   // withhold: no Q load and (no K tile arrives) no MMA
       if (leader) load_q(q, decode_unit(p, u));
       __syncwarp();
       ++q_loads;
@@ -635,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     }
     // Drain: a Q load issued for a unit never started has landed, and every
     // MMA issued here has completed before TMEM is released.
-    if (q_loads > q_seen) mbar_wait(bar(B_QFULL + q), q_seen & 1, nullptr, cap);
+    if (q_loads > q_seen) mbar_wait(bar(B_QFULL + q), q_seen & 1, nullptr, kDrainCap);
     if (leader) umma_commit(bar(B_FIN + q));
     __syncwarp();
-    mbar_wait(bar(B_FIN + q), 0, nullptr, cap);
+    mbar_wait(bar(B_FIN + q), 0, nullptr, kDrainCap);
   }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
@@ -923,15 +933,31 @@ int grid_for(int n_units) {
   return n_units < sms ? n_units : sms;
 }
 
+namespace {
+// The shared-memory attribute is a per-device setting: set it once for each
+// device and head size, under a lock (calls may come from several threads).
+constexpr int kMaxDevices = 64;
+std::mutex g_attr_mutex;
+bool g_attr_done[kMaxDevices][2] = {};
+}  // namespace
+
+cudaError_t ensure_kernel_attributes(int i) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (g_attr_done[dev][i]) return cudaSuccess;
+  e = i == 0 ? prepare_kernel<64>() : prepare_kernel<128>();
+  if (e == cudaSuccess) g_attr_done[dev][i] = true;
+  return e;
+}
+
 cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table) {
   if (n_units <= 0) return cudaSuccess;
-  static bool attr_done[2] = {false, false};
   const int i = p.D == 64 ? 0 : 1;
-  if (!attr_done[i]) {
-    cudaError_t e = i == 0 ? prepare_kernel<64>() : prepare_kernel<128>();
-    if (e != cudaSuccess) return e;
-    attr_done[i] = true;
-  }
+  cudaError_t ea = ensure_kernel_attributes(i);
+  if (ea != cudaSuccess) return ea;
   cudaError_t e = launch_kernel(unit_table_kernel, dim3((n_units + 255) / 256), dim3(256), 0, s, chain_table, p, n_units);
   if (e != cudaSuccess) return e;
   if (i == 0)
@@ -940,15 +966,15 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain
 }
 
 int device_sm_count() {
-  static int sms[64] = {0};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (sms[dev] == 0) {
-    int v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-    sms[dev] = v;
+    sms[dev].store(v, std::memory_order_relaxed);
   }
-  return sms[dev];
+  return v;
 }
 
 int tc_rows_per_load(int d) { return rows_per_load(d); }

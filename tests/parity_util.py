@@ -35,41 +35,44 @@ def compare(name, dtype, out_gpu, lse_gpu, out_ref, lse_ref):
     return float(err.max()), float(err.mean()), float(lerr.max())
 
 
-def run_longformer(lg, w: workloads.Workload, rows=None):
-    """CUDA path vs oracle for a (non-ETC) workload; rows=None compares every row."""
+def run_longformer(lg, w: workloads.Workload, rows=None, scale=None):
+    """CUDA path vs oracle for a (non-ETC) workload; rows=None compares every row.
+
+    scale: the logit scale passed to both sides (None: the default 1/sqrt(D))."""
     inp = workloads.make_inputs(w)
     dev = torch.device("cuda")
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     g = inp["global_idx"]
     gd = torch.from_numpy(g).to(dev) if g.size else None
-    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd)
+    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd, scale=scale)
     torch.cuda.synchronize()
     st = lg.query_status(lg.attn_fwd.last_workspace)
     assert st == 0, lg.status_string(st)
     qn, kn, vn = (to_np32(inp[n]) for n in ("q", "k", "v"))
     if rows is None:
-        ref_o, ref_l = lg_oracle.attn_fwd(qn, kn, vn, w.w_left, w.w_right, w.dilations(), w.causal, g)
+        ref_o, ref_l = lg_oracle.attn_fwd(qn, kn, vn, w.w_left, w.w_right, w.dilations(), w.causal, g, scale=scale)
         return compare(w.name, w.dtype, out.cpu(), lse.cpu(), ref_o, ref_l)
     rows = np.asarray(sorted(set(int(r) for r in rows if 0 <= r < w.N)), dtype=np.int64)
-    ref_o, ref_l = lg_oracle.attn_fwd_rows(qn, kn, vn, w.w_left, w.w_right, w.dilations(), w.causal, g, rows)
+    ref_o, ref_l = lg_oracle.attn_fwd_rows(qn, kn, vn, w.w_left, w.w_right, w.dilations(), w.causal, g, rows,
+                                           scale=scale)
     return compare(w.name, w.dtype, out.cpu()[:, :, rows], lse.cpu()[:, :, rows], ref_o, ref_l)
 
 
-def run_etc(lg, w: workloads.Workload, long_rows=None):
+def run_etc(lg, w: workloads.Workload, long_rows=None, scale=None):
     inp = workloads.make_inputs(w)
     dev = torch.device("cuda")
     t = [inp[n].to(dev) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
-    out_l, out_g, lse_l, lse_g = lg.etc_attn_fwd(*t, w.radius)
+    out_l, out_g, lse_l, lse_g = lg.etc_attn_fwd(*t, w.radius, scale=scale)
     torch.cuda.synchronize()
     st = lg.query_status(lg.etc_attn_fwd.last_workspace)
     assert st == 0, lg.status_string(st)
     npx = [to_np32(inp[n]) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
     if long_rows is None:
-        rl, rg, rll, rlg = lg_oracle.etc_attn_fwd(*npx, w.radius)
+        rl, rg, rll, rlg = lg_oracle.etc_attn_fwd(*npx, w.radius, scale=scale)
         a = compare(w.name + " long", w.dtype, out_l.cpu(), lse_l.cpu(), rl, rll)
     else:
         long_rows = np.asarray(sorted(set(int(r) for r in long_rows if 0 <= r < w.N)), dtype=np.int64)
-        rl, rg, rll, rlg = lg_oracle.etc_attn_fwd_rows(*npx, w.radius, long_rows)
+        rl, rg, rll, rlg = lg_oracle.etc_attn_fwd_rows(*npx, w.radius, long_rows, scale=scale)
         a = compare(w.name + " long", w.dtype, out_l.cpu()[:, :, long_rows], lse_l.cpu()[:, :, long_rows], rl, rll)
     b = compare(w.name + " global", w.dtype, out_g.cpu(), lse_g.cpu(), rg, rlg)
     return a, b

@@ -161,6 +161,20 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert call(dil=(ctypes.c_int32 * 2)(1, 0)) == lg.LG_ERR_INVALID_ARG
     assert call(wsb=64) == lg.LG_ERR_WORKSPACE
     assert call(ws=None) == lg.LG_ERR_WORKSPACE
+    # Checks of the whole problem come before the first copy is queued (the
+    # FAKE pointers would fault any copy): a bf16 dilation beyond the limit on
+    # the last head, with the heads split over two groups; D unsupported by the
+    # tensor cores; a misaligned staging buffer; a missing global list.
+    assert call(dil=(ctypes.c_int32 * 2)(1, 9), groups=2) == lg.LG_ERR_UNSUPPORTED
+    assert call(D=96, groups=2) == lg.LG_ERR_UNSUPPORTED
+    assert call(ptrs=[FAKE] * 6 + [FAKE + 8] + [FAKE] * 3) == lg.LG_ERR_INVALID_ARG
+    assert call(ng=4, gidx=None, groups=2) == lg.LG_ERR_INVALID_ARG
+    assert call(causal=3) == lg.LG_ERR_INVALID_ARG
+
+
+def test_debug_timeout_switch_checks_its_argument(lib):
+    assert lib.lg_debug_timeout_test(2, 0) == lg.LG_ERR_INVALID_ARG
+    assert lib.lg_debug_timeout_test(0, 0) == lg.LG_OK
 
 
 def test_binding_checks_tensors_before_the_library(lib):

@@ -8,9 +8,14 @@
    Transformers to 1,000,000,000 Tokens", section 3.4, "Mixture of Dilated
    Attentions") reproduces the unsharded row.  The arithmetic here is the CPU
    oracle's; only the protocol is under test.
+3. A rank that dies before that exchange: the survivor's collective gives up
+   within a short process-group timeout and reports an error; it does not
+   hang.  (The failure is made on the host: the rank exits.)
 """
+import datetime
 import os
 import socket
+import time
 
 import numpy as np
 import pytest
@@ -68,3 +73,46 @@ def test_two_ranks_gloo():
         assert t == 15.0                                  # slowest rank's time on every rank
         assert v == pytest.approx(1e12 * 4 * 2 / 15e-3 / 1e12)
         assert err_o < 1e-12 and err_l < 1e-12
+
+
+EXCHANGE_TIMEOUT_S = 10
+
+
+def _worker_killed(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=EXCHANGE_TIMEOUT_S))
+    if rank == 1:
+        os._exit(0)            # dies after joining, before the exchange of partial statistics
+    from oracle import lg_oracle
+    rng = np.random.default_rng(1)
+    qq, kk, vv = rng.standard_normal((2, 8)), rng.standard_normal((16, 8)), rng.standard_normal((16, 8))
+    mask = np.zeros((2, 16), bool); mask[:, :8] = True
+    m, l, acc = lg_oracle.partial_stats(qq, kk, vv, mask, 0.5)
+    pack = torch.from_numpy(np.concatenate([m[:, None], l[:, None], acc], axis=1))
+    parts = [torch.zeros_like(pack) for _ in range(world)]
+    t0 = time.monotonic()
+    try:
+        dist.all_gather(parts, pack)
+        q.put(("no error", time.monotonic() - t0))
+    except Exception as e:  # the survivor learns of the dead peer from the collective
+        q.put((type(e).__name__, time.monotonic() - t0))
+    os._exit(0)                # the process group is broken; leave without a collective teardown
+
+
+def test_killed_rank_times_out_instead_of_hanging():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_killed, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    what, secs = q.get(timeout=EXCHANGE_TIMEOUT_S + 60)
+    for p in procs:
+        p.join(timeout=30)
+        if p.is_alive():
+            p.kill()
+            pytest.fail("a rank did not exit")
+    assert what != "no error", "the exchange with a dead rank did not fail"
+    assert secs <= EXCHANGE_TIMEOUT_S + 5

@@ -90,6 +90,29 @@ def test_bf16_etc_star(cuda_lib):
     pu.run_etc(cuda_lib, W("bf16 etc star", "bf16", 1, 2, 300, 64, 0, 0, etc_G=1, radius=1))
 
 
+# ---------------------------------------------------------------- a logit scale other than 1/sqrt(D)
+
+SCALE_CASES = [
+    (W("f32 scale dilated globals", "f32", 1, 3, 300, 64, 20, 12, (1, 2, 3), False, (0, 150, 299)), 0.37),
+    (W("f32 scale causal", "f32", 1, 2, 200, 32, 30, 30, (1, 4), True, (7,)), 0.05),
+    (W("bf16 scale D64 dilated globals", "bf16", 1, 4, 900, 64, 50, 30, (1, 2, 3, 5), False, (0, 5, 450, 899)), 0.37),
+    (W("bf16 scale D64 causal", "bf16", 1, 2, 700, 64, 100, 0, (1, 2), True, None, 9), 0.05),
+    (W("bf16 scale D128 dilated globals", "bf16", 1, 3, 1100, 128, 64, 64, (1, 2, 4), False, None, 40), 0.37),
+    (W("bf16 scale D128 causal", "bf16", 1, 2, 800, 128, 90, 0, (3, 1), True, (0, 799)), 0.05),
+]
+
+
+@pytest.mark.parametrize("w,scale", SCALE_CASES, ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_explicit_scale(cuda_lib, w, scale):
+    """The ABI's scale argument, taken by both the kernels and the oracle."""
+    pu.run_longformer(cuda_lib, w, scale=scale)
+
+
+@pytest.mark.parametrize("dtype,D,scale", [("f32", 32, 0.37), ("bf16", 64, 0.05), ("bf16", 128, 0.37)])
+def test_explicit_scale_etc(cuda_lib, dtype, D, scale):
+    pu.run_etc(cuda_lib, W(f"{dtype} etc scale D{D}", dtype, 1, 2, 500, D, 0, 0, etc_G=40, radius=15), scale=scale)
+
+
 # ---------------------------------------------------------------- the reference workloads at full size
 
 def test_longformer_base_full(cuda_lib):
