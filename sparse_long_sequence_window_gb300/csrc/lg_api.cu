@@ -60,14 +60,16 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int rows, int BH, int d
   return r == CUDA_SUCCESS;
 }
 
-// bf16 output viewed as {D, rows, BH} for tiled stores of 32 rows x 64 columns.
-bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH) {
+// bf16 output viewed as {D, rows, BH} for tiled stores of 32 rows x 64
+// columns, the rows `d` apart (element stride d along the row dimension, a
+// box of 32*d rows: the 32 rows of one dilation residue class).
+bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH, int d) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-  cuuint32_t box[3] = {64, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(32 * d), 1};
+  cuuint32_t estr[3] = {1, static_cast<cuuint32_t>(d), 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -370,14 +372,13 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
       tp.slot_dil[sl] = slot_d[sl];
       tp.slot_units[sl] = band_units_for(N, slot_d[sl]);
       if (!encode_map(&tp.mapQ[sl], q, D, N, BH, slot_d[sl]) || !encode_map(&tp.mapK[sl], k, D, N, BH, slot_d[sl]) ||
-          !encode_map(&tp.mapV[sl], v, D, N, BH, slot_d[sl]))
+          !encode_map(&tp.mapV[sl], v, D, N, BH, slot_d[sl]) || !encode_store_map(&tp.mapO[sl], out, D, N, BH, slot_d[sl]))
         return LG_ERR_CUDA;
     }
     for (int sl = n_slots; sl < kMaxSlots; ++sl) {
       tp.slot_dil[sl] = 1;
-      tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0];
+      tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
     }
-    if (!encode_store_map(&tp.mapO, out, D, N, BH)) return LG_ERR_CUDA;
     if (n_global > 0) {
       if (!encode_map(&tp.mapQg, qg, D, n_global, BH, 0) || !encode_map(&tp.mapKg, kg, D, n_global, BH, 0) ||
           !encode_map(&tp.mapVg, vg, D, n_global, BH, 0))
@@ -479,10 +480,11 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
       !encode_map(&tp.mapV[0], v_l, D, L, BH, 1) || !encode_map(&tp.mapQg, q_g, D, G, BH, 0) ||
       !encode_map(&tp.mapKg, k_g, D, G, BH, 0) || !encode_map(&tp.mapVg, v_g, D, G, BH, 0) ||
-      !encode_store_map(&tp.mapO, out_l, D, L, BH))
+      !encode_store_map(&tp.mapO[0], out_l, D, L, BH, 1))
     return LG_ERR_CUDA;
   for (int sl = 1; sl < kMaxSlots; ++sl) {
-    tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.slot_dil[sl] = 1;
+    tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
+    tp.slot_dil[sl] = 1;
   }
   tp.slot_dil[0] = 1;
   tp.slot_units[0] = band_units_for(L, 1);

@@ -82,7 +82,7 @@ struct TcParams {
   CUtensorMap mapK[kMaxSlots];
   CUtensorMap mapV[kMaxSlots];
   CUtensorMap mapQg, mapKg, mapVg;  // global side {D, g, BH}: gathered rows (Longformer) or q_g/k_g/v_g (ETC)
-  CUtensorMap mapO;               // output {D, N, BH}, boxes of 32 rows x 64 columns (stores of d = 1 rows)
+  CUtensorMap mapO[kMaxSlots];    // output {D, N, BH}, boxes of 32 rows x 64 columns, rows strided by the slot's dilation
   void* out;                      // bf16 [BH, N, D]
   float* lse;                     // [BH, N]
   float* part_acc;                // [BH, n_glob, n_parts, D] unnormalised partial outputs

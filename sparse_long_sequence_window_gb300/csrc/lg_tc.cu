@@ -186,6 +186,13 @@ __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_unit
   grid_dep_wait();     // complete only after the call's earlier kernels
 }
 
+// Brings unit u's 64-byte record into this SM's L1 (shared by every warp of
+// the CTA), so that the decode at the start of that unit does not wait for L2.
+__device__ __forceinline__ void prefetch_unit(const TcParams& p, int u) {
+  if (u >= 0)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const int4*>(p.units) + 4 * static_cast<size_t>(u)));
+}
+
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   const int4* rec = reinterpret_cast<const int4*>(p.units) + 4 * static_cast<size_t>(u);
   const int4 a = __ldg(rec), b = __ldg(rec + 1), c = __ldg(rec + 2), d = __ldg(rec + 3);
@@ -404,7 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       if (!ok) fail();
       for (int k = 0; ok && u >= 0; ++k) {
         int un = -1;
-        if (is_k && !publish(k + 1, un = claim(k + 1))) { fail(); ok = false; break; }
+        if (is_k) {
+          if (!publish(k + 1, un = claim(k + 1))) { fail(); ok = false; break; }
+          prefetch_unit(p, un);   // every role decodes it at its next unit
+        }
         const Unit w = decode_unit(p, u);
         // (p.withhold: a test of the timeout path; no load is issued, so the
         // consumers' first wait runs out with nothing in flight.)
@@ -418,6 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
           load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
           issued = g + 1;
+          // At the start of a launch every CTA wants its first tiles at once:
+          // the CTA's first tile lands before the rest of the ring is
+          // requested, so that it does not queue behind the others' prefetches.
         }
         if (ok && !is_k && !take(k + 1, un)) { fail(); ok = false; }
         u = un;
@@ -837,60 +850,67 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       if (n_unit > 0) {
         if (!wait_all(bar(B_ODONE + q), nact & 1)) { fail(); ok = false; break; }
         tc_fence_after();
-        float o[D];
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, *reinterpret_cast<float(*)[32]>(o + cc * 32));
-        tc_fence_before();
-        mbar_arrive(bar(B_OFREE + q));                  // O may be overwritten by the next unit
         ++nact;
+        // The epilogue reads O 32 columns at a time in rolled loops: this code
+        // runs once per unit, and kept small it evicts less of the tile loop
+        // from the instruction cache.  O_q is released (OFREE) after its last
+        // read; the next unit's first PV_q waits for that.
         if (!w.grow) {
           const float inv_l = row_valid ? 1.f / l_run : 0.f;
-          if (w.d == 1) {
-            // Consecutive rows: each warp stages its 32 rows, 64 columns at a
-            // time, in shared memory (128-byte swizzle, conflict-free) and
-            // writes them with one TMA store per 64 columns; rows past the
-            // end of the sequence are clipped by the store.
-            const uint32_t stage = sbase + C::kOffStage + (warp - 4) * 4096;
-            const int row0 = w.c + w.t0 + q * kTileM + 32 * (warp & 3);
+          // Each warp stages its 32 rows (positions c + d*t of one residue
+          // class), 64 columns at a time, in shared memory (128-byte swizzle,
+          // conflict-free) and writes them with one TMA store per 64 columns
+          // through the slot's store map, whose element stride d puts row k of
+          // the box at position row0 + d*k; rows past the end of the sequence
+          // are clipped by the store.
+          const uint32_t stage = sbase + C::kOffStage + (warp - 4) * 4096;
+          const int row0 = w.c + w.d * (w.t0 + q * kTileM + 32 * (warp & 3));
+#pragma unroll 1
+          for (int half = 0; half < D / 64; ++half) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+              float o[32];
+              tmem_ld32(tO + half * 64 + cc * 32, o);
 #pragma unroll
-            for (int half = 0; half < D / 64; ++half) {
-              if (lane == 0) bulk_wait_read_all();   // this buffer's previous store has read it
-              __syncwarp();
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const float* v = o + half * 64 + 8 * c;
-                st_shared_v4(stage + lane * 128 + ((c ^ (lane & 7)) << 4), pack_bf16x2(v[0] * inv_l, v[1] * inv_l),
-                             pack_bf16x2(v[2] * inv_l, v[3] * inv_l), pack_bf16x2(v[4] * inv_l, v[5] * inv_l),
-                             pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_store_3d(&p.mapO, stage, half * 64, row0, w.bh);
-                bulk_commit_group();
+              for (int c = 0; c < 4; ++c) {
+                const int ci = cc * 4 + c;
+                st_shared_v4(stage + lane * 128 + ((ci ^ (lane & 7)) << 4), pack_bf16x2(o[8 * c] * inv_l, o[8 * c + 1] * inv_l),
+                             pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l),
+                             pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l),
+                             pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l));
               }
             }
-          } else if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                  (static_cast<size_t>(w.bh) * p.N + pos_q) * D);
-#pragma unroll
-            for (int k = 0; k < D / 8; ++k) {
-              uint4 val;
-              val.x = pack_bf16x2(o[8 * k + 0] * inv_l, o[8 * k + 1] * inv_l);
-              val.y = pack_bf16x2(o[8 * k + 2] * inv_l, o[8 * k + 3] * inv_l);
-              val.z = pack_bf16x2(o[8 * k + 4] * inv_l, o[8 * k + 5] * inv_l);
-              val.w = pack_bf16x2(o[8 * k + 6] * inv_l, o[8 * k + 7] * inv_l);
-              dst[k] = val;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&p.mapO[w.slot], stage, half * 64, row0, w.bh);
+              bulk_commit_group();
             }
           }
+          tc_fence_before();
+          mbar_arrive(bar(B_OFREE + q));
           if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
-        } else if (row_valid) {
-          const int slot = (w.kt0 / p.grow_split) * 2 + q;   // partial slot of this warpgroup
-          const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D);
+        } else {
+          {
+            // Every lane takes part in the warp-collective TMEM loads; only valid rows store.
+            const int slot = (w.kt0 / p.grow_split) * 2 + q;
+            const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.grow0 + r) * p.n_parts + slot;
+            float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D);
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              float o[32];
+              tmem_ld32(tO + cc * 32, o);
+              if (row_valid) {
 #pragma unroll
-          for (int k = 0; k < D / 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-          reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
+                for (int k = 0; k < 8; ++k) dst[8 * cc + k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+              }
+            }
+            if (row_valid) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
+          }
+          tc_fence_before();
+          mbar_arrive(bar(B_OFREE + q));
         }
       } else if (w.grow && row_valid) {
         // A warpgroup with no key tile in this split leaves an empty partial.
