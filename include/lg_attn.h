@@ -1,6 +1,6 @@
 /*
  * lg_attn.h -- C ABI of the window + dilation + global sparse self-attention
- * forward pass for one NVIDIA GB300 GPU (sm_103a).
+ * forward and backward passes for one NVIDIA GB300 GPU (sm_103a).
  *
  * What is computed (per batch b and head h, query i, key j, 0 <= i, j < N):
  *
@@ -201,6 +201,60 @@ size_t lg_etc_attn_fwd_workspace_size(int B, int H, int L, int G, int D, lg_dtyp
 lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l,
                           const void* q_g, const void* k_g, const void* v_g,
                           void* out_l, void* out_g, float* lse_l, float* lse_g,
+                          lg_dtype dt, int B, int H, int L, int G, int D, int radius, float scale,
+                          void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/*
+ * Backward pass.  The gradients of the forward's function with respect to q,
+ * k and v, given dO = dLoss/dout (the gradient of the LSE output is taken as
+ * zero): the chain rule of the same masked softmax, with P recomputed from
+ * the forward's saved out and lse instead of a second softmax pass,
+ *   P_ij = exp(s <q_i, k_j> - LSE_i) on the allowed pairs, 0 elsewhere,
+ *   dV = P^T dO,  Delta_i = <dO_i, out_i>,  dS_ij = P_ij (<dO_i, v_j> - Delta_i),
+ *   dQ = s dS K,  dK = s dS^T Q.
+ * The pages train with this attention and take these gradients through it
+ * ("LONGNET: Scaling Transformers to 1,000,000,000 Tokens", section 3.4,
+ * "Distributed Training Algorithm": the gradients of the keys and values;
+ * "Longformer", "Autoregressive Language Modeling Configuration": the
+ * activations recomputed in the backward pass).
+ *
+ * Bytes of device workspace lg_attn_bwd needs (256-byte aligned); 0 if the
+ * sizes are invalid.  It holds the status word, Delta and LSE per row, the
+ * gathered global rows and the partial sums of the global rows and keys.
+ */
+size_t lg_attn_bwd_workspace_size(int B, int H, int N, int D, int n_global, lg_dtype dt);
+
+/*
+ *  q, k, v, out, lse   the forward's inputs and outputs (as for lg_attn_fwd).
+ *  dout         device, [B, H, N, D], dtype dt: the gradient of out.
+ *  dq, dk, dv   device, [B, H, N, D], dtype dt, written (every row).
+ *  Every other argument, the layouts, the checks and the errors are those of
+ *  lg_attn_fwd, with this call's workspace size.  bf16: tensor cores, fp32
+ *  accumulation, outputs rounded to bf16; fp32: CUDA cores (dk and dv are
+ *  accumulated with atomic additions, so their low bits may differ between
+ *  calls).  Asynchronous on `stream`.
+ */
+lg_status lg_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv,
+                      lg_dtype dt, int B, int H, int N, int D,
+                      int w_left, int w_right, const int32_t* dilation, int causal,
+                      const int32_t* global_idx, int n_global, float scale,
+                      void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/* Bytes of device workspace lg_etc_attn_bwd needs; 0 if the sizes are invalid. */
+size_t lg_etc_attn_bwd_workspace_size(int B, int H, int L, int G, int D, lg_dtype dt);
+
+/*
+ * Backward of lg_etc_attn_fwd: gradients of the long input (dq_l, dk_l, dv_l,
+ * [B, H, L, D]) and of the global input (dq_g, dk_g, dv_g, [B, H, G, D]),
+ * given the forward's outputs and lse and the gradients dout_l, dout_g of
+ * out_l, out_g.  Layouts, checks and errors as for lg_etc_attn_fwd.
+ */
+lg_status lg_etc_attn_bwd(const void* q_l, const void* k_l, const void* v_l,
+                          const void* q_g, const void* k_g, const void* v_g,
+                          const void* out_l, const void* out_g, const float* lse_l, const float* lse_g,
+                          const void* dout_l, const void* dout_g,
+                          void* dq_l, void* dk_l, void* dv_l, void* dq_g, void* dk_g, void* dv_g,
                           lg_dtype dt, int B, int H, int L, int G, int D, int radius, float scale,
                           void* workspace, size_t workspace_bytes, lg_stream_t stream);
 

@@ -1,4 +1,4 @@
-"""Window + dilation + global sparse self-attention (forward) for one GB300 GPU.
+"""Window + dilation + global sparse self-attention (forward and backward) for one GB300 GPU.
 
 Python binding of the C ABI in ``include/lg_attn.h``.  This module only
 marshals arguments (device pointers, sizes, the current CUDA stream) into the
@@ -17,6 +17,7 @@ import numpy as np
 
 __all__ = [
     "LgError", "load", "attn_fwd", "attn_fwd_host", "etc_attn_fwd", "attn_fwd_workspace_size",
+    "attn_bwd", "etc_attn_bwd", "attn_bwd_workspace_size", "etc_attn_bwd_workspace_size",
     "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
     "profile_begin", "profile_end", "status_string", "debug_timeout_test", "LIB_PATH",
 ]
@@ -65,6 +66,14 @@ def load() -> ctypes.CDLL:
     lib.lg_count_pairs.argtypes = [i32, i32, i32, i32, i32, vp, i32]
     lib.lg_etc_count_pairs.restype = ctypes.c_int64
     lib.lg_etc_count_pairs.argtypes = [i32, i32, i32]
+    lib.lg_attn_bwd_workspace_size.restype = sz
+    lib.lg_attn_bwd_workspace_size.argtypes = [i32] * 6
+    lib.lg_etc_attn_bwd_workspace_size.restype = sz
+    lib.lg_etc_attn_bwd_workspace_size.argtypes = [i32] * 6
+    lib.lg_attn_bwd.restype = i32
+    lib.lg_attn_bwd.argtypes = [vp] * 9 + [i32] * 7 + [vp, i32, vp, i32, f32, vp, sz, vp]
+    lib.lg_etc_attn_bwd.restype = i32
+    lib.lg_etc_attn_bwd.argtypes = [vp] * 18 + [i32] * 7 + [f32, vp, sz, vp]
     lib.lg_debug_timeout_test.restype = i32
     lib.lg_debug_timeout_test.argtypes = [i32, ctypes.c_longlong]
     lib.lg_profile_begin.restype = i32
@@ -294,6 +303,84 @@ def etc_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius: int, scale: Optional[floa
         _keep_for(stream, ws)
     etc_attn_fwd.last_workspace = ws
     return out_l, out_g, lse_l, lse_g
+
+
+def attn_bwd_workspace_size(B, H, N, D, n_global, dtype_code) -> int:
+    return int(load().lg_attn_bwd_workspace_size(B, H, N, D, n_global, dtype_code))
+
+
+def etc_attn_bwd_workspace_size(B, H, L, G, D, dtype_code) -> int:
+    return int(load().lg_etc_attn_bwd_workspace_size(B, H, L, G, D, dtype_code))
+
+
+def attn_bwd(q, k, v, out, lse, dout, w_left: int, w_right: int, dilation: Optional[Sequence[int]] = None,
+             causal: bool = False, global_idx=None, scale: Optional[float] = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd: (dq, dk, dv) given the forward's out and lse and dout.
+
+    Same arguments as attn_fwd plus out [B, H, N, D], lse [B, H, N] float32 and
+    dout [B, H, N, D].  Asynchronous on the current stream.
+    """
+    import torch
+    lib = load()
+    if q.dim() != 4 or not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor [B, H, N, D]")
+    _same(q, "k", k, v, out, dout)
+    B, H, N, D = q.shape
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
+    dil = np.ascontiguousarray(np.asarray(dilation if dilation is not None else [1] * H, dtype=np.int32))
+    if dil.size != H:
+        raise ValueError("dilation needs H entries")
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    if global_idx is not None and (global_idx.dtype != torch.int32 or global_idx.device != q.device):
+        raise TypeError("global_idx must be an int32 tensor on q's device")
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_out(t, q.shape, q.dtype, q.device, name)
+    need = attn_bwd_workspace_size(B, H, N, D, n_global, dt)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.lg_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                         dt, B, H, N, D, int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
+                         _ptr(global_idx) if n_global else None, n_global, float(scale) if scale else 0.0,
+                         ws.data_ptr(), _nbytes(ws), _stream(stream))
+    _check(st, "lg_attn_bwd")
+    if workspace is None:
+        _keep_for(stream, ws)
+    attn_bwd.last_workspace = ws
+    return dq, dk, dv
+
+
+def etc_attn_bwd(q_l, k_l, v_l, q_g, k_g, v_g, out_l, out_g, lse_l, lse_g, dout_l, dout_g, radius: int,
+                 scale: Optional[float] = None, workspace=None, stream=None):
+    """Backward of etc_attn_fwd.  Returns (dq_l, dk_l, dv_l, dq_g, dk_g, dv_g)."""
+    import torch
+    lib = load()
+    if q_l.dim() != 4 or q_g.dim() != 4 or not q_l.is_cuda:
+        raise ValueError("q_l, q_g must be CUDA tensors [B, H, L, D] and [B, H, G, D]")
+    _same(q_l, "long input", k_l, v_l, out_l, dout_l)
+    _same(q_g, "global input", k_g, v_g, out_g, dout_g)
+    B, H, L, D = q_l.shape
+    G = q_g.shape[2]
+    if q_g.shape[:2] != q_l.shape[:2] or q_g.shape[3] != D or q_g.dtype != q_l.dtype or q_g.device != q_l.device:
+        raise ValueError("q_g must match q_l in B, H, D, dtype and device")
+    _check_out(lse_l, (B, H, L), torch.float32, q_l.device, "lse_l")
+    _check_out(lse_g, (B, H, G), torch.float32, q_l.device, "lse_g")
+    dt = _dtype_code(q_l)
+    grads = [torch.empty_like(x) for x in (q_l, q_l, q_l, q_g, q_g, q_g)]
+    need = etc_attn_bwd_workspace_size(B, H, L, G, D, dt)
+    ws = _workspace(need, q_l.device, workspace)
+    st = lib.lg_etc_attn_bwd(_ptr(q_l), _ptr(k_l), _ptr(v_l), _ptr(q_g), _ptr(k_g), _ptr(v_g),
+                             _ptr(out_l), _ptr(out_g), _ptr(lse_l), _ptr(lse_g), _ptr(dout_l), _ptr(dout_g),
+                             *(_ptr(x) for x in grads), dt, B, H, L, G, D, int(radius),
+                             float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
+    _check(st, "lg_etc_attn_bwd")
+    if workspace is None:
+        _keep_for(stream, ws)
+    etc_attn_bwd.last_workspace = ws
+    return tuple(grads)
 
 
 def query_status(workspace, stream=None) -> int:

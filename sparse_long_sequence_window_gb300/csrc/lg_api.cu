@@ -257,14 +257,14 @@ long long wait_cap_cycles() {
 
 int withhold_for_test() { return g_withhold.load(std::memory_order_relaxed); }
 
-// Every argument check of lg_attn_fwd, on sizes and pointers only (no CUDA
-// call).  max_heads_per_call: the head count one kernel call may hold
-// (lg_attn_fwd: LG_MAX_HEADS; the host-memory entry point splits larger
-// problems into groups of at most that many slices).
-lg_status validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                       lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right, const int32_t* dilation,
-                       int causal, const int32_t* global_idx, int n_global, const void* workspace,
-                       size_t workspace_bytes, bool per_call_head_limit) {
+// Every argument check of lg_attn_fwd but the workspace, on sizes and
+// pointers only (no CUDA call).  per_call_head_limit: refuse H >
+// LG_MAX_HEADS (the host-memory entry point splits larger problems into
+// groups of at most that many slices).
+lg_status validate_fwd_args(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                            lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right,
+                            const int32_t* dilation, int causal, const int32_t* global_idx, int n_global,
+                            bool per_call_head_limit) {
   if (!valid_dt(dt) || B < 1 || H < 1 || N < 1 || w_left < 0 || w_right < 0 || (causal != 0 && causal != 1) ||
       n_global < 0 || n_global > N || dilation == nullptr)
     return LG_ERR_INVALID_ARG;
@@ -281,6 +281,16 @@ lg_status validate_fwd(const void* q, const void* k, const void* v, const void* 
   if (dt == LG_BF16)
     for (int h = 0; h < H; ++h)
       if (dilation[h] > LG_MAX_BF16_DILATION) return LG_ERR_UNSUPPORTED;
+  return LG_OK;
+}
+
+lg_status validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right, const int32_t* dilation,
+                       int causal, const int32_t* global_idx, int n_global, const void* workspace,
+                       size_t workspace_bytes, bool per_call_head_limit) {
+  const lg_status st = validate_fwd_args(q, k, v, out, lse, dt, B, H, N, D, w_left, w_right, dilation, causal,
+                                         global_idx, n_global, per_call_head_limit);
+  if (st != LG_OK) return st;
   const size_t need = lg_attn_fwd_workspace_size(B, H, N, D, n_global, dt);
   if (need == 0) return LG_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return LG_ERR_WORKSPACE;
@@ -529,6 +539,7 @@ lg_status lg_query_status(const void* workspace, lg_stream_t stream_) {
   int word = 0;
   if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LG_ERR_CUDA;
   if (word != 0 && cudaMemset(const_cast<void*>(workspace), 0, sizeof(int)) != cudaSuccess) return LG_ERR_CUDA;
+  if (word & ST_INTERNAL) return LG_ERR_CUDA;
   if (word & ST_TIMEOUT) return LG_ERR_TIMEOUT;
   if (word & ST_GLOBAL_IDX) return LG_ERR_GLOBAL_IDX;
   return LG_OK;

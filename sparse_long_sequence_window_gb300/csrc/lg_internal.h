@@ -18,6 +18,7 @@ namespace lg {
 enum : int {
   ST_GLOBAL_IDX = 1 << 0,
   ST_TIMEOUT = 1 << 1,
+  ST_INTERNAL = 1 << 2,   // an internal invariant failed on the device; the work was abandoned
 };
 
 constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace
@@ -67,6 +68,24 @@ struct SimtParams {
   int BH, H, N, D;
   int wl, wr;                                        // wr already 0 when causal
   int n_glob;                                        // Longformer: g; ETC: G
+  int etc;
+  float scale;
+  int dil[LG_MAX_HEADS];
+};
+
+// fp32 backward on the CUDA cores: one warp per query row; dQ written, dK and
+// dV accumulated with atomic adds into zeroed outputs.
+struct SimtBwdParams {
+  const float* q; const float* k; const float* v; const float* out; const float* lse; const float* dout;
+  const float* qg; const float* kg; const float* vg; const float* out_g; const float* lse_g; const float* dout_g;
+  float* dq; float* dk; float* dv;                   // [BH, N, D]
+  float* dq_g; float* dk_g; float* dv_g;             // ETC only: [BH, G, D]
+  float* delta;                                      // workspace: [BH, N] (+ [BH, G] for ETC)
+  const int* gidx;
+  int* status;
+  int BH, H, N, D;
+  int wl, wr;
+  int n_glob;
   int etc;
   float scale;
   int dil[LG_MAX_HEADS];
@@ -129,19 +148,95 @@ struct PrepParams {
   int* status;
 };
 
+// ---------------------------------------------------------------- bf16 backward (tensor cores)
+
+// One launch of a backward tensor-core kernel covers the heads of one
+// dilation (all batches).  The two kernels share this block:
+//  * the q kernel: rows of TMEM are queries; band units are 128-step query
+//    tiles of one residue class against their band key tiles and the
+//    global-key tiles (dQ written); global-row units are a tile of global
+//    queries against one split of all key tiles (partial dQ in `part_a`).
+//  * the kv kernel: rows of TMEM are keys; band units are 128-step key tiles
+//    of one residue class against the query tiles whose windows reach them
+//    and the global-query tiles (dK, dV written); global-key units are a tile
+//    of global keys against one split of all query tiles (partial dK in
+//    `part_a`, dV in `part_b`).
+// "Global" is the Longformer global set (rows gathered by the prep kernel)
+// or, for ETC, the separate global input.  Class-major vectors: lse2 / delta
+// of (b, h) position c + d*t at [bh * CM + c * M + t].
+struct BwdParams {
+  CUtensorMap mQ, mK, mV, mdO;      // main input {D, N, BH}, rows strided by d
+  CUtensorMap mQG, mKG, mVG, mdOG;  // global side {D, g, BH}
+  CUtensorMap sA, sB;               // store maps of the main outputs, rows strided by d (q: dQ; kv: dK, dV)
+  const float* lse2;                // LSE * log2(e), class-major [BH][CM]
+  const float* delta;               // rowsum(dO * O), class-major [BH][CM]
+  const float* lse2g;               // [BH][gpad] of the global rows
+  const float* deltag;              // [BH][gpad]
+  const int* gidx;                  // Longformer global positions (device); NULL for ETC
+  const int* gcount;                // Longformer: gcount[x] = number of global positions < x
+  float* part_a;                    // grow-unit partials [BH * g][n_splits][D] (q: dQ; kv: dK)
+  float* part_b;                    // kv: dV partials
+  int* status;
+  long long wait_cap;
+  float scale, scale_log2;          // s and s * log2(e)
+  int B, H, N, D, wl, wr, d, n_glob, etc, CM, M, gpad;
+  int n_heads;                      // heads of this launch
+  int heads[LG_MAX_HEADS];
+  int tiles_per_head;               // class-major 128-step tiles of one (b, h)
+  int n_gt;                         // tiles of the global side
+  int n_splits, split;              // grow units: splits of the other side's tiles, tiles per split
+  int ns_stride;                    // partial slots per row in part_a / part_b (>= n_splits; unused slots stay 0)
+  int other_tiles;                  // tiles of the other side for grow units
+  int n_grow, n_band;               // units of this launch (grow units first)
+};
+
+struct BwdPrepParams {
+  const __nv_bfloat16* out; const __nv_bfloat16* dout; const float* lse;  // main [BH, N, D], [BH, N]
+  const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;  // Longformer: gathered at gidx
+  const int* gidx;                  // NULL: no gather (ETC or no globals)
+  int dil[LG_MAX_HEADS];            // per head dilation
+  __nv_bfloat16* qg; __nv_bfloat16* kg; __nv_bfloat16* vg; __nv_bfloat16* dog;  // [BH, g, D]
+  float* lse2; float* delta;        // class-major [BH][CM]
+  float* lse2g; float* deltag;      // [BH][gpad] (Longformer: gathered rows; ETC: from the global-side inputs)
+  const __nv_bfloat16* out_g; const __nv_bfloat16* dout_g; const float* lse_g;  // ETC global side
+  int* gcount;                      // [N + 1] or NULL
+  int* status;
+  int BH, H, N, D, n_glob, CM, gpad, etc;
+};
+
+struct BwdReduceParams {
+  const float* part_a; const float* part_b;  // [BH * g][n_splits][D]
+  void* out_a; void* out_b;                  // bf16 [BH, n_rows_out, D] (b may be NULL)
+  const int* gidx;                           // scatter rows (Longformer) or NULL (row r -> r)
+  int BH, n_glob, n_rows_out, D, n_splits;
+  float scale_a, scale_b;
+};
+
 // Host-side launchers (each defined next to its kernel).
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_simt_bwd(const SimtBwdParams& p, cudaStream_t s);
 // The unit-table kernel and the tensor-core kernel; the table kernel is
 // chained to the stream's previous kernel when chain_table (not when that
 // kernel may still read the unit table), the tensor-core kernel always is.
 cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table);
 cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t s);
+cudaError_t launch_bwd_q(const BwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_kv(const BwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_reduce(const BwdReduceParams& p, cudaStream_t s);
+__host__ __device__ int bwd_class_stride(int N, int d);   // M: class stride of the class-major vectors
+int bwd_cm(int N);                     // CM: per-(b, h) length of the class-major vectors
 size_t tc_smem_bytes(int D);
 // Cap of the bounded work waits (clock64 cycles) and the timeout-test switch,
 // as set by lg_debug_timeout_test (default: about one second, no withholding).
 long long wait_cap_cycles();
 int withhold_for_test();
+// Every argument check of lg_attn_fwd but the workspace (sizes, values, pointers).
+lg_status validate_fwd_args(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                            lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right,
+                            const int32_t* dilation, int causal, const int32_t* global_idx, int n_global,
+                            bool per_call_head_limit);
 // Every argument check of lg_attn_fwd (sizes, values, pointers, workspace),
 // without any CUDA call.  per_call_head_limit: also refuse H > LG_MAX_HEADS
 // (one kernel call); the host-memory entry point splits larger problems.

@@ -10,7 +10,9 @@ Recipe: Q, K, V are iid N(0, 1) float32 drawn from
 v_g [B, H, G, D]).  bf16 workloads are rounded to bfloat16 with
 round-to-nearest-even before either side sees them, so a comparison measures
 kernel error only.  Random global positions are distinct, drawn with
-``default_rng(seed + 1000)`` and sorted ascending.
+``default_rng(seed + 1000)`` and sorted ascending.  The upstream gradient dO
+of the backward pass (and dO_g of the ETC global outputs) is iid N(0, 1)
+from ``default_rng(seed + 7919)``, rounded like the inputs.
 
 The presets mirror the pages' workloads: a Longformer-base QA shape
 (CLS + question span global), an ETC-base shape (local radius 84, a few
@@ -117,3 +119,14 @@ def make_inputs(w: Workload) -> dict:
 def as_f64(t: torch.Tensor) -> np.ndarray:
     """The exact values of an input tensor as float64 (bf16 and f32 upcast exactly)."""
     return t.to(torch.float64).numpy()
+
+
+def make_grad_out(w: Workload) -> dict:
+    """The upstream gradient of the outputs for the backward pass: dout
+    [B, H, N, D] (and dout_g [B, H, G, D] for ETC), iid N(0, 1) from
+    default_rng(seed + 7919), in the workload's dtype."""
+    rng = np.random.default_rng(w.seed + 7919)
+    out = {"dout": _round(rng.standard_normal((w.B, w.H, w.N, w.D), dtype=np.float32), w.dtype)}
+    if w.is_etc:
+        out["dout_g"] = _round(rng.standard_normal((w.B, w.H, w.etc_G, w.D), dtype=np.float32), w.dtype)
+    return out
