@@ -419,6 +419,88 @@ def attn_bwd(q, k, v, dout, w_left, w_right, dilation, causal, global_idx, scale
     return dq, dk, dv
 
 
+def allowed_col(j: int, N: int, w_left: int, w_right: int, dilation: int, causal: bool, gflags: np.ndarray) -> np.ndarray:
+    """Boolean [N]: the rows i with allowed(i, j), column j of ``allowed_mask``.
+
+    Same predicate as ``allowed_row``, read down a column: key j is in row i's
+    band when j - i = d*t with -w_left <= t <= w_right (0 if causal); a global
+    row allows every key, and a global key is allowed by every row.
+    """
+    i = np.arange(N, dtype=np.int64)
+    diff = j - i
+    right = 0 if causal else w_right
+    inband = ((diff % dilation) == 0) & (diff // dilation >= -w_left) & (diff // dilation <= right)
+    if gflags[j]:
+        return np.ones(N, dtype=bool)
+    return inband | gflags
+
+
+def _row_stats(q, k, v, dout, i, keys, s):
+    """Row i over its allowed keys: P_i (over `keys`), Delta_i = <dO_i, O_i>."""
+    qi = np.asarray(q[i], np.float64)[None, :]
+    kk = np.asarray(k[keys], np.float64)
+    vv = np.asarray(v[keys], np.float64)
+    o, _, p = masked_attention(qi, kk, vv, np.ones((1, keys.size), dtype=bool), s)
+    return p[0], float(np.dot(np.asarray(dout[i], np.float64), o[0]))
+
+
+def attn_bwd_rows(q, k, v, dout, w_left, w_right, dilation, causal, global_idx, rows, scale=None):
+    """dQ of the listed query rows, [B, H, len(rows), D]: the backward of ``attn_fwd_rows``.
+
+    dQ_i needs row i alone: its allowed keys, P_i over them, Delta_i =
+    <dO_i, O_i>, dS_ij = P_ij (<dO_i, v_j> - Delta_i), dQ_i = s sum_j dS_ij k_j
+    (the chain rule of ``masked_attention_bwd`` restricted to one row).
+    """
+    B, H, N, D = q.shape
+    s = default_scale(D, scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    gflags = global_flags(N, global_idx)
+    out = np.empty((B, H, rows.size, D), dtype=np.float64)
+    for h in range(H):
+        d = int(dilation[h])
+        for r, i in enumerate(rows):
+            keys = np.nonzero(allowed_row(int(i), N, w_left, w_right, d, bool(causal), gflags))[0]
+            for b in range(B):
+                p, delta = _row_stats(q[b, h], k[b, h], v[b, h], dout[b, h], int(i), keys, s)
+                dp = np.asarray(v[b, h, keys], np.float64) @ np.asarray(dout[b, h, i], np.float64)
+                ds = p * (dp - delta)
+                out[b, h, r] = s * (ds @ np.asarray(k[b, h, keys], np.float64))
+    return out
+
+
+def attn_bwd_cols(q, k, v, dout, w_left, w_right, dilation, causal, global_idx, cols, scale=None, heads=None):
+    """dK and dV of the listed keys, [B, H, len(cols), D] each (heads not in `heads` left 0).
+
+    Key j collects from every row i that allows it (``allowed_col``):
+    dV_j = sum_i P_ij dO_i and dK_j = s sum_i dS_ij q_i, where P_i and Delta_i
+    come from row i's own allowed keys.  Rows are evaluated once per (b, h).
+    """
+    B, H, N, D = q.shape
+    s = default_scale(D, scale)
+    cols = np.asarray(cols, dtype=np.int64)
+    gflags = global_flags(N, global_idx)
+    dk = np.zeros((B, H, cols.size, D), dtype=np.float64)
+    dv = np.zeros((B, H, cols.size, D), dtype=np.float64)
+    for h in (range(H) if heads is None else heads):
+        d = int(dilation[h])
+        for b in range(B):
+            cache = {}
+            for c, j in enumerate(cols):
+                rows = np.nonzero(allowed_col(int(j), N, w_left, w_right, d, bool(causal), gflags))[0]
+                for i in rows:
+                    i = int(i)
+                    if i not in cache:
+                        keys = np.nonzero(allowed_row(i, N, w_left, w_right, d, bool(causal), gflags))[0]
+                        p, delta = _row_stats(q[b, h], k[b, h], v[b, h], dout[b, h], i, keys, s)
+                        cache[i] = (keys, p, delta)
+                    keys, p, delta = cache[i]
+                    pij = p[np.searchsorted(keys, j)]
+                    dij = pij * (float(np.dot(np.asarray(dout[b, h, i], np.float64), np.asarray(v[b, h, j], np.float64))) - delta)
+                    dv[b, h, c] += pij * np.asarray(dout[b, h, i], np.float64)
+                    dk[b, h, c] += s * dij * np.asarray(q[b, h, i], np.float64)
+    return dk, dv
+
+
 def etc_attn_bwd(q_l, k_l, v_l, q_g, k_g, v_g, radius, dout_l, dout_g, scale=None):
     """Dense-mask backward of ``etc_attn_fwd``: gradients of the long and global inputs.
 

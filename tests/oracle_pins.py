@@ -343,10 +343,27 @@ def pin_etc_bwd_finite_differences(O, seed=18):
         assert np.abs(num - g).max() < 1e-6 * (1 + np.abs(g).max())
 
 
+def pin_bwd_rows_cols_vs_dense(O, seed=19):
+    """The sampled-row dQ and sampled-key dK, dV equal the dense backward (dilation, causal, globals)."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 3, 41, 5
+    q, k, v, dout = (_rand(rng, B, H, N, D) for _ in range(4))
+    g = [0, 17, 40]
+    for causal in (False, True):
+        args = (4, 3, [1, 2, 5], causal, g)
+        dq, dk, dv = O.attn_bwd(q, k, v, dout, *args)
+        rows = [0, 1, 9, 17, 33, 40]
+        assert np.abs(O.attn_bwd_rows(q, k, v, dout, *args, rows) - dq[:, :, rows]).max() < 1e-12
+        cols = [0, 2, 17, 25, 39, 40]
+        ck, cv = O.attn_bwd_cols(q, k, v, dout, *args, cols)
+        assert np.abs(ck - dk[:, :, cols]).max() < 1e-12 and np.abs(cv - dv[:, :, cols]).max() < 1e-12
+
+
 ALL_PINS = [
     pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
     pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
     pin_identity_window, pin_dilation_residues, pin_key_shift, pin_constant_values,
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
     pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
+    pin_bwd_rows_cols_vs_dense,
 ]

@@ -133,3 +133,96 @@ def test_bwd_longformer_base_full(cuda_lib):
     """bf16 B1 H12 N4096 D64, window 256/256, globals 0..64: every element of dq, dk, dv."""
     w = workloads.PRESETS["longformer_base"]
     check(w, run_bwd(cuda_lib, w))
+
+
+# ---------------------------------------------------------------- the reference workloads at full size
+
+def _fwd_bwd(lg, w):
+    inp = workloads.make_inputs(w)
+    gr = workloads.make_grad_out(w)
+    dev = torch.device("cuda")
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    dout = gr["dout"].to(dev)
+    g = inp["global_idx"]
+    gd = torch.from_numpy(g).to(dev) if g.size else None
+    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd)
+    dq, dk, dv = lg.attn_bwd(q, k, v, out, lse, dout, w.w_left, w.w_right, w.dilations(), w.causal, gd)
+    torch.cuda.synchronize()
+    assert lg.query_status(lg.attn_bwd.last_workspace) == 0
+    return inp, gr, (dq.cpu(), dk.cpu(), dv.cpu())
+
+
+def _sum_identities(name, dk, dv, dout):
+    """Exact at any size: shifting every key leaves O unchanged (sum_j dK_j = 0)
+    and every row of P sums to 1 (sum_j dV_j = sum_i dO_i), per (b, h)."""
+    dk = dk.double().numpy(); dv = dv.double().numpy(); do = dout.double().numpy()
+    ek = np.abs(dk.sum(axis=2)).max() / np.abs(dk).sum(axis=2).max()
+    ev = np.abs(dv.sum(axis=2) - do.sum(axis=2)).max() / np.abs(dv).sum(axis=2).max()
+    print(f"{name}: sum identities: dK {ek:.2e}, dV {ev:.2e}")
+    assert ek < 5e-3 and ev < 5e-3
+
+
+def _check_sampled(w, got, ref, what):
+    tmax, tmean = BWD_TOL[w.dtype]
+    g = got.double().numpy()
+    err = np.abs(g - ref)
+    emax, emean = err.max() / np.abs(ref).max(), err.mean() / np.abs(ref).mean()
+    print(f"{w.name} {what}: max {emax:.2e} mean {emean:.2e}")
+    assert emax <= tmax and emean <= tmean
+
+
+def test_bwd_charlm_full_sampled(cuda_lib):
+    """bf16 B1 H8 N16384 D64 causal wl 512, dilation [1,1,2,2,3,3,4,4]: sampled dQ rows and dK, dV keys."""
+    w = workloads.PRESETS["charlm_dilated"]
+    inp, gr, (dq, dk, dv) = _fwd_bwd(cuda_lib, w)
+    qn, kn, vn, don = (pu.to_np32(x) for x in (inp["q"], inp["k"], inp["v"], gr["dout"]))
+    rows = pu.sample_rows(w.N, dilations=(1, 2, 3, 4), n_random=24, seed=41)
+    _check_sampled(w, dq[:, :, rows], lg_oracle.attn_bwd_rows(qn, kn, vn, don, w.w_left, w.w_right, w.dilations(),
+                                                               w.causal, [], rows), "dq rows")
+    cols = pu.sample_rows(w.N, dilations=(1, 2, 3, 4), n_random=8, seed=42)[::3]
+    rk, rv = lg_oracle.attn_bwd_cols(qn, kn, vn, don, w.w_left, w.w_right, w.dilations(), w.causal, [], cols)
+    _check_sampled(w, dk[:, :, cols], rk, "dk keys")
+    _check_sampled(w, dv[:, :, cols], rv, "dv keys")
+    _sum_identities(w.name, dk, dv, gr["dout"])
+
+
+def test_bwd_long_scale_full_sampled(cuda_lib):
+    """bf16 B1 H16 N131072 D128, window 512/512, 128 random globals (the benchmarked launch):
+    sampled dQ rows (band and global) on every head, sampled band keys' dK, dV on two heads,
+    and the sum identities (which take in every global key) on every head."""
+    w = workloads.PRESETS["long_128k"]
+    inp, gr, (dq, dk, dv) = _fwd_bwd(cuda_lib, w)
+    g = workloads.global_positions(w)
+    qn, kn, vn, don = (pu.to_np32(x) for x in (inp["q"], inp["k"], inp["v"], gr["dout"]))
+    rows = pu.sample_rows(w.N, globals_=g.tolist()[:4], n_random=12, seed=43)
+    _check_sampled(w, dq[:, :, rows], lg_oracle.attn_bwd_rows(qn, kn, vn, don, w.w_left, w.w_right, w.dilations(),
+                                                               w.causal, g, rows), "dq rows")
+    gset = set(g.tolist())
+    cols = [c for c in (0, 127, 128, 4095, 65536, w.N - 1) if c not in gset]
+    heads = [0, w.H - 1]
+    rk, rv = lg_oracle.attn_bwd_cols(qn, kn, vn, don, w.w_left, w.w_right, w.dilations(), w.causal, g, cols,
+                                     heads=heads)
+    _check_sampled(w, dk[:, heads][:, :, cols], rk[:, heads], "dk keys")
+    _check_sampled(w, dv[:, heads][:, :, cols], rv[:, heads], "dv keys")
+    _sum_identities(w.name, dk, dv, gr["dout"])
+
+
+def test_bwd_etc_base_two_slices(cuda_lib):
+    """bf16 ETC B2 H12 L4096 G256 D64 r84: every gradient element of two (b, h) slices against the dense oracle."""
+    lg = cuda_lib
+    w = workloads.PRESETS["etc_base"]
+    inp = workloads.make_inputs(w)
+    gr = workloads.make_grad_out(w)
+    dev = torch.device("cuda")
+    t = [inp[n].to(dev) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
+    out_l, out_g, lse_l, lse_g = lg.etc_attn_fwd(*t, w.radius)
+    grads = lg.etc_attn_bwd(*t, out_l, out_g, lse_l, lse_g, gr["dout"].to(dev), gr["dout_g"].to(dev), w.radius)
+    torch.cuda.synchronize()
+    assert lg.query_status(lg.etc_attn_bwd.last_workspace) == 0
+    names = ("dq_l", "dk_l", "dv_l", "dq_g", "dk_g", "dv_g")
+    for b, h in ((0, 0), (1, 11)):
+        sl = lambda x: pu.to_np32(x)[b:b + 1, h:h + 1]
+        ref = lg_oracle.etc_attn_bwd(*(sl(inp[n]) for n in ("q", "k", "v", "q_g", "k_g", "v_g")), w.radius,
+                                     sl(gr["dout"]), sl(gr["dout_g"]))
+        for n, x, r in zip(names, grads, ref):
+            _check_sampled(w, x.cpu()[b:b + 1, h:h + 1], r, f"{n} (b={b}, h={h})")
