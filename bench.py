@@ -334,8 +334,13 @@ def run_native(args, rank, world):
     else:
         roofline = None
 
+    backward = None
+    if not args.no_bwd:
+        backward = bench_backward(lg, torch, w, t, outs, flush, args.bwd_steps, peaks, peak_kind)
+
     per_config = None
     if rank == 0 and world == 1 and not args.no_sweep:
+        sweep.no_bwd = args.no_bwd
         per_config = sweep(lg, torch, dev)
 
     line = {
@@ -352,6 +357,7 @@ def run_native(args, rank, world):
         "e2e": e2e,
         "gpu_launches": launches_per_call(w) * args.steps,
         "roofline": roofline,
+        "backward": backward,
         "clocks": clk,
         "step_ms_median": round(statistics.median(step_ms), 5),
     }
@@ -363,6 +369,60 @@ def run_native(args, rank, world):
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def bench_backward(lg, torch, w, t, outs, flush, steps, peaks, peak_kind):
+    """The backward pass of the same workload (lg_attn_bwd / lg_etc_attn_bwd) after one forward.
+
+    Useful FLOPs: 8 * D per allowed pair (the contractions dP = dO V^T, dV =
+    P^T dO, dK = dS^T Q, dQ = dS K; the recomputed S = Q K^T is not counted).
+    The time is the whole library call (prep, tensor-core kernels, reduce),
+    CUDA events on the current stream, L2 flushed between steps when the
+    inputs fit in it.
+    """
+    if w.dtype != "bf16":
+        return None
+    gen = torch.Generator(device=t["q"].device)
+    gen.manual_seed(w.seed + 7919)
+    dout = torch.randn(t["q"].shape, generator=gen, device=t["q"].device, dtype=torch.float32).to(torch.bfloat16)
+    pairs = useful_pairs(lg, w)
+    flops = 8.0 * w.D * pairs
+    if w.is_etc:
+        out_l, out_g, lse_l, lse_g = outs
+        dout_g = torch.randn(t["q_g"].shape, generator=gen, device=t["q"].device, dtype=torch.float32).to(torch.bfloat16)
+        ws = torch.empty(lg.etc_attn_bwd_workspace_size(w.B, w.H, w.N, w.etc_G, w.D, 1), dtype=torch.uint8,
+                         device=t["q"].device)
+
+        def f():
+            lg.etc_attn_bwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], out_l, out_g, lse_l, lse_g,
+                            dout, dout_g, w.radius, workspace=ws)
+    else:
+        out, lse = outs
+        ng = 0 if t["g"] is None else t["g"].numel()
+        ws = torch.empty(lg.attn_bwd_workspace_size(w.B, w.H, w.N, w.D, ng, 1), dtype=torch.uint8,
+                         device=t["q"].device)
+        grads = [torch.empty_like(t["q"]) for _ in range(3)]
+
+        def f():
+            lg.attn_bwd(t["q"], t["k"], t["v"], out, lse, dout, w.w_left, w.w_right, w.dilations(), w.causal,
+                        t["g"], dq=grads[0], dk=grads[1], dv=grads[2], workspace=ws)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    st = lg.query_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after the backward warm-up: {lg.status_string(st)}")
+    ms = time_steps(torch, f, steps, flush)
+    med = statistics.median(ms)
+    achieved = flops / (med / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) if peaks else FALLBACK_BF16_TFLOPS
+    res = {"metric": "sparse attn bwd TFLOP/s (8*D per allowed pair)", "value": round(achieved, 2),
+           "unit": "TFLOP/s", "ms_per_call": round(med, 4), "steps": steps,
+           "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops of {peak_kind}",
+                        "kernel": "whole backward call (bwd_kv_kernel + bwd_q_kernel dominate)"}}
+    del ws, dout
+    return res
 
 
 def sweep(lg, torch, dev):
@@ -382,6 +442,10 @@ def sweep(lg, torch, dev):
         med = statistics.median(ms)
         res[name] = {"tflops": round(flops / (med / 1e3) / 1e12, 2), "ms": round(med, 5),
                      "status": lg.status_string(st)}
+        if w.dtype == "bf16" and not getattr(sweep, "no_bwd", False):
+            b = bench_backward(lg, torch, w, t, outs, in_bytes < 2 * L2_BYTES, 10 if w.N >= 100000 else 30, {}, "")
+            res[name]["bwd_tflops"] = b["value"]
+            res[name]["bwd_ms"] = b["ms_per_call"]
         del t, f, outs, ws
         torch.cuda.empty_cache()
     return res
@@ -571,6 +635,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--bwd-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
