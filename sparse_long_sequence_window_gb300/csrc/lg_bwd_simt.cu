@@ -133,9 +133,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_kernel(const SimtBwdPara
       const float* kr = key >= 0 ? p.k + base_l + static_cast<size_t>(key) * D : p.kg + base_g + static_cast<size_t>(-2 - key) * D;
       const float* vr = key >= 0 ? p.v + base_l + static_cast<size_t>(key) * D : p.vg + base_g + static_cast<size_t>(-2 - key) * D;
       float s = 0.f, dp = 0.f;
+#pragma unroll 8
       for (int x = 0; x < D; x += 4) {
-        const float4 kv = *reinterpret_cast<const float4*>(kr + x);
-        const float4 vv = *reinterpret_cast<const float4*>(vr + x);
+        const float4 kv = __ldg(reinterpret_cast<const float4*>(kr + x));
+        const float4 vv = __ldg(reinterpret_cast<const float4*>(vr + x));
         s = fmaf(sq[wib][x], kv.x, s); s = fmaf(sq[wib][x + 1], kv.y, s);
         s = fmaf(sq[wib][x + 2], kv.z, s); s = fmaf(sq[wib][x + 3], kv.w, s);
         dp = fmaf(sg[wib][x], vv.x, dp); dp = fmaf(sg[wib][x + 1], vv.y, dp);

@@ -1,16 +1,26 @@
 // fp32 window + dilation + global attention forward on the CUDA cores.
 //
-// This is the exact-precision path (fp32 inputs, fp32 FMA, no TF32).  One
-// warp owns one query row.  The row's candidate keys are enumerated in
-// chunks of 32, one key per lane: band steps t (keys i + d*t inside [0, N)),
-// then the global keys that are not already in the band ("Longformer: The
-// Long-Document Transformer", section 3.4, "Sliding Window Attention",
-// "Dilated Sliding Window Attention", "Global Attention").  A global query
-// row enumerates every key.  For the ETC call ("ETC: Encoding Long and
-// Structured Inputs in Transformers", section 3.4, "Global-Local Attention")
-// a long row enumerates its |i - j| <= r long keys and the G global keys; a
-// global row enumerates all G + L keys.  Each chunk updates an online softmax
-// (running max m and sum l) merged across the lanes with warp shuffles.
+// This is the exact-precision path (fp32 inputs, fp32 FMA, no TF32).  A
+// row's candidate keys are enumerated in chunks of 32, one key per lane:
+// band steps t (keys i + d*t inside [0, N)), then the global keys that are
+// not already in the band ("Longformer: The Long-Document Transformer",
+// section 3.4, "Sliding Window Attention", "Dilated Sliding Window
+// Attention", "Global Attention").  A global query row takes every key.  For
+// the ETC call ("ETC: Encoding Long and Structured Inputs in Transformers",
+// section 3.4, "Global-Local Attention") a long row takes its |i - j| <= r
+// long keys and the G global keys; a global row takes all G + L keys.  Each
+// chunk updates an online softmax (running max m and sum l) merged across
+// the lanes with warp shuffles.
+//
+// Work split: a band row is one warp (eight rows per block).  A global row,
+// which takes every key, is one block of eight warps: warp w takes the w-th
+// eighth of the key list, and the block combines the eight partial
+// (m, l, O) by their softmax denominators ("LONGNET: Scaling Transformers to
+// 1,000,000,000 Tokens", section 3.4, "Mixture of Dilated Attentions": one
+// joint softmax over the union of the parts).  In the P V step the 32 keys
+// of a chunk are taken without branches (a missing key has weight 0 and
+// points at a valid row), so the value loads of consecutive keys are
+// independent and issue together.
 #include <math.h>
 
 #include "lg_internal.h"
@@ -49,60 +59,38 @@ __device__ __forceinline__ bool in_band(int i, int j, int d, int wl, int wr) {
   return t >= -wl && t <= wr;
 }
 
+// One query row (or, for a global row, one slice of its key list) in one warp.
+struct RowPart {
+  float m, l;     // running max and sum (natural-log units of the scaled logits)
+  float o[4];     // unnormalised output, columns lane + 32 r
+};
+
+// Runs the online softmax of row (bh, i) over candidates [c_lo, c_hi) of its
+// key list.  qs: the row's query in shared memory.
 template <bool ETC>
-__global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams p) {
-  __shared__ float sq[kWarps][128];
-  const int wib = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const long long row_id = static_cast<long long>(blockIdx.x) * kWarps + wib;
+__device__ RowPart row_part(const SimtParams& p, int bh, int i, bool grow_row, int d, long long c_lo, long long c_hi,
+                            const float* qs, int lane) {
   const int N = p.N, D = p.D;
-  const long long n_rows_long = static_cast<long long>(p.BH) * N;
-  const long long n_rows = ETC ? n_rows_long + static_cast<long long>(p.BH) * p.n_glob : n_rows_long;
-  if (row_id >= n_rows) return;
-
-  // ---- which row, and its candidate list
-  bool grow_row;  // query attends to every key
-  int bh, i;
-  if (ETC && row_id >= n_rows_long) {
-    const long long g = row_id - n_rows_long;
-    bh = static_cast<int>(g / p.n_glob);
-    i = static_cast<int>(g % p.n_glob);
-    grow_row = true;
-  } else {
-    bh = static_cast<int>(row_id / N);
-    i = static_cast<int>(row_id % N);
-    grow_row = !ETC && p.n_glob > 0 && is_global_pos(p.gidx, p.n_glob, i);
-  }
-  const int h = bh % p.H;
-  const int d = ETC ? 1 : p.dil[h];
-  const float* qrow = (ETC && grow_row) ? p.qg + (static_cast<size_t>(bh) * p.n_glob + i) * D
-                                        : p.q + (static_cast<size_t>(bh) * N + i) * D;
-  for (int x = lane; x < D; x += 32) sq[wib][x] = qrow[x];
-  __syncwarp();
-
-  // band step range of a band row
   int t_lo = 0, n_band = 0;
   if (!grow_row) {
     t_lo = max(-p.wl, -(i / d));
     const int t_hi = min(p.wr, (N - 1 - i) / d);
     n_band = max(0, t_hi - t_lo + 1);
   }
-  long long n_cand;
-  if (grow_row) n_cand = ETC ? static_cast<long long>(p.n_glob) + N : N;
-  else n_cand = static_cast<long long>(n_band) + p.n_glob;
-
   const float* kl = p.k + static_cast<size_t>(bh) * N * D;
   const float* vl = p.v + static_cast<size_t>(bh) * N * D;
   const float* kgl = ETC ? p.kg + static_cast<size_t>(bh) * p.n_glob * D : nullptr;
   const float* vgl = ETC ? p.vg + static_cast<size_t>(bh) * p.n_glob * D : nullptr;
-
-  float m = -INFINITY, l = 0.f;
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  for (long long base = 0; base < n_cand; base += 32) {
+  RowPart rp;
+  rp.m = -INFINITY;
+  rp.l = 0.f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) rp.o[r] = 0.f;
+  for (long long base = c_lo; base < c_hi; base += 32) {
     const long long c = base + lane;
     // key row of this lane: >= 0 long/main row, < -1 global-input row (-2 - r), -1 none
     int key = -1;
-    if (c < n_cand) {
+    if (c < c_hi) {
       if (grow_row) {
         if (ETC) key = (c < p.n_glob) ? -2 - static_cast<int>(c) : static_cast<int>(c - p.n_glob);
         else key = static_cast<int>(c);
@@ -122,41 +110,51 @@ __global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams
     if (key != -1) {
       const float* kr = key >= 0 ? kl + static_cast<size_t>(key) * D : kgl + static_cast<size_t>(-2 - key) * D;
       float acc = 0.f;
+      // unrolled so that the row's loads issue together rather than one per step
+#pragma unroll 8
       for (int x = 0; x < D; x += 4) {
-        const float4 kv = *reinterpret_cast<const float4*>(kr + x);
-        acc = fmaf(sq[wib][x], kv.x, acc);
-        acc = fmaf(sq[wib][x + 1], kv.y, acc);
-        acc = fmaf(sq[wib][x + 2], kv.z, acc);
-        acc = fmaf(sq[wib][x + 3], kv.w, acc);
+        const float4 kv = __ldg(reinterpret_cast<const float4*>(kr + x));
+        acc = fmaf(qs[x], kv.x, acc);
+        acc = fmaf(qs[x + 1], kv.y, acc);
+        acc = fmaf(qs[x + 2], kv.z, acc);
+        acc = fmaf(qs[x + 3], kv.w, acc);
       }
       s = acc * p.scale;
     }
     const float cmax = warp_max(s);
-    const float m_new = fmaxf(m, cmax);
+    const float m_new = fmaxf(rp.m, cmax);
     if (m_new == -INFINITY) continue;
-    const float corr = expf(m - m_new);
+    const float corr = expf(rp.m - m_new);
     const float pj = (key != -1) ? expf(s - m_new) : 0.f;
-    l = l * corr + warp_sum(pj);
+    rp.l = rp.l * corr + warp_sum(pj);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) o[r] *= corr;
+    for (int r = 0; r < 4; ++r) rp.o[r] *= corr;
+    // P V without branches: a missing key has weight 0 and reads row 0.
+    const float* vsafe = key >= 0 ? vl + static_cast<size_t>(key) * D
+                                  : (key < -1 ? vgl + static_cast<size_t>(-2 - key) * D : vl);
+#pragma unroll 8
     for (int src = 0; src < 32; ++src) {
       const float pb = __shfl_sync(0xffffffffu, pj, src);
-      const int kb = __shfl_sync(0xffffffffu, key, src);
-      if (pb == 0.f) continue;
-      const float* vr = kb >= 0 ? vl + static_cast<size_t>(kb) * D : vgl + static_cast<size_t>(-2 - kb) * D;
+      const float* vr = reinterpret_cast<const float*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(vsafe), src));
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int x = lane + 32 * r;
-        if (x < D) o[r] = fmaf(pb, vr[x], o[r]);
+        if (x < D) rp.o[r] = fmaf(pb, __ldg(vr + x), rp.o[r]);
       }
     }
-    m = m_new;
+    rp.m = m_new;
   }
+  return rp;
+}
 
-  const float inv_l = 1.f / l;
+template <bool ETC>
+__device__ __forceinline__ void write_row(const SimtParams& p, int bh, int i, bool gside, const RowPart& rp, int lane) {
+  const int D = p.D, N = p.N;
+  const float inv_l = 1.f / rp.l;
   float* orow;
   float* lrow;
-  if (ETC && grow_row) {
+  if (ETC && gside) {
     orow = p.out_g + (static_cast<size_t>(bh) * p.n_glob + i) * D;
     lrow = p.lse_g + static_cast<size_t>(bh) * p.n_glob + i;
   } else {
@@ -166,20 +164,102 @@ __global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int x = lane + 32 * r;
-    if (x < D) orow[x] = o[r] * inv_l;
+    if (x < D) orow[x] = rp.o[r] * inv_l;
   }
-  if (lane == 0) *lrow = m + logf(l);
+  if (lane == 0) *lrow = rp.m + logf(rp.l);
+}
+
+// Blocks [0, n_grow_blocks): one global row each, its key list split over the
+// eight warps.  The other blocks: eight band rows each, one per warp (a
+// Longformer row that is global is left to its global-row block).
+template <bool ETC>
+__global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams p, int n_grow_blocks) {
+  __shared__ float sq[kWarps][128];
+  __shared__ float pm[kWarps], pl[kWarps];
+  __shared__ float po[kWarps][128];
+  const int wib = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = p.N, D = p.D;
+
+  if (static_cast<int>(blockIdx.x) < n_grow_blocks) {
+    // ---- one global row per block
+    const int bh = blockIdx.x / p.n_glob;
+    const int gi = blockIdx.x % p.n_glob;
+    int i;
+    const float* qrow;
+    if (ETC) {
+      i = gi;
+      qrow = p.qg + (static_cast<size_t>(bh) * p.n_glob + gi) * D;
+    } else {
+      i = __ldg(p.gidx + gi);
+      if (i < 0 || i >= N) return;   // a bad list is reported by the prep kernel; nothing is written
+      qrow = p.q + (static_cast<size_t>(bh) * N + i) * D;
+    }
+    for (int x = lane; x < D; x += 32) sq[wib][x] = qrow[x];
+    __syncwarp();
+    const long long n_cand = ETC ? static_cast<long long>(p.n_glob) + N : N;
+    const long long seg = ((n_cand + kWarps - 1) / kWarps + 31) / 32 * 32;
+    const long long c_lo = wib * seg, c_hi = min(n_cand, c_lo + seg);
+    const RowPart rp = row_part<ETC>(p, bh, i, true, 1, c_lo, c_hi, sq[wib], lane);
+    if (lane == 0) {
+      pm[wib] = rp.m;
+      pl[wib] = rp.l;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int x = lane + 32 * r;
+      if (x < D) po[wib][x] = rp.o[r];
+    }
+    __syncthreads();
+    if (wib != 0) return;
+    RowPart all;
+    all.m = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) all.m = fmaxf(all.m, pm[w]);
+    all.l = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) all.o[r] = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = pm[w] == -INFINITY ? 0.f : expf(pm[w] - all.m);
+      all.l += f * pl[w];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int x = lane + 32 * r;
+        if (x < D) all.o[r] = fmaf(f, po[w][x], all.o[r]);
+      }
+    }
+    write_row<ETC>(p, bh, i, true, all, lane);
+    return;
+  }
+
+  // ---- band rows, one per warp
+  const long long row_id = static_cast<long long>(blockIdx.x - n_grow_blocks) * kWarps + wib;
+  if (row_id >= static_cast<long long>(p.BH) * N) return;
+  const int bh = static_cast<int>(row_id / N);
+  const int i = static_cast<int>(row_id % N);
+  if (!ETC && p.n_glob > 0 && is_global_pos(p.gidx, p.n_glob, i)) return;
+  const int d = ETC ? 1 : p.dil[bh % p.H];
+  const float* qrow = p.q + (static_cast<size_t>(bh) * N + i) * D;
+  for (int x = lane; x < D; x += 32) sq[wib][x] = qrow[x];
+  __syncwarp();
+  const int t_lo = max(-p.wl, -(i / d));
+  const int t_hi = min(p.wr, (N - 1 - i) / d);
+  const long long n_cand = static_cast<long long>(max(0, t_hi - t_lo + 1)) + p.n_glob;
+  const RowPart rp = row_part<ETC>(p, bh, i, false, d, 0, n_cand, sq[wib], lane);
+  write_row<ETC>(p, bh, i, false, rp, lane);
 }
 
 }  // namespace
 
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s) {
-  long long rows = static_cast<long long>(p.BH) * p.N;
-  if (p.etc) rows += static_cast<long long>(p.BH) * p.n_glob;
-  const long long blocks = (rows + kWarps - 1) / kWarps;
+  const long long band_rows = static_cast<long long>(p.BH) * p.N;
+  const long long grow_blocks = static_cast<long long>(p.BH) * p.n_glob;
+  const long long blocks = grow_blocks + (band_rows + kWarps - 1) / kWarps;
   if (blocks <= 0) return cudaSuccess;
-  if (p.etc) simt_attn_kernel<true><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(p);
-  else simt_attn_kernel<false><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(p);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (p.etc)
+    simt_attn_kernel<true><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(p, static_cast<int>(grow_blocks));
+  else
+    simt_attn_kernel<false><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(p, static_cast<int>(grow_blocks));
   return cudaGetLastError();
 }
 

@@ -906,6 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 #pragma unroll
                 for (int k = 0; k < 8; ++k) dst[8 * cc + k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
               }
+              __syncwarp();   // reconverged before the next warp-collective TMEM load
             }
             if (row_valid) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
           }
