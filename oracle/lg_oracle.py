@@ -175,6 +175,33 @@ def attn_fwd(q, k, v, w_left, w_right, dilation, causal, global_idx, scale=None)
     return out, lse
 
 
+def attn_fwd_gproj(q, k, v, q_glob, k_glob, v_glob, w_left, w_right, dilation, causal, global_idx, scale=None):
+    """Longformer attention with separate projections for global attention.
+
+    Longformer page, "Separate Linear Projections for Local vs. Global
+    Attention": local attention is softmax(Q_s K_s^T / sqrt(d_k) + mask_local)
+    V_s, global attention is softmax(Q_g K_g^T / sqrt(d_k)) V_g with no mask,
+    "applied to the designated global tokens".  Reading (the page does not say
+    which projection a local row uses for the global columns): a global row i
+    takes the global formula over every token, q_glob[i] against k_glob, with
+    v_glob; every other row takes the local formula over its allowed keys
+    (band plus global columns) with q, k, v.  With q_glob = q, k_glob = k,
+    v_glob = v this is ``attn_fwd``.  All tensors [B, H, N, D]; returns
+    O [B, H, N, D], LSE [B, H, N].
+    """
+    out, lse = attn_fwd(q, k, v, w_left, w_right, dilation, causal, global_idx, scale=scale)
+    B, H, N, D = np.asarray(q).shape
+    s = default_scale(D, scale)
+    g = sorted(set(int(x) for x in np.asarray(global_idx).reshape(-1)))
+    for b in range(B):
+        for h in range(H):
+            for i in g:
+                o, l, _ = masked_attention(np.asarray(q_glob[b, h, i], np.float64)[None, :], k_glob[b, h], v_glob[b, h],
+                                           np.ones((1, N), dtype=bool), s)
+                out[b, h, i], lse[b, h, i] = o[0], l[0]
+    return out, lse
+
+
 def attn_fwd_rows(q, k, v, w_left, w_right, dilation, causal, global_idx, rows, scale=None):
     """Sampled-row oracle.  Same definition as ``attn_fwd`` for the listed rows only.
 

@@ -359,11 +359,29 @@ def pin_bwd_rows_cols_vs_dense(O, seed=19):
         assert np.abs(ck - dk[:, :, cols]).max() < 1e-12 and np.abs(cv - dv[:, :, cols]).max() < 1e-12
 
 
+def pin_gproj(O, seed=20):
+    """Separate global projections: equal projections reduce to attn_fwd; a global row is the
+    full-attention row of (q_glob, k_glob, v_glob) (library SDPA); other rows ignore the global projections."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 2, 30, 8
+    q, k, v, qg, kg, vg = (_rand(rng, B, H, N, D) for _ in range(6))
+    args = (3, 2, [1, 2], False, [0, 11, 29])
+    o1, l1 = O.attn_fwd_gproj(q, k, v, q, k, v, *args)
+    o0, l0 = O.attn_fwd(q, k, v, *args)
+    assert np.abs(o1 - o0).max() < 1e-13 and np.abs(l1 - l0).max() < 1e-13
+    o2, l2 = O.attn_fwd_gproj(q, k, v, qg, kg, vg, *args)
+    ref = _sdpa64(qg, kg, vg, 1 / np.sqrt(D))
+    for i in (0, 11, 29):
+        assert np.abs(o2[:, :, i] - ref[:, :, i]).max() < 1e-12
+    rest = [i for i in range(N) if i not in (0, 11, 29)]
+    assert np.abs(o2[:, :, rest] - o0[:, :, rest]).max() < 1e-13 and np.abs(l2[:, :, rest] - l0[:, :, rest]).max() < 1e-13
+
+
 ALL_PINS = [
     pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
     pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
     pin_identity_window, pin_dilation_residues, pin_key_shift, pin_constant_values,
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
     pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
-    pin_bwd_rows_cols_vs_dense,
+    pin_bwd_rows_cols_vs_dense, pin_gproj,
 ]

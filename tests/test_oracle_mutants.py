@@ -143,10 +143,24 @@ def mut_bwd_dv_untransposed(O):
     _bwd_mutant(O, "dv_untransposed")
 
 
+def mut_gproj_local_keys(O):
+    # global rows scored against the local keys instead of the global projection's
+    orig = O.attn_fwd_gproj
+    O.attn_fwd_gproj = lambda q, k, v, qg, kg, vg, *a, **kw: orig(q, k, v, qg, k, vg, *a, **kw)
+
+
+def mut_bwd_cols_drop_global_rows(O):
+    # sampled-key backward that forgets the global rows attending every key
+    orig_col = O.allowed_col
+    O.allowed_col = lambda j, N, wl, wr, d, causal, g: orig_col(j, N, wl, wr, d, causal, g) & ~g | (
+        g if g[j] else False)
+
+
 MUTANTS = [mut_swap_sides, mut_ignore_dilation, mut_span_not_steps, mut_causal_keeps_right,
            mut_no_global_columns, mut_no_scale, mut_transposed_logits, mut_lse_log2,
            mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale,
-           mut_bwd_no_delta, mut_bwd_no_scale, mut_bwd_dk_untransposed, mut_bwd_dv_untransposed]
+           mut_bwd_no_delta, mut_bwd_no_scale, mut_bwd_dk_untransposed, mut_bwd_dv_untransposed,
+           mut_gproj_local_keys, mut_bwd_cols_drop_global_rows]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
