@@ -118,6 +118,30 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       void* workspace, size_t workspace_bytes, lg_stream_t stream);
 
 /*
+ * lg_attn_fwd with separate projections for global attention ("Longformer",
+ * "Separate Linear Projections for Local vs. Global Attention": Q_s, K_s,
+ * V_s for the sliding window, Q_g, K_g, V_g for global attention).
+ *
+ *  q, k, v     the local projections Q_s, K_s, V_s: [B, H, N, D] of every token.
+ *  q_glob, k_glob, v_glob  the global projections Q_g, K_g, V_g: [B, H, N, D]
+ *              of every token, same dtype and layout.
+ * A global row i is softmax(s q_glob_i . k_glob_j over every j) applied to
+ * v_glob.  Every other row attends to its band and to the global columns with
+ * the local projections (q_i . k_j, v_j), as in lg_attn_fwd.  (The page does
+ * not say which projection a local row uses for the global columns; the local
+ * one is this library's reading.)  With q_glob = q, k_glob = k, v_glob = v the
+ * result is lg_attn_fwd's.  Every other argument, the workspace size, the
+ * checks and the errors are lg_attn_fwd's; the three extra pointers must be
+ * non-NULL and 16-byte aligned.
+ */
+lg_status lg_attn_fwd_gproj(const void* q, const void* k, const void* v,
+                            const void* q_glob, const void* k_glob, const void* v_glob,
+                            void* out, float* lse, lg_dtype dt, int B, int H, int N, int D,
+                            int w_left, int w_right, const int32_t* dilation, int causal,
+                            const int32_t* global_idx, int n_global, float scale,
+                            void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/*
  * lg_attn_fwd without a caller-supplied workspace.  (Not a step of the
  * method: the paper has no counterpart; this exists for integration.)
  *

@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
     lib.lg_attn_fwd.restype = i32
     lib.lg_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32,
                                 vp, sz, vp]
+    lib.lg_attn_fwd_gproj.restype = i32
+    lib.lg_attn_fwd_gproj.argtypes = [vp] * 8 + [i32] * 7 + [vp, i32, vp, i32, f32, vp, sz, vp]
     lib.lg_attn_fwd_host.restype = i32
     lib.lg_attn_fwd_host.argtypes = [vp] * 10 + [i32] * 7 + [vp, i32, vp, i32, f32, vp, sz, i32, vp]
     lib.lg_etc_attn_fwd.restype = i32
@@ -167,12 +169,14 @@ def _nbytes(t) -> int:
 
 def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int]] = None,
              causal: bool = False, global_idx=None, scale: Optional[float] = None,
-             out=None, lse=None, workspace=None, stream=None):
+             out=None, lse=None, workspace=None, stream=None, q_global=None, k_global=None, v_global=None):
     """Longformer-style window + dilation + global attention forward.
 
     q, k, v: CUDA tensors [B, H, N, D] (float32 or bfloat16, contiguous).
     dilation: H ints (default all 1).  global_idx: sorted unique int32 CUDA
-    tensor of positions (or None).  Returns (out [B, H, N, D], lse [B, H, N]
+    tensor of positions (or None).  q_global, k_global, v_global: optional
+    separate projections for global attention (all three or none, shaped like
+    q; lg_attn_fwd_gproj).  Returns (out [B, H, N, D], lse [B, H, N]
     float32).  Asynchronous on the current stream.
     """
     import torch
@@ -197,11 +201,22 @@ def attn_fwd(q, k, v, w_left: int, w_right: int, dilation: Optional[Sequence[int
     _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
     need = attn_fwd_workspace_size(B, H, N, D, n_global, dt)
     ws = _workspace(need, q.device, workspace)
-    st = lib.lg_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), dt, B, H, N, D,
-                         int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
-                         _ptr(global_idx) if n_global else None, n_global,
-                         float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
-    _check(st, "lg_attn_fwd")
+    gp = (q_global, k_global, v_global)
+    if any(x is not None for x in gp):
+        if any(x is None for x in gp):
+            raise ValueError("q_global, k_global and v_global go together")
+        _same(q, "global projections", *gp)
+        st = lib.lg_attn_fwd_gproj(_ptr(q), _ptr(k), _ptr(v), *(_ptr(x) for x in gp), _ptr(out), _ptr(lse), dt,
+                                   B, H, N, D, int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
+                                   _ptr(global_idx) if n_global else None, n_global,
+                                   float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
+        _check(st, "lg_attn_fwd_gproj")
+    else:
+        st = lib.lg_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), dt, B, H, N, D,
+                             int(w_left), int(w_right), dil.ctypes.data, int(bool(causal)),
+                             _ptr(global_idx) if n_global else None, n_global,
+                             float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
+        _check(st, "lg_attn_fwd")
     if workspace is None:
         _keep_for(stream, ws)
     attn_fwd.last_workspace = ws

@@ -299,17 +299,20 @@ lg_status validate_fwd(const void* q, const void* k, const void* v, const void* 
 
 }  // namespace lg
 
-extern "C" {
+namespace {
 
-lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
-                      int H, int N, int D, int w_left, int w_right, const int32_t* dilation, int causal,
-                      const int32_t* global_idx, int n_global, float scale, void* workspace,
-                      size_t workspace_bytes, lg_stream_t stream_) {
+// The Longformer forward; qgl / kgl / vgl: the global rows' separate
+// projections (all three, or none: then q, k, v serve the global rows too).
+lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void* qgl, const void* kgl,
+                        const void* vgl, void* out, float* lse, lg_dtype dt, int B, int H, int N, int D, int w_left,
+                        int w_right, const int32_t* dilation, int causal, const int32_t* global_idx, int n_global,
+                        float scale, void* workspace, size_t workspace_bytes, lg_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   // ---- argument checks (nothing is launched on failure)
   lg_status st = validate_fwd(q, k, v, out, lse, dt, B, H, N, D, w_left, w_right, dilation, causal, global_idx,
                               n_global, workspace, workspace_bytes, true);
   if (st != LG_OK) return st;
+  if (qgl == nullptr) { qgl = q; kgl = k; vgl = v; }
 
   const int BH = B * H;
   const int wl = std::min(w_left, N);
@@ -328,6 +331,8 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     SimtParams sp{};
     sp.q = static_cast<const float*>(q); sp.k = static_cast<const float*>(k); sp.v = static_cast<const float*>(v);
     sp.out = static_cast<float*>(out); sp.lse = lse; sp.gidx = global_idx;
+    sp.qgl = static_cast<const float*>(qgl); sp.kgl = static_cast<const float*>(kgl);
+    sp.vgl = static_cast<const float*>(vgl);
     sp.BH = BH; sp.H = H; sp.N = N; sp.D = D; sp.wl = wl; sp.wr = wr; sp.n_glob = n_global; sp.etc = 0;
     sp.scale = s;
     for (int h = 0; h < H; ++h) sp.dil[h] = dilation[h];
@@ -355,7 +360,7 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   if (n_global > 0) {
     PrepParams pp{};
     pp.gidx = global_idx; pp.n_glob = n_global; pp.N = N; pp.status = status; pp.BH = BH; pp.D = D;
-    pp.q = static_cast<const __nv_bfloat16*>(q); pp.k = static_cast<const __nv_bfloat16*>(k);
+    pp.q = static_cast<const __nv_bfloat16*>(qgl); pp.k = static_cast<const __nv_bfloat16*>(k);
     pp.v = static_cast<const __nv_bfloat16*>(v);
     pp.qg = qg; pp.kg = kg; pp.vg = vg;
     pp.gcount = reinterpret_cast<int*>(ws + lay.cnt);
@@ -391,10 +396,12 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     }
     if (n_global > 0) {
       if (!encode_map(&tp.mapQg, qg, D, n_global, BH, 0) || !encode_map(&tp.mapKg, kg, D, n_global, BH, 0) ||
-          !encode_map(&tp.mapVg, vg, D, n_global, BH, 0))
+          !encode_map(&tp.mapVg, vg, D, n_global, BH, 0) || !encode_map(&tp.mapKgr, kgl, D, N, BH, 1) ||
+          !encode_map(&tp.mapVgr, vgl, D, N, BH, 1))
         return LG_ERR_CUDA;
     } else {
       tp.mapQg = tp.mapQ[0]; tp.mapKg = tp.mapK[0]; tp.mapVg = tp.mapV[0];
+      tp.mapKgr = tp.mapK[0]; tp.mapVgr = tp.mapV[0];
     }
     int start = 0;
     for (int h = 0; h < H; ++h) {
@@ -440,6 +447,29 @@ lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     if ((e = launch_merge(mp, 1, stream)) != cudaSuccess) return LG_ERR_CUDA;
   }
   return LG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lg_status lg_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, lg_dtype dt, int B,
+                      int H, int N, int D, int w_left, int w_right, const int32_t* dilation, int causal,
+                      const int32_t* global_idx, int n_global, float scale, void* workspace,
+                      size_t workspace_bytes, lg_stream_t stream) {
+  return attn_fwd_impl(q, k, v, nullptr, nullptr, nullptr, out, lse, dt, B, H, N, D, w_left, w_right, dilation,
+                       causal, global_idx, n_global, scale, workspace, workspace_bytes, stream);
+}
+
+lg_status lg_attn_fwd_gproj(const void* q, const void* k, const void* v, const void* q_glob, const void* k_glob,
+                            const void* v_glob, void* out, float* lse, lg_dtype dt, int B, int H, int N, int D,
+                            int w_left, int w_right, const int32_t* dilation, int causal,
+                            const int32_t* global_idx, int n_global, float scale, void* workspace,
+                            size_t workspace_bytes, lg_stream_t stream) {
+  if (q_glob == nullptr || k_glob == nullptr || v_glob == nullptr) return LG_ERR_INVALID_ARG;
+  if (!aligned(q_glob, 16) || !aligned(k_glob, 16) || !aligned(v_glob, 16)) return LG_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, q_glob, k_glob, v_glob, out, lse, dt, B, H, N, D, w_left, w_right, dilation,
+                       causal, global_idx, n_global, scale, workspace, workspace_bytes, stream);
 }
 
 lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, const void* q_g, const void* k_g,
@@ -496,6 +526,8 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
     tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
     tp.slot_dil[sl] = 1;
   }
+  tp.mapKgr = tp.mapK[0];
+  tp.mapVgr = tp.mapV[0];
   tp.slot_dil[0] = 1;
   tp.slot_units[0] = band_units_for(L, 1);
   for (int h = 0; h < H; ++h) {

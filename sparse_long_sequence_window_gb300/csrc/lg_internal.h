@@ -65,6 +65,7 @@ struct SimtParams {
   float* out; float* lse;                           // [BH, N, D], [BH, N]
   float* out_g; float* lse_g;                       // ETC only
   const int* gidx;                                   // Longformer global positions (device)
+  const float* qgl; const float* kgl; const float* vgl;  // Longformer global rows: their projections (= q, k, v if shared)
   int BH, H, N, D;
   int wl, wr;                                        // wr already 0 when causal
   int n_glob;                                        // Longformer: g; ETC: G
@@ -102,6 +103,8 @@ struct TcParams {
   CUtensorMap mapV[kMaxSlots];
   CUtensorMap mapQg, mapKg, mapVg;  // global side {D, g, BH}: gathered rows (Longformer) or q_g/k_g/v_g (ETC)
   CUtensorMap mapO[kMaxSlots];    // output {D, N, BH}, boxes of 32 rows x 64 columns, rows strided by the slot's dilation
+  CUtensorMap mapKgr, mapVgr;     // keys / values of the global-row units over the main sequence {D, N, BH}
+                                  // (the separate global projections, or the main k / v)
   void* out;                      // bf16 [BH, N, D]
   float* lse;                     // [BH, N]
   float* part_acc;                // [BH, n_glob, n_parts, D] unnormalised partial outputs
@@ -142,6 +145,7 @@ struct MergeParams {
 struct PrepParams {
   const int* gidx; int n_glob; int N;
   const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;  // NULL: validate only
+                                                                            // (q: the global rows' query projection)
   __nv_bfloat16* qg; __nv_bfloat16* kg; __nv_bfloat16* vg;                 // [BH, g, D]
   int* gcount;                                                              // [N + 1] or NULL
   int BH, D;

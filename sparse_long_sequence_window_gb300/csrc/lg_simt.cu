@@ -12,6 +12,10 @@
 // chunk updates an online softmax (running max m and sum l) merged across
 // the lanes with warp shuffles.
 //
+// Longformer with separate global projections ("Separate Linear Projections
+// for Local vs. Global Attention"): a global row is q_glob[i] against
+// k_glob, v_glob of every token; the other rows use q, k, v throughout.
+//
 // Work split: a band row is one warp (eight rows per block).  A global row,
 // which takes every key, is one block of eight warps: warp w takes the w-th
 // eighth of the key list, and the block combines the eight partial
@@ -69,7 +73,7 @@ struct RowPart {
 // key list.  qs: the row's query in shared memory.
 template <bool ETC>
 __device__ RowPart row_part(const SimtParams& p, int bh, int i, bool grow_row, int d, long long c_lo, long long c_hi,
-                            const float* qs, int lane) {
+                            const float* qs, int lane, const float* kmain, const float* vmain) {
   const int N = p.N, D = p.D;
   int t_lo = 0, n_band = 0;
   if (!grow_row) {
@@ -77,8 +81,8 @@ __device__ RowPart row_part(const SimtParams& p, int bh, int i, bool grow_row, i
     const int t_hi = min(p.wr, (N - 1 - i) / d);
     n_band = max(0, t_hi - t_lo + 1);
   }
-  const float* kl = p.k + static_cast<size_t>(bh) * N * D;
-  const float* vl = p.v + static_cast<size_t>(bh) * N * D;
+  const float* kl = kmain + static_cast<size_t>(bh) * N * D;
+  const float* vl = vmain + static_cast<size_t>(bh) * N * D;
   const float* kgl = ETC ? p.kg + static_cast<size_t>(bh) * p.n_glob * D : nullptr;
   const float* vgl = ETC ? p.vg + static_cast<size_t>(bh) * p.n_glob * D : nullptr;
   RowPart rp;
@@ -193,14 +197,14 @@ __global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams
     } else {
       i = __ldg(p.gidx + gi);
       if (i < 0 || i >= N) return;   // a bad list is reported by the prep kernel; nothing is written
-      qrow = p.q + (static_cast<size_t>(bh) * N + i) * D;
+      qrow = p.qgl + (static_cast<size_t>(bh) * N + i) * D;   // the global rows' query projection
     }
     for (int x = lane; x < D; x += 32) sq[wib][x] = qrow[x];
     __syncwarp();
     const long long n_cand = ETC ? static_cast<long long>(p.n_glob) + N : N;
     const long long seg = ((n_cand + kWarps - 1) / kWarps + 31) / 32 * 32;
     const long long c_lo = wib * seg, c_hi = min(n_cand, c_lo + seg);
-    const RowPart rp = row_part<ETC>(p, bh, i, true, 1, c_lo, c_hi, sq[wib], lane);
+    const RowPart rp = row_part<ETC>(p, bh, i, true, 1, c_lo, c_hi, sq[wib], lane, ETC ? p.k : p.kgl, ETC ? p.v : p.vgl);
     if (lane == 0) {
       pm[wib] = rp.m;
       pl[wib] = rp.l;
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_attn_kernel(const SimtParams
   const int t_lo = max(-p.wl, -(i / d));
   const int t_hi = min(p.wr, (N - 1 - i) / d);
   const long long n_cand = static_cast<long long>(max(0, t_hi - t_lo + 1)) + p.n_glob;
-  const RowPart rp = row_part<ETC>(p, bh, i, false, d, 0, n_cand, sq[wib], lane);
+  const RowPart rp = row_part<ETC>(p, bh, i, false, d, 0, n_cand, sq[wib], lane, p.k, p.v);
   write_row<ETC>(p, bh, i, false, rp, lane);
 }
 

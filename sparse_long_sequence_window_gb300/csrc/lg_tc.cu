@@ -284,7 +284,7 @@ __device__ __forceinline__ void tile_source(const TcParams& p, const Unit& w, in
     if (p.etc && kt < gt_src) {
       m = is_k ? &p.mapKg : &p.mapVg; strided = false; y = kt * kTileN;
     } else {
-      m = is_k ? &p.mapK[0] : &p.mapV[0]; strided = true;
+      m = is_k ? &p.mapKgr : &p.mapVgr; strided = true;   // d = 1 view of the main sequence
       y = (kt - (p.etc ? gt_src : 0)) * kTileN;
     }
   }

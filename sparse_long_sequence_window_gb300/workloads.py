@@ -12,7 +12,9 @@ round-to-nearest-even before either side sees them, so a comparison measures
 kernel error only.  Random global positions are distinct, drawn with
 ``default_rng(seed + 1000)`` and sorted ascending.  The upstream gradient dO
 of the backward pass (and dO_g of the ETC global outputs) is iid N(0, 1)
-from ``default_rng(seed + 7919)``, rounded like the inputs.
+from ``default_rng(seed + 7919)``, rounded like the inputs.  Separate global
+projections (q_glob, k_glob, v_glob) are iid N(0, 1) from
+``default_rng(seed + 4243)``, in that order, rounded like the inputs.
 
 The presets mirror the pages' workloads: a Longformer-base QA shape
 (CLS + question span global), an ETC-base shape (local radius 84, a few
@@ -130,3 +132,12 @@ def make_grad_out(w: Workload) -> dict:
     if w.is_etc:
         out["dout_g"] = _round(rng.standard_normal((w.B, w.H, w.etc_G, w.D), dtype=np.float32), w.dtype)
     return out
+
+
+def make_global_projections(w: Workload) -> dict:
+    """Separate projections for global attention, [B, H, N, D] each: q_glob,
+    k_glob, v_glob iid N(0, 1) from default_rng(seed + 4243), in the
+    workload's dtype."""
+    rng = np.random.default_rng(w.seed + 4243)
+    shape = (w.B, w.H, w.N, w.D)
+    return {n: _round(rng.standard_normal(shape, dtype=np.float32), w.dtype) for n in ("q_glob", "k_glob", "v_glob")}

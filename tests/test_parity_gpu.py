@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import lg_oracle
 from sparse_long_sequence_window_gb300 import workloads
 from sparse_long_sequence_window_gb300.workloads import Workload
 from tests import parity_util as pu
@@ -111,6 +112,58 @@ def test_explicit_scale(cuda_lib, w, scale):
 @pytest.mark.parametrize("dtype,D,scale", [("f32", 32, 0.37), ("bf16", 64, 0.05), ("bf16", 128, 0.37)])
 def test_explicit_scale_etc(cuda_lib, dtype, D, scale):
     pu.run_etc(cuda_lib, W(f"{dtype} etc scale D{D}", dtype, 1, 2, 500, D, 0, 0, etc_G=40, radius=15), scale=scale)
+
+
+# ---------------------------------------------------------------- separate global projections
+
+def run_gproj(lg, w):
+    inp = workloads.make_inputs(w)
+    gp = workloads.make_global_projections(w)
+    dev = torch.device("cuda")
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    qg, kg, vg = (gp[n].to(dev) for n in ("q_glob", "k_glob", "v_glob"))
+    g = inp["global_idx"]
+    gd = torch.from_numpy(g).to(dev)
+    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd,
+                           q_global=qg, k_global=kg, v_global=vg)
+    torch.cuda.synchronize()
+    assert lg.query_status(lg.attn_fwd.last_workspace) == 0
+    npx = [pu.to_np32(x) for x in (inp["q"], inp["k"], inp["v"], gp["q_glob"], gp["k_glob"], gp["v_glob"])]
+    ref_o, ref_l = lg_oracle.attn_fwd_gproj(*npx, w.w_left, w.w_right, w.dilations(), w.causal, g)
+    return pu.compare(w.name, w.dtype, out.cpu(), lse.cpu(), ref_o, ref_l)
+
+
+GPROJ_CASES = [
+    W("gproj bf16 D64 dilated globals", "bf16", 1, 4, 900, 64, 50, 30, (1, 2, 3, 5), False, (0, 5, 450, 899)),
+    W("gproj bf16 D128 causal random globals", "bf16", 1, 2, 1300, 128, 90, 0, (1, 2), True, None, 150),
+    W("gproj f32 globals", "f32", 1, 3, 300, 64, 20, 12, (1, 2, 3), False, (0, 150, 299)),
+    W("gproj bf16 every token global", "bf16", 1, 1, 140, 64, 2, 2, (), False, tuple(range(140))),
+]
+
+
+@pytest.mark.parametrize("w", GPROJ_CASES, ids=lambda w: w.name)
+def test_separate_global_projections(cuda_lib, w):
+    run_gproj(cuda_lib, w)
+
+
+def test_separate_global_projections_longformer_base_full(cuda_lib):
+    """bf16 B1 H12 N4096 D64, window 256/256, globals 0..64, separate global projections: every element."""
+    run_gproj(cuda_lib, workloads.PRESETS["longformer_base"])
+
+
+def test_equal_global_projections_match_shared(cuda_lib):
+    """Passing q, k, v as the global projections gives lg_attn_fwd's bits."""
+    lg = cuda_lib
+    w = W("gproj equal", "bf16", 1, 3, 700, 128, 40, 40, (1, 2, 1), False, (0, 300, 699))
+    inp = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    gd = torch.from_numpy(inp["global_idx"]).to(dev)
+    o1, l1 = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, gd)
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2 = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), False, gd, q_global=q, k_global=k, v_global=v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 # ---------------------------------------------------------------- the reference workloads at full size
