@@ -28,9 +28,12 @@ Sources (each function names the passage it follows):
   ("Softmax unification").
 * "LONGNET: Scaling Transformers to 1,000,000,000 Tokens" (arXiv 2307.02486),
   commentary page, section 3.4, "Standard Self-Attention and Sparse Attention"
-  (a binary mask S sends disallowed logits to -inf) and "Mixture of Dilated
-  Attentions" (outputs computed over parts of the key set, weighted by their
-  softmax denominators, equal one joint softmax over the union of the keys).
+  (a binary mask S sends disallowed logits to -inf), "Dilated Attention: Core
+  Mechanism" (segments of w, every r-th row kept, dense attention among the
+  kept rows), "Multi-Head Dilated Attention: Offset Mechanism" (head j starts
+  at offset j mod r) and "Mixture of Dilated Attentions" (outputs computed
+  over parts of the key set, weighted by their softmax denominators, equal
+  one joint softmax over the union of the keys).
 
 Readings taken where the pages are silent or ambiguous (window counted in
 steps of the dilation; stride-style dilation; keys outside [0, N) dropped; a
@@ -301,6 +304,85 @@ def etc_attn_fwd_rows(q_l, k_l, v_l, q_g, k_g, v_g, radius, long_rows, scale=Non
                 o, l, _ = masked_attention(np.asarray(q_l[b, h, i], np.float64)[None, :], kk, vv, row_mask[None, :], s)
                 out_l[b, h, r], lse_l[b, h, r] = o[0], l[0]
     return out_l, out_g, lse_l, lse_g
+
+
+# --------------------------------------------------------------------------
+# LongNet dilated attention
+# --------------------------------------------------------------------------
+
+def longnet_rows(N: int, w: int, r: int, s: int, seg: int) -> np.ndarray:
+    """Positions kept by one dilation pattern (w, r) with offset s in segment `seg`.
+
+    LONGNET page, "Dilated Attention: Core Mechanism" and "Multi-Head Dilated
+    Attention: Offset Mechanism": segment i covers [i w, (i + 1) w); the
+    sparsified rows are i w + s, i w + s + r, i w + s + 2 r, ... (w / r of
+    them), clipped to the sequence.
+    """
+    a = seg * w
+    return np.array([p for p in range(a + s, min(a + w, N)) if (p - a - s) % r == 0], dtype=np.int64)
+
+
+def longnet_pattern(q, k, v, w, r, s, causal, scale):
+    """One pattern (w, r, offset s) on one head: O, LSE of the kept rows (zeros / -inf elsewhere).
+
+    Dense softmax attention among the sparsified rows of each segment (the
+    page's gather, dense attention, scatter); causal: a kept query sees the
+    kept keys at or before its own position.
+    """
+    N, D = np.asarray(q).shape
+    out = np.zeros((N, D), dtype=np.float64)
+    lse = np.full(N, -np.inf, dtype=np.float64)
+    for seg in range((N + w - 1) // w):
+        rows = longnet_rows(N, w, r, s, seg)
+        if rows.size == 0:
+            continue
+        mask = np.ones((rows.size, rows.size), dtype=bool)
+        if causal:
+            mask = rows[None, :] <= rows[:, None]
+        o, l, _ = masked_attention(np.asarray(q)[rows], np.asarray(k)[rows], np.asarray(v)[rows], mask, scale)
+        out[rows], lse[rows] = o, l
+    return out, lse
+
+
+def longnet_attn_fwd(q, k, v, seg_w, seg_r, causal=False, scale=None):
+    """LongNet mixture of dilated attentions.  q, k, v [B, H, N, D]; patterns (seg_w[i], seg_r[i]).
+
+    LONGNET page, "Mixture of Dilated Attentions": O = sum_i alpha_i O_i with
+    alpha_i = s_i / sum_j s_j, s_i the softmax denominator of pattern i for
+    the row (0 where the pattern does not keep the row).  Head h uses offset
+    s = h mod r_i for pattern i ("Multi-Head Dilated Attention: Offset
+    Mechanism").  In terms of each pattern's LSE_i = ln s_i: LSE = ln sum_i
+    s_i and O = sum_i exp(LSE_i - LSE) O_i.  A row no pattern keeps gets O = 0
+    and LSE = -inf.  Returns O [B, H, N, D], LSE [B, H, N].
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    B, H, N, D = q.shape
+    sc = default_scale(D, scale)
+    out = np.zeros((B, H, N, D)); lse = np.full((B, H, N), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            os_, ls_ = [], []
+            for w, r in zip(seg_w, seg_r):
+                o, l = longnet_pattern(q[b, h], k[b, h], v[b, h], int(w), int(r), h % int(r), causal, sc)
+                os_.append(o); ls_.append(l)
+            ls_ = np.stack(ls_); os_ = np.stack(os_)
+            m = ls_.max(axis=0)
+            keep = np.isfinite(m)
+            wts = np.where(np.isfinite(ls_), np.exp(ls_ - np.where(keep, m, 0.0)[None, :]), 0.0)
+            tot = wts.sum(axis=0)
+            lse[b, h] = np.where(keep, m + np.log(np.where(keep, tot, 1.0)), -np.inf)
+            out[b, h] = np.where(keep[:, None], (wts[:, :, None] * os_).sum(axis=0) / np.where(keep, tot, 1.0)[:, None], 0.0)
+    return out, lse
+
+
+def longnet_count_pairs(N, seg_w, seg_r, causal, h):
+    """Query-key pairs head h computes, summed over the patterns (a key kept by two patterns counts twice)."""
+    total = 0
+    for w, r in zip(seg_w, seg_r):
+        for seg in range((N + w - 1) // w):
+            n = longnet_rows(N, int(w), int(r), h % int(r), seg).size
+            total += n * (n + 1) // 2 if causal else n * n
+    return total
 
 
 # --------------------------------------------------------------------------

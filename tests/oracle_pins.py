@@ -377,11 +377,60 @@ def pin_gproj(O, seed=20):
     assert np.abs(o2[:, :, rest] - o0[:, :, rest]).max() < 1e-13 and np.abs(l2[:, :, rest] - l0[:, :, rest]).max() < 1e-13
 
 
+def pin_golden_longnet(O):
+    """Hand-worked LongNet kept rows and mixtures (tests/golden/longnet.txt)."""
+    for parts in _golden_lines("longnet.txt"):
+        if parts[0] == "rows":
+            N, w, r, head, seg = (int(x) for x in parts[1:6])
+            assert O.longnet_rows(N, w, r, head % r, seg).tolist() == _parse_list(parts[6]), parts
+        else:
+            N = int(parts[1]); ws = _parse_list(parts[2]); rs = _parse_list(parts[3]); causal = bool(int(parts[4]))
+            row, o_ref, s_ref = int(parts[5]), float(parts[6]), float(parts[7])
+            z = np.zeros((1, 1, N, 1)); v = (np.arange(N, dtype=np.float64) + 1).reshape(1, 1, N, 1)
+            o, l = O.longnet_attn_fwd(z, z, v, ws, rs, causal)
+            assert abs(o[0, 0, row, 0] - o_ref) < 1e-12 and abs(l[0, 0, row] - np.log(s_ref)) < 1e-12, parts
+
+
+def pin_longnet_reductions(O, seed=21):
+    """One pattern with w >= N, r = 1 is full attention; one pattern (w, r) on head h is dense
+    attention on the gathered rows of each segment (library SDPA), zero elsewhere."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 1, 3, 37, 8
+    q, k, v = (_rand(rng, B, H, N, D) for _ in range(3))
+    s = 1 / np.sqrt(D)
+    o, l = O.longnet_attn_fwd(q, k, v, [64], [1])
+    assert np.abs(o - _sdpa64(q, k, v, s)).max() < 1e-12
+    for w, r in ((12, 3), (16, 4), (8, 2)):
+        o, l = O.longnet_attn_fwd(q, k, v, [w], [r])
+        for h in range(H):
+            covered = np.zeros(N, dtype=bool)
+            for seg in range((N + w - 1) // w):
+                rows = [p for p in range(seg * w + h % r, min(seg * w + w, N), r)]
+                if not rows:
+                    continue
+                covered[rows] = True
+                ref = _sdpa64(q[:, h:h + 1, rows], k[:, h:h + 1, rows], v[:, h:h + 1, rows], s)
+                assert np.abs(o[:, h:h + 1, rows] - ref).max() < 1e-12
+            assert np.abs(o[:, h, ~covered]).max() == 0.0 and np.isneginf(l[:, h, ~covered]).all()
+
+
+def pin_longnet_counts(O):
+    """Pair count of the patterns: (w/r)^2 per full segment (non-causal), against brute force."""
+    assert O.longnet_count_pairs(4096, [2048, 4096], [1, 2], False, 0) == 2 * 2048 ** 2 + 2048 ** 2
+    for N, ws, rs, causal, h in ((37, [8, 16], [1, 4], False, 3), (50, [10, 20], [2, 5], True, 1)):
+        brute = 0
+        for w, r in zip(ws, rs):
+            for seg in range((N + w - 1) // w):
+                n = len(range(seg * w + h % r, min(seg * w + w, N), r))
+                brute += n * (n + 1) // 2 if causal else n * n
+        assert O.longnet_count_pairs(N, ws, rs, causal, h) == brute
+
+
 ALL_PINS = [
     pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
     pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
     pin_identity_window, pin_dilation_residues, pin_key_shift, pin_constant_values,
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
     pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
-    pin_bwd_rows_cols_vs_dense, pin_gproj,
+    pin_bwd_rows_cols_vs_dense, pin_gproj, pin_golden_longnet, pin_longnet_reductions, pin_longnet_counts,
 ]

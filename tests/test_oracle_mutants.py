@@ -156,11 +156,28 @@ def mut_bwd_cols_drop_global_rows(O):
         g if g[j] else False)
 
 
+def mut_longnet_no_offset(O):
+    # every head starts its sparsification at offset 0
+    orig = O.longnet_rows
+    O.longnet_rows = lambda N, w, r, s, seg: orig(N, w, r, 0, seg)
+
+
+def mut_longnet_plain_average(O):
+    # patterns averaged with equal weights instead of their softmax denominators
+    orig = O.longnet_pattern
+
+    def pattern(q, k, v, w, r, s, causal, scale):
+        o, l = orig(q, k, v, w, r, s, causal, scale)
+        return o, np.where(np.isfinite(l), 0.0, l)
+    O.longnet_pattern = pattern
+
+
 MUTANTS = [mut_swap_sides, mut_ignore_dilation, mut_span_not_steps, mut_causal_keeps_right,
            mut_no_global_columns, mut_no_scale, mut_transposed_logits, mut_lse_log2,
            mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale,
            mut_bwd_no_delta, mut_bwd_no_scale, mut_bwd_dk_untransposed, mut_bwd_dv_untransposed,
-           mut_gproj_local_keys, mut_bwd_cols_drop_global_rows]
+           mut_gproj_local_keys, mut_bwd_cols_drop_global_rows, mut_longnet_no_offset,
+           mut_longnet_plain_average]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
