@@ -50,6 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 def useful_pairs(lg, w: workloads.Workload) -> int:
+    if w.is_longnet:
+        return w.B * sum(lg.longnet_count_pairs(w.N, w.seg_w, w.seg_r, w.causal, h) for h in range(w.H))
     if w.is_etc:
         return w.B * w.H * lg.etc_count_pairs(w.N, w.etc_G, w.radius)
     g = workloads.global_positions(w)
@@ -139,6 +141,8 @@ def device_inputs(w, dev, torch):
         for n in ("q_g", "k_g", "v_g"):
             t[n] = rnd(w.B, w.H, w.etc_G, w.D)
         t["g"] = None
+    elif w.is_longnet:
+        t["g"] = None
     else:
         g = workloads.global_positions(w)
         t["g"] = torch.from_numpy(g).to(dev) if g.size else None
@@ -148,6 +152,15 @@ def device_inputs(w, dev, torch):
 def make_call(lg, w, t, torch):
     """Returns f() that runs one forward pass with preallocated outputs and workspace."""
     dev = t["q"].device
+    if w.is_longnet:
+        out = torch.empty_like(t["q"])
+        lse = torch.empty(w.B, w.H, w.N, device=dev)
+        ws = torch.empty(lg.longnet_attn_fwd_workspace_size(w.B, w.H, w.N, w.D, w.seg_w, w.seg_r),
+                         dtype=torch.uint8, device=dev)
+
+        def f():
+            lg.longnet_attn_fwd(t["q"], t["k"], t["v"], w.seg_w, w.seg_r, w.causal, out=out, lse=lse, workspace=ws)
+        return f, (out, lse), ws
     if w.is_etc:
         B, H, L, D, G = w.B, w.H, w.N, w.D, w.etc_G
         out_l, out_g = torch.empty_like(t["q"]), torch.empty_like(t["q_g"])
@@ -174,6 +187,10 @@ def make_call(lg, w, t, torch):
 
 
 def launches_per_call(w):
+    if w.is_longnet:
+        # per pattern: unit table + tensor-core kernel (+ gather for the packed layout); then the mix
+        packed = sum(1 for a, r in zip(w.seg_w, w.seg_r) if not (r <= 8 and a % r == 0))
+        return 2 * len(w.seg_w) + packed + 1
     if w.dtype == "f32":
         return 2 if (not w.is_etc and (w.global_positions or w.n_random_global)) else 1
     if w.is_etc:
@@ -283,7 +300,7 @@ def run_native(args, rank, world):
     h2d = sum(x.numel() * x.element_size() for x in host.values() if x is not None)
     d2h = sum(o.numel() * o.element_size() for o in host_out)
     e_times = []
-    if not w.is_etc and w.dtype == "bf16":
+    if not w.is_etc and not w.is_longnet and w.dtype == "bf16":
         # lg_attn_fwd_host: the library copies q/k/v in and out/lse back itself,
         # overlapping the copies of one group of heads with the kernels of another.
         g_host = host.pop("g", None)
@@ -380,7 +397,7 @@ def bench_backward(lg, torch, w, t, outs, flush, steps, peaks, peak_kind):
     CUDA events on the current stream, L2 flushed between steps when the
     inputs fit in it.
     """
-    if w.dtype != "bf16":
+    if w.dtype != "bf16" or w.is_longnet:   # no LongNet backward
         return None
     gen = torch.Generator(device=t["q"].device)
     gen.manual_seed(w.seed + 7919)
@@ -444,8 +461,9 @@ def sweep(lg, torch, dev):
                      "status": lg.status_string(st)}
         if w.dtype == "bf16" and not getattr(sweep, "no_bwd", False):
             b = bench_backward(lg, torch, w, t, outs, in_bytes < 2 * L2_BYTES, 10 if w.N >= 100000 else 30, {}, "")
-            res[name]["bwd_tflops"] = b["value"]
-            res[name]["bwd_ms"] = b["ms_per_call"]
+            if b is not None:
+                res[name]["bwd_tflops"] = b["value"]
+                res[name]["bwd_ms"] = b["ms_per_call"]
         del t, f, outs, ws
         torch.cuda.empty_cache()
     return res
@@ -514,6 +532,19 @@ def cpu_sample(w, budget_s, seed=1234, arrs=None):
             lg_oracle.etc_attn_fwd_rows(*arrs, w.radius, [i])
             lo, hi = max(0, i - w.radius), min(N - 1, i + w.radius)
             flops += 4.0 * D * ((hi - lo + 1) + G)
+            rows += 1
+        return flops, time.perf_counter() - t0, rows
+    if w.is_longnet:
+        q, k, v = arrs
+        flops = 0.0; rows = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            i = int(rng.integers(0, N))
+            lg_oracle.longnet_attn_fwd_rows(q, k, v, w.seg_w, w.seg_r, w.causal, [i])
+            for sw, sr in zip(w.seg_w, w.seg_r):   # head 0: offset 0
+                kept = lg_oracle.longnet_rows(N, sw, sr, 0, i // sw)
+                if (kept == i).any():
+                    flops += 4.0 * D * int((kept <= i).sum() if w.causal else kept.size)
             rows += 1
         return flops, time.perf_counter() - t0, rows
     g = workloads.global_positions(w)

@@ -283,6 +283,42 @@ lg_status lg_etc_attn_bwd(const void* q_l, const void* k_l, const void* v_l,
                           void* workspace, size_t workspace_bytes, lg_stream_t stream);
 
 /*
+ * LongNet mixture of dilated attentions ("LONGNET: Scaling Transformers to
+ * 1,000,000,000 Tokens", section 3.4, "Dilated Attention: Core Mechanism",
+ * "Mixture of Dilated Attentions", "Multi-Head Dilated Attention: Offset
+ * Mechanism").  Pattern k (segment length seg_w[k], dilation rate seg_r[k])
+ * on head h keeps the rows i*w + s, i*w + s + r, ... below (i+1)*w (s = h mod
+ * r) of each segment [i*w, (i+1)*w) and runs softmax attention among the kept
+ * rows of the segment (causal: a kept row sees the kept rows at or before
+ * it).  The patterns of a row are mixed by their softmax denominators: LSE =
+ * ln sum_k exp(LSE_k) over the patterns that keep the row, O = sum_k
+ * exp(LSE_k - LSE) O_k; a row no pattern keeps gets O = 0 and LSE = -inf.
+ *
+ *  q, k, v, out  device, [B, H, N, D], bf16, D in {64, 128}; lse fp32 [B, H, N]
+ *                (LG_ERR_UNSUPPORTED for fp32 or another D).
+ *  n_patterns    1..16; seg_w, seg_r: HOST arrays of n_patterns ints >= 1
+ *                (any r; r need not divide w).
+ *  workspace     >= lg_longnet_attn_fwd_workspace_size(...) bytes, 256-byte
+ *                aligned: one output and LSE per pattern, the packed copies
+ *                of q, k, v for patterns read through a gather, and the
+ *                work-unit table.
+ * Other arguments, errors and asynchrony as for lg_attn_fwd.  0 from the
+ * size query means invalid or unsupported arguments.
+ */
+size_t lg_longnet_attn_fwd_workspace_size(int B, int H, int N, int D, int n_patterns, const int32_t* seg_w,
+                                          const int32_t* seg_r, lg_dtype dt);
+lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                              lg_dtype dt, int B, int H, int N, int D,
+                              int n_patterns, const int32_t* seg_w, const int32_t* seg_r, int causal,
+                              float scale, void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/* Query-key pairs head `head` computes over all patterns (a pair two
+ * patterns keep counts twice): the useful work of lg_longnet_attn_fwd is
+ * 4 * D times the sum over batches and heads.  -1 on invalid arguments. */
+int64_t lg_longnet_count_pairs(int N, int n_patterns, const int32_t* seg_w, const int32_t* seg_r, int causal,
+                               int head);
+
+/*
  * Synchronises `stream`, then returns the device status recorded in
  * `workspace` by the last call that used it (LG_OK if none) and clears it.
  * Returns LG_ERR_CUDA if the synchronisation or the read fails.

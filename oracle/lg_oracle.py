@@ -319,7 +319,7 @@ def longnet_rows(N: int, w: int, r: int, s: int, seg: int) -> np.ndarray:
     them), clipped to the sequence.
     """
     a = seg * w
-    return np.array([p for p in range(a + s, min(a + w, N)) if (p - a - s) % r == 0], dtype=np.int64)
+    return np.arange(a + s, min(a + w, N), r, dtype=np.int64)
 
 
 def longnet_pattern(q, k, v, w, r, s, causal, scale):
@@ -365,13 +365,48 @@ def longnet_attn_fwd(q, k, v, seg_w, seg_r, causal=False, scale=None):
             for w, r in zip(seg_w, seg_r):
                 o, l = longnet_pattern(q[b, h], k[b, h], v[b, h], int(w), int(r), h % int(r), causal, sc)
                 os_.append(o); ls_.append(l)
-            ls_ = np.stack(ls_); os_ = np.stack(os_)
-            m = ls_.max(axis=0)
-            keep = np.isfinite(m)
-            wts = np.where(np.isfinite(ls_), np.exp(ls_ - np.where(keep, m, 0.0)[None, :]), 0.0)
-            tot = wts.sum(axis=0)
-            lse[b, h] = np.where(keep, m + np.log(np.where(keep, tot, 1.0)), -np.inf)
-            out[b, h] = np.where(keep[:, None], (wts[:, :, None] * os_).sum(axis=0) / np.where(keep, tot, 1.0)[:, None], 0.0)
+            out[b, h], lse[b, h] = _longnet_mix(np.stack(os_), np.stack(ls_))
+    return out, lse
+
+
+def _longnet_mix(os_, ls_):
+    """Mix per-pattern outputs os_ [k, n, D] with their LSE ls_ [k, n] (-inf: not kept) by softmax denominators."""
+    m = ls_.max(axis=0)
+    keep = np.isfinite(m)
+    wts = np.where(np.isfinite(ls_), np.exp(ls_ - np.where(keep, m, 0.0)[None, :]), 0.0)
+    tot = wts.sum(axis=0)
+    lse = np.where(keep, m + np.log(np.where(keep, tot, 1.0)), -np.inf)
+    out = np.where(keep[:, None], (wts[:, :, None] * os_).sum(axis=0) / np.where(keep, tot, 1.0)[:, None], 0.0)
+    return out, lse
+
+
+def longnet_attn_fwd_rows(q, k, v, seg_w, seg_r, causal, rows, scale=None):
+    """``longnet_attn_fwd`` at the given query rows only, one row at a time.
+
+    Row i of head h under pattern (w, r): if the pattern keeps i (i in
+    ``longnet_rows`` of its segment i // w with offset h mod r), its keys are
+    the kept rows of that segment (those at or before i when causal).
+    Returns O [B, H, len(rows), D], LSE [B, H, len(rows)].
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    B, H, N, D = q.shape
+    sc = default_scale(D, scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((B, H, rows.size, D)); lse = np.full((B, H, rows.size), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            os_ = np.zeros((len(seg_w), rows.size, D)); ls_ = np.full((len(seg_w), rows.size), -np.inf)
+            for pi, (w, r) in enumerate(zip(seg_w, seg_r)):
+                w, r = int(w), int(r)
+                for x, i in enumerate(rows):
+                    kept = longnet_rows(N, w, r, h % r, int(i) // w)
+                    if not (kept == i).any():
+                        continue
+                    keys = kept[kept <= i] if causal else kept
+                    o, l, _ = masked_attention(q[b, h, i][None, :], k[b, h, keys], v[b, h, keys],
+                                               np.ones((1, keys.size), dtype=bool), sc)
+                    os_[pi, x], ls_[pi, x] = o[0], l[0]
+            out[b, h], lse[b, h] = _longnet_mix(os_, ls_)
     return out, lse
 
 

@@ -18,6 +18,7 @@ import numpy as np
 __all__ = [
     "LgError", "load", "attn_fwd", "attn_fwd_host", "etc_attn_fwd", "attn_fwd_workspace_size",
     "attn_bwd", "etc_attn_bwd", "attn_bwd_workspace_size", "etc_attn_bwd_workspace_size",
+    "longnet_attn_fwd", "longnet_count_pairs", "longnet_attn_fwd_workspace_size",
     "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
     "profile_begin", "profile_end", "status_string", "debug_timeout_test", "LIB_PATH",
 ]
@@ -76,6 +77,12 @@ def load() -> ctypes.CDLL:
     lib.lg_attn_bwd.argtypes = [vp] * 9 + [i32] * 7 + [vp, i32, vp, i32, f32, vp, sz, vp]
     lib.lg_etc_attn_bwd.restype = i32
     lib.lg_etc_attn_bwd.argtypes = [vp] * 18 + [i32] * 7 + [f32, vp, sz, vp]
+    lib.lg_longnet_attn_fwd_workspace_size.restype = sz
+    lib.lg_longnet_attn_fwd_workspace_size.argtypes = [i32] * 5 + [vp, vp, i32]
+    lib.lg_longnet_attn_fwd.restype = i32
+    lib.lg_longnet_attn_fwd.argtypes = [vp] * 5 + [i32] * 6 + [vp, vp, i32, f32, vp, sz, vp]
+    lib.lg_longnet_count_pairs.restype = ctypes.c_int64
+    lib.lg_longnet_count_pairs.argtypes = [i32, i32, vp, vp, i32, i32]
     lib.lg_debug_timeout_test.restype = i32
     lib.lg_debug_timeout_test.argtypes = [i32, ctypes.c_longlong]
     lib.lg_profile_begin.restype = i32
@@ -396,6 +403,56 @@ def etc_attn_bwd(q_l, k_l, v_l, q_g, k_g, v_g, out_l, out_g, lse_l, lse_g, dout_
         _keep_for(stream, ws)
     etc_attn_bwd.last_workspace = ws
     return tuple(grads)
+
+
+def longnet_attn_fwd(q, k, v, seg_w: Sequence[int], seg_r: Sequence[int], causal: bool = False,
+                     scale: Optional[float] = None, out=None, lse=None, workspace=None, stream=None):
+    """LongNet mixture of dilated attentions (lg_longnet_attn_fwd): patterns (seg_w[k], seg_r[k]),
+    head h offset h mod r.  q, k, v: bf16 CUDA tensors [B, H, N, D].  Returns (out, lse)."""
+    import torch
+    lib = load()
+    if q.dim() != 4 or not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor [B, H, N, D]")
+    _same(q, "k", k, v)
+    B, H, N, D = q.shape
+    sw = np.ascontiguousarray(np.asarray(seg_w, dtype=np.int32))
+    sr = np.ascontiguousarray(np.asarray(seg_r, dtype=np.int32))
+    if sw.size != sr.size:
+        raise ValueError("seg_w and seg_r need the same length")
+    dt = _dtype_code(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_out(out, q.shape, q.dtype, q.device, "out")
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
+    need = int(lib.lg_longnet_attn_fwd_workspace_size(B, H, N, D, int(sw.size), sw.ctypes.data, sr.ctypes.data, dt))
+    if need == 0:
+        raise NotImplementedError("lg_longnet_attn_fwd: unsupported shape, dtype or patterns")
+    ws = _workspace(need, q.device, workspace)
+    st = lib.lg_longnet_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), dt, B, H, N, D, int(sw.size),
+                                 sw.ctypes.data, sr.ctypes.data, int(bool(causal)), float(scale) if scale else 0.0,
+                                 ws.data_ptr(), _nbytes(ws), _stream(stream))
+    _check(st, "lg_longnet_attn_fwd")
+    if workspace is None:
+        _keep_for(stream, ws)
+    longnet_attn_fwd.last_workspace = ws
+    return out, lse
+
+
+def longnet_attn_fwd_workspace_size(B, H, N, D, seg_w, seg_r, dtype=LG_BF16) -> int:
+    sw = np.ascontiguousarray(np.asarray(seg_w, dtype=np.int32))
+    sr = np.ascontiguousarray(np.asarray(seg_r, dtype=np.int32))
+    return int(load().lg_longnet_attn_fwd_workspace_size(B, H, N, D, int(sw.size), sw.ctypes.data, sr.ctypes.data,
+                                                          int(dtype)))
+
+
+def longnet_count_pairs(N, seg_w, seg_r, causal, head) -> int:
+    sw = np.ascontiguousarray(np.asarray(seg_w, dtype=np.int32))
+    sr = np.ascontiguousarray(np.asarray(seg_r, dtype=np.int32))
+    r = load().lg_longnet_count_pairs(int(N), int(sw.size), sw.ctypes.data, sr.ctypes.data, int(bool(causal)),
+                                      int(head))
+    if r < 0:
+        raise ValueError("invalid arguments to lg_longnet_count_pairs")
+    return int(r)
 
 
 def query_status(workspace, stream=None) -> int:

@@ -16,19 +16,7 @@ namespace lg {
 int tc_rows_per_load(int d);
 }
 
-using namespace lg;
-
-namespace {
-
-// ------------------------------------------------------------------ helpers
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
-
-// Cap of the bounded work waits and the timeout-test switch (lg_debug_timeout_test).
-std::atomic<long long> g_wait_cap_override{0};
-std::atomic<int> g_withhold{0};
+namespace lg {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -76,6 +64,63 @@ bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH, int d
   return r == CUDA_SUCCESS;
 }
 
+// Band units at the end of a launch of `units` units to split in two
+// one-tile units each: the last round of a persistent launch (units mod grid
+// units) when splitting it still leaves at most one item per CTA; 0 otherwise.
+long long tail_split(long long units, long long band_units) {
+  const long long grid = std::min<long long>(units, device_sm_count());
+  if (grid <= 0 || units <= grid) return 0;
+  const long long last = units % grid;
+  return (last > 0 && last <= grid - last && last <= band_units) ? last : 0;
+}
+
+// ------------------------------------------------------------------ profiling
+
+struct Profiler {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> events;
+  size_t used = 0;
+};
+Profiler& prof() {
+  static Profiler p;
+  return p;
+}
+
+cudaError_t prof_mark(cudaStream_t s, bool start) {
+  Profiler& p = prof();
+  if (!p.on) return cudaSuccess;
+  if (start) {
+    if (p.used == p.events.size()) {
+      cudaEvent_t a, b;
+      cudaError_t e = cudaEventCreate(&a);
+      if (e != cudaSuccess) return e;
+      e = cudaEventCreate(&b);
+      if (e != cudaSuccess) return e;
+      p.events.emplace_back(a, b);
+    }
+    return cudaEventRecord(p.events[p.used].first, s);
+  }
+  cudaError_t e = cudaEventRecord(p.events[p.used].second, s);
+  ++p.used;
+  return e;
+}
+
+}  // namespace lg
+
+using namespace lg;
+
+namespace {
+
+// ------------------------------------------------------------------ helpers
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Cap of the bounded work waits and the timeout-test switch (lg_debug_timeout_test).
+std::atomic<long long> g_wait_cap_override{0};
+std::atomic<int> g_withhold{0};
+
 // Band work units of one head: pairs of 128-step query tiles in each residue class.
 int band_units_for(int N, int d) {
   int units = 0;
@@ -113,16 +158,6 @@ GrowPlan grow_plan(int n_glob, int key_tiles, int split) {
   g.n_splits = cdiv(key_tiles, g.split);
   g.n_parts = 2 * g.n_splits;
   return g;
-}
-
-// Band units at the end of a launch of `units` units to split in two
-// one-tile units each: the last round of a persistent launch (units mod grid
-// units) when splitting it still leaves at most one item per CTA; 0 otherwise.
-long long tail_split(long long units, long long band_units) {
-  const long long grid = std::min<long long>(units, device_sm_count());
-  if (grid <= 0 || units <= grid) return 0;
-  const long long last = units % grid;
-  return (last > 0 && last <= grid - last && last <= band_units) ? last : 0;
 }
 
 // Key tiles per split for a launch: a global-row unit (split / 2 key tiles per
@@ -169,37 +204,6 @@ WsLayout ws_layout(int BH, int n_glob, int D, int n_splits, bool gather, int N, 
   off += round_up(w.max_units * 64, 256);
   w.total = off;
   return w;
-}
-
-// ------------------------------------------------------------------ profiling
-
-struct Profiler {
-  bool on = false;
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> events;
-  size_t used = 0;
-};
-Profiler& prof() {
-  static Profiler p;
-  return p;
-}
-
-cudaError_t prof_mark(cudaStream_t s, bool start) {
-  Profiler& p = prof();
-  if (!p.on) return cudaSuccess;
-  if (start) {
-    if (p.used == p.events.size()) {
-      cudaEvent_t a, b;
-      cudaError_t e = cudaEventCreate(&a);
-      if (e != cudaSuccess) return e;
-      e = cudaEventCreate(&b);
-      if (e != cudaSuccess) return e;
-      p.events.emplace_back(a, b);
-    }
-    return cudaEventRecord(p.events[p.used].first, s);
-  }
-  cudaError_t e = cudaEventRecord(p.events[p.used].second, s);
-  ++p.used;
-  return e;
 }
 
 lg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LG_OK : LG_ERR_CUDA; }
@@ -416,6 +420,9 @@ lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void*
     }
     tp.head_unit_start[H] = start;
     tp.band_units_per_batch = start;
+    for (int h = 0; h < H; ++h) tp.head_class[h] = -1;
+    tp.seg_w = 0;
+    tp.seg_causal = 0;
     tp.out = out; tp.lse = lse;
     tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
     tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);
@@ -536,6 +543,9 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   }
   tp.head_unit_start[H] = H * tp.slot_units[0];
   tp.band_units_per_batch = H * tp.slot_units[0];
+  for (int h = 0; h < H; ++h) tp.head_class[h] = -1;
+  tp.seg_w = 0;
+  tp.seg_causal = 0;
   tp.out = out_l; tp.lse = lse_l;
   tp.part_acc = reinterpret_cast<float*>(ws + lay.acc);
   tp.part_ml = reinterpret_cast<float*>(ws + lay.ml);

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -132,8 +133,26 @@ struct TcParams {
   int slot_dil[kMaxSlots];
   int slot_units[kMaxSlots];      // band units of one head with this slot's dilation
   unsigned char head_slot[LG_MAX_HEADS];  // 255: head not in this launch
+  signed char head_class[LG_MAX_HEADS];   // >= 0: the one residue class this head computes (LongNet offset); -1: all
+  // Segment mode (LongNet dilated attention), seg_w > 0: pattern (seg_w,
+  // seg_r) over a sequence of seg_n tokens; a row sees the keys of its
+  // segment's block (seg_block).  seg_packed = 0: the tensors are the
+  // original [BH, N, D] ones, read in class h mod seg_r with stride seg_r;
+  // 1: they hold each head's kept rows packed segment after segment
+  // (N = the packed length, class 0, stride 1).
+  int seg_w, seg_r, seg_n, seg_packed;
+  int seg_causal;                 // segment mode: only keys at or before the query
   int head_unit_start[LG_MAX_HEADS + 1];  // prefix of band units over heads (one batch)
 };
+
+// LongNet pattern (w, r), head offset s = h mod r: the kept rows of segment i
+// are i w + s + t r, 0 <= t < seg_block (those below N).  seg_class_len: the
+// kept rows of one head over the sequence (the packed length).
+__host__ __device__ inline int seg_block(int w, int r, int s) { return w > s ? (w - s + r - 1) / r : 0; }
+__host__ __device__ inline int seg_class_len(int N, int w, int r, int s) {
+  const int n_full = N / w, rest = N - n_full * w;
+  return n_full * seg_block(w, r, s) + (rest > s ? (rest - s + r - 1) / r : 0);
+}
 
 struct MergeParams {
   const float* part_acc; const float* part_ml;
@@ -232,6 +251,12 @@ cudaError_t launch_bwd_reduce(const BwdReduceParams& p, cudaStream_t s);
 __host__ __device__ int bwd_class_stride(int N, int d);   // M: class stride of the class-major vectors
 int bwd_cm(int N);                     // CM: per-(b, h) length of the class-major vectors
 size_t tc_smem_bytes(int D);
+// bf16 tensor maps of [BH, rows, D] as {D, rows, BH}: load maps with boxes of
+// rows_per_load(d) * d rows (element stride d; d = 0: plain 128-row boxes),
+// store maps with boxes of 32 * d rows.
+bool encode_map(CUtensorMap* m, const void* base, int D, int rows, int BH, int d);
+bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH, int d);
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 // Cap of the bounded work waits (clock64 cycles) and the timeout-test switch,
 // as set by lg_debug_timeout_test (default: about one second, no withholding).
 long long wait_cap_cycles();
@@ -248,6 +273,10 @@ lg_status validate_fwd(const void* q, const void* k, const void* v, const void* 
                        lg_dtype dt, int B, int H, int N, int D, int w_left, int w_right, const int32_t* dilation,
                        int causal, const int32_t* global_idx, int n_global, const void* workspace,
                        size_t workspace_bytes, bool per_call_head_limit);
-int device_sm_count();  // SMs of the current device (cached per device)
+int device_sm_count();
+// Band units of a launch of `units` units to split into one-tile halves (the last round).
+long long tail_split(long long units, long long band_units);
+// Profiling of the tensor-core launches (lg_profile_begin/end): events around a launch.
+cudaError_t prof_mark(cudaStream_t s, bool start);  // SMs of the current device (cached per device)
 
 }  // namespace lg

@@ -105,6 +105,7 @@ struct Unit {
   int n_tiles;
   int first[2], last[2];  // band: range of band tiles each query tile needs (first > last: none)
   int active[2];
+  int seg;           // band, segment mode: class steps of a segment block (0: window mode)
 };
 
 // Unit u of a launch of n_units from its index (the arithmetic behind the
@@ -143,18 +144,34 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
   w.bh = b * p.H + h;
   w.slot = p.head_slot[h];
   w.d = p.slot_dil[w.slot];
-  for (int c = 0; c < w.d; ++c) {
-    const int n_c = (p.N - c + w.d - 1) / w.d;
-    const int units = (n_c + 2 * kTileM - 1) / (2 * kTileM);
-    if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
-    rem -= units;
+  w.seg = 0;
+  if (p.seg_w > 0) {            // LongNet: one residue class per head (offset h mod r)
+    const int s = h % p.seg_r;
+    w.seg = p.seg_packed ? seg_block(p.seg_w, p.seg_r, s) : p.seg_w / p.seg_r;
+    w.c = p.seg_packed ? 0 : s;
+    w.n_c = p.seg_packed ? seg_class_len(p.seg_n, p.seg_w, p.seg_r, s) : (p.N - s + w.d - 1) / w.d;
+    w.t0 = rem * 2 * kTileM;
+  } else if (p.head_class[h] >= 0) {
+    w.c = p.head_class[h];
+    w.n_c = (p.N - w.c + w.d - 1) / w.d;
+    w.t0 = rem * 2 * kTileM;
+  } else {
+    for (int c = 0; c < w.d; ++c) {
+      const int n_c = (p.N - c + w.d - 1) / w.d;
+      const int units = (n_c + 2 * kTileM - 1) / (2 * kTileM);
+      if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
+      rem -= units;
+    }
   }
   const int span = half >= 0 ? 1 : 2;                 // query tiles of this unit
   if (half > 0) w.t0 += kTileM;
   if (w.n_c <= 0 || w.t0 >= w.n_c) { w.n_tiles = 0; return w; }
   const int t_last = min(w.t0 + span * kTileM - 1, w.n_c - 1);
-  w.band_lo = max(0, w.t0 - p.wl);
-  const int band_hi = min(w.n_c - 1, t_last + p.wr);
+  // key steps of a query step t: [t - w_left, t + w_right], or in segment
+  // mode its block [B floor(t / B), B floor(t / B) + B - 1] (up to t if causal)
+  const int B = w.seg;
+  w.band_lo = B > 0 ? (w.t0 / B) * B : max(0, w.t0 - p.wl);
+  const int band_hi = min(w.n_c - 1, B > 0 ? (p.seg_causal ? t_last : (t_last / B) * B + B - 1) : t_last + p.wr);
   w.n_band = (band_hi - w.band_lo + kTileN) / kTileN;
   const int n_gt = (p.n_glob + kTileN - 1) / kTileN;
   w.n_tiles = w.n_band + n_gt;
@@ -163,7 +180,8 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
     w.active[q] = q < span && a < w.n_c;
     if (!w.active[q]) { w.first[q] = 1; w.last[q] = 0; continue; }
     const int b_ = min(a + kTileM - 1, w.n_c - 1);
-    const int klo = max(0, a - p.wl), khi = min(w.n_c - 1, b_ + p.wr);
+    const int klo = B > 0 ? (a / B) * B : max(0, a - p.wl);
+    const int khi = min(w.n_c - 1, B > 0 ? (p.seg_causal ? b_ : (b_ / B) * B + B - 1) : b_ + p.wr);
     w.first[q] = (klo - w.band_lo) / kTileN;
     w.last[q] = (khi - w.band_lo) / kTileN;
   }
@@ -181,7 +199,7 @@ __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_unit
     rec[0] = make_int4(w.bh, flags, w.t0, w.n_c);
     rec[1] = make_int4(w.band_lo, w.n_band, w.kt0, w.grow0);
     rec[2] = make_int4(w.n_tiles, w.first[0], w.first[1], w.last[0]);
-    rec[3] = make_int4(w.last[1], 0, 0, 0);
+    rec[3] = make_int4(w.last[1], w.grow ? 0 : w.seg, 0, 0);
   }
   grid_dep_wait();     // complete only after the call's earlier kernels
 }
@@ -215,6 +233,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   w.first[1] = c.z;
   w.last[0] = c.w;
   w.last[1] = d.x;
+  w.seg = d.y;
   return w;
 }
 
@@ -703,6 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const int t_q = w.t0 + q * kTileM + r;            // band: query step in the class
       const int pos_q = w.c + w.d * t_q;                // band: query position
       const bool row_valid = w.grow ? (w.grow0 + r < p.n_glob) : (t_q < w.n_c);
+      // this row's key steps in its class: the window, or its segment block
+      const int seg_b = w.seg > 0 ? (t_q / w.seg) * w.seg : 0;
+      const int row_lo = w.seg > 0 ? seg_b : t_q - p.wl;
+      const int row_hi = min(w.seg > 0 ? (p.seg_causal ? t_q : seg_b + w.seg - 1) : t_q + p.wr, w.n_c - 1);
       float m_run = -INFINITY, l_run = 0.f;             // m_run in log2 units of the scaled logits
       int n_unit = 0;
       // Global keys (Longformer) already inside this row's band are masked in
@@ -725,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       if (!w.grow) {
         if (j < w.n_band) {
           const int k0 = w.band_lo + j * kTileN;
-          lo = t_q - p.wl - k0;
-          hi = min(t_q + p.wr, w.n_c - 1) - k0;
+          lo = row_lo - k0;
+          hi = row_hi - k0;
         } else {
           const int g0 = (j - w.n_band) * kTileN;
           hi = min(kTileN, p.n_glob - g0) - 1;

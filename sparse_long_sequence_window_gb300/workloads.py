@@ -18,8 +18,9 @@ projections (q_glob, k_glob, v_glob) are iid N(0, 1) from
 
 The presets mirror the pages' workloads: a Longformer-base QA shape
 (CLS + question span global), an ETC-base shape (local radius 84, a few
-hundred global tokens), a character-LM shape (causal, dilated heads) and a
-long-sequence sweep.  The pages evaluate on datasets that are not used here;
+hundred global tokens), a character-LM shape (causal, dilated heads), a
+long-sequence sweep, and the LongNet language-model mixture (12 heads of 64,
+32K tokens, causal, segments 2K..32K with rates 1, 2, 4, 6, 12).  The pages evaluate on datasets that are not used here;
 these synthetic tensors stand in for them.
 """
 from __future__ import annotations
@@ -48,10 +49,16 @@ class Workload:
     etc_G: int = 0               # > 0 selects the ETC call with a separate global input
     radius: int = 0              # ETC local radius
     seed: int = 0
+    seg_w: Sequence[int] = ()    # LongNet: segment lengths of the mixture's patterns
+    seg_r: Sequence[int] = ()    # LongNet: their dilation rates
 
     @property
     def is_etc(self) -> bool:
         return self.etc_G > 0
+
+    @property
+    def is_longnet(self) -> bool:
+        return len(self.seg_w) > 0
 
     def dilations(self):
         return list(self.dilation) if self.dilation else [1] * self.H
@@ -60,7 +67,7 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five reference workloads.
+# The reference workloads.
 PRESETS = {
     "tiny_f32": Workload("tiny_f32 B1 H2 N512 D64 w64/64 G={0}", "f32", 1, 2, 512, 64,
                          64, 64, (), False, (0,), seed=1),
@@ -74,6 +81,9 @@ PRESETS = {
                         1, 16, 8192, 128, 512, 512, (), False, None, 128, seed=5),
     "long_32k": Workload("long_scale bf16 B1 H16 N32768 D128 w512/512 G=128 random", "bf16",
                          1, 16, 32768, 128, 512, 512, (), False, None, 128, seed=5),
+    "longnet_lm": Workload("longnet_lm bf16 B1 H12 N32768 D64 causal w=2K..32K r=1,2,4,6,12", "bf16",
+                           1, 12, 32768, 64, causal=True, seg_w=(2048, 4096, 8192, 16384, 32768),
+                           seg_r=(1, 2, 4, 6, 12), seed=6),
     "long_128k": Workload("long_scale bf16 B1 H16 N131072 D128 w512/512 G=128 random", "bf16",
                           1, 16, 131072, 128, 512, 512, (), False, None, 128, seed=5),
 }

@@ -400,7 +400,7 @@ def pin_longnet_reductions(O, seed=21):
     s = 1 / np.sqrt(D)
     o, l = O.longnet_attn_fwd(q, k, v, [64], [1])
     assert np.abs(o - _sdpa64(q, k, v, s)).max() < 1e-12
-    for w, r in ((12, 3), (16, 4), (8, 2)):
+    for w, r in ((12, 3), (16, 4), (8, 2), (10, 3), (16, 6), (5, 7)):   # r need not divide w; r > w
         o, l = O.longnet_attn_fwd(q, k, v, [w], [r])
         for h in range(H):
             covered = np.zeros(N, dtype=bool)
@@ -412,6 +412,21 @@ def pin_longnet_reductions(O, seed=21):
                 ref = _sdpa64(q[:, h:h + 1, rows], k[:, h:h + 1, rows], v[:, h:h + 1, rows], s)
                 assert np.abs(o[:, h:h + 1, rows] - ref).max() < 1e-12
             assert np.abs(o[:, h, ~covered]).max() == 0.0 and np.isneginf(l[:, h, ~covered]).all()
+
+
+def pin_longnet_rows_vs_full(O, seed=23):
+    """The row-at-a-time LongNet oracle equals the whole-sequence one (several patterns, causal, r not dividing w)."""
+    rng = np.random.default_rng(seed)
+    B, H, N, D = 2, 5, 53, 8
+    q, k, v = (_rand(rng, B, H, N, D) for _ in range(3))
+    rows = [0, 1, 6, 17, 30, 31, 52]
+    for ws, rs, causal in (([8, 24, 53], [1, 3, 7], False), ([10, 32], [2, 5], True), ([4, 64], [6, 4], False)):
+        o, l = O.longnet_attn_fwd(q, k, v, ws, rs, causal)
+        o2, l2 = O.longnet_attn_fwd_rows(q, k, v, ws, rs, causal, rows)
+        assert np.abs(o2 - o[:, :, rows]).max() < 1e-13
+        assert np.array_equal(np.isneginf(l2), np.isneginf(l[:, :, rows]))
+        fin = np.isfinite(l2)
+        assert np.abs(l2[fin] - l[:, :, rows][fin]).max() < 1e-13
 
 
 def pin_longnet_counts(O):
@@ -433,4 +448,5 @@ ALL_PINS = [
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
     pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
     pin_bwd_rows_cols_vs_dense, pin_gproj, pin_golden_longnet, pin_longnet_reductions, pin_longnet_counts,
+    pin_longnet_rows_vs_full,
 ]

@@ -136,6 +136,60 @@ def test_etc_count_pairs(lib):
         assert lg.etc_count_pairs(L, G, r) == int(lg_oracle.etc_mask(L, G, r).sum()) or L > 1000
 
 
+def _i32(*xs):
+    return (ctypes.c_int32 * len(xs))(*xs)
+
+
+def call_longnet(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, dt=lg.LG_BF16, B=1, H=2, N=256, D=64, n=2,
+             w=_i32(64, 256), r=_i32(1, 6), causal=0, scale=0.0, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.lg_longnet_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dt"], a["B"], a["H"], a["N"],
+                                   a["D"], a["n"], ctypes.cast(a["w"], ctypes.c_void_p) if a["w"] else None,
+                                   ctypes.cast(a["r"], ctypes.c_void_p) if a["r"] else None, a["causal"],
+                                   a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), lg.LG_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), lg.LG_ERR_INVALID_ARG),
+    (dict(N=0), lg.LG_ERR_INVALID_ARG),
+    (dict(causal=3), lg.LG_ERR_INVALID_ARG),
+    (dict(n=0), lg.LG_ERR_INVALID_ARG),
+    (dict(w=None), lg.LG_ERR_INVALID_ARG),
+    (dict(w=_i32(64, 0)), lg.LG_ERR_INVALID_ARG),
+    (dict(r=_i32(0, 1)), lg.LG_ERR_INVALID_ARG),
+    (dict(n=17, w=_i32(*([64] * 17)), r=_i32(*([1] * 17))), lg.LG_ERR_UNSUPPORTED),
+    (dict(dt=lg.LG_F32), lg.LG_ERR_UNSUPPORTED),
+    (dict(D=96), lg.LG_ERR_UNSUPPORTED),
+    (dict(ws=None), lg.LG_ERR_WORKSPACE),
+    (dict(wsb=1024), lg.LG_ERR_WORKSPACE),
+])
+def test_longnet_argument_errors_return_before_launch(lib, over, expect):
+    assert call_longnet(lib, **over) == expect
+
+
+def test_longnet_workspace_and_counts(lib):
+    ws_, rs_ = _i32(2048, 4096, 8192, 16384, 32768), _i32(1, 2, 4, 6, 12)
+    size = lib.lg_longnet_attn_fwd_workspace_size(1, 12, 32768, 64, 5, ctypes.cast(ws_, ctypes.c_void_p),
+                                                  ctypes.cast(rs_, ctypes.c_void_p), lg.LG_BF16)
+    # at least one bf16 output and fp32 LSE per pattern kept in strided layout (r divides w, r <= 8)
+    assert size >= 3 * 12 * 32768 * (64 * 2 + 4) and size % 256 == 0
+    assert lib.lg_longnet_attn_fwd_workspace_size(1, 12, 32768, 64, 5, ctypes.cast(ws_, ctypes.c_void_p),
+                                                  ctypes.cast(rs_, ctypes.c_void_p), lg.LG_F32) == 0
+    rng = np.random.default_rng(5)
+    for _ in range(60):
+        N = int(rng.integers(1, 400)); k = int(rng.integers(1, 5))
+        ws = [int(x) for x in rng.integers(1, 300, size=k)]; rs = [int(x) for x in rng.integers(1, 14, size=k)]
+        causal = bool(rng.integers(0, 2)); h = int(rng.integers(0, 20))
+        assert lg.longnet_count_pairs(N, ws, rs, causal, h) == lg_oracle.longnet_count_pairs(N, ws, rs, causal, h)
+    for h in range(12):
+        assert lg.longnet_count_pairs(32768, list(ws_), list(rs_), True, h) == \
+            lg_oracle.longnet_count_pairs(32768, list(ws_), list(rs_), True, h)
+    with pytest.raises(ValueError):
+        lg.longnet_count_pairs(100, [0], [1], False, 0)
+
+
 def test_count_pairs_rejects_bad_lists(lib):
     with pytest.raises(ValueError):
         lg.count_pairs(10, 1, 1, 1, False, [3, 3])
