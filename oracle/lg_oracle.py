@@ -26,6 +26,10 @@ Sources (each function names the passage it follows):
   Sparse Mechanism": g2g, g2l and l2g are full; l2l is the band |i - j| <= r
   clamped to valid indices; g2g+g2l share one softmax and l2g+l2l share another
   ("Softmax unification").
+* ETC page, "Relative Position Encoding" and the four pieces' logits of
+  "Global-Local Attention": a learnable vector a^K_l per relation label and
+  head is added to the key, e_ij = x_i W^Q (x_j W^K + a^K_ij)^T / sqrt(d_z) -
+  (1 - M_ij) C with per-instance binary masks M and C = 10000.
 * "LONGNET: Scaling Transformers to 1,000,000,000 Tokens" (arXiv 2307.02486),
   commentary page, section 3.4, "Standard Self-Attention and Sparse Attention"
   (a binary mask S sends disallowed logits to -inf), "Dilated Attention: Core
@@ -303,6 +307,134 @@ def etc_attn_fwd_rows(q_l, k_l, v_l, q_g, k_g, v_g, radius, long_rows, scale=Non
                 row_mask = np.concatenate([np.ones(G, bool), np.abs(j - i) <= radius])
                 o, l, _ = masked_attention(np.asarray(q_l[b, h, i], np.float64)[None, :], kk, vv, row_mask[None, :], s)
                 out_l[b, h, r], lse_l[b, h, r] = o[0], l[0]
+    return out_l, out_g, lse_l, lse_g
+
+
+# --------------------------------------------------------------------------
+# ETC structured attention: relative-position labels and per-instance masks
+# --------------------------------------------------------------------------
+
+ETC_MASK_C = 10000.0   # ETC page, "Global-Local Attention": C = 10000
+
+
+def etc_dense_codes(L, G, radius, code_l2l=None, code_l2g=None, code_g2l=None, code_g2g=None):
+    """One instance's per-pair codes over the concatenation [global; long], uint8 [G+L, G+L].
+
+    A code byte holds the relative-position label of the edge i -> j in bits
+    0..6 and 1 - M_ij (1: blocked by the instance mask) in bit 7.  The four
+    pieces come as code_g2g [G, G], code_g2l [G, L], code_l2g [L, G] and
+    code_l2l [L, 2 radius + 1] (entry [i, t + radius] for the long key j = i + t);
+    a piece given as None has code 0 on every edge (label 0, allowed).  Edges
+    outside the l2l band keep code 0 here; they are not part of any softmax.
+    """
+    n = G + L
+    codes = np.zeros((n, n), dtype=np.uint8)
+    if code_g2g is not None:
+        codes[:G, :G] = np.asarray(code_g2g, dtype=np.uint8)
+    if code_g2l is not None:
+        codes[:G, G:] = np.asarray(code_g2l, dtype=np.uint8)
+    if code_l2g is not None:
+        codes[G:, :G] = np.asarray(code_l2g, dtype=np.uint8)
+    if code_l2l is not None:
+        c = np.asarray(code_l2l, dtype=np.uint8)
+        for t in range(-radius, radius + 1):
+            i = np.arange(max(0, -t), min(L, L - t))
+            codes[G + i, G + i + t] = c[i, t + radius]
+    return codes
+
+
+def _etc_struct_row_block(qq, kk, vv, member, codes, rel_k_h, s):
+    """Softmax rows of e_ij = s q_i (k_j + a_label)^T - C (1 - M_ij) over the member keys."""
+    logits = s * (qq @ kk.T)
+    lab = (codes & 0x7F).astype(np.int64)
+    if rel_k_h is not None:
+        qa = qq @ np.asarray(rel_k_h, np.float64).T              # [rows, V]: q_i . a_l for every label
+        if lab.size and lab[member].max(initial=0) >= qa.shape[1]:
+            raise ValueError("a label is outside the relative-position vocabulary")
+        logits = logits + s * np.take_along_axis(qa, np.minimum(lab, qa.shape[1] - 1), axis=1)
+    logits = logits - ETC_MASK_C * ((codes >> 7) & 1)
+    logits = np.where(member, logits, -np.inf)
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    den = e.sum(axis=1, keepdims=True)
+    return (e / den) @ vv, (m + np.log(den))[:, 0]
+
+
+def etc_struct_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius, rel_k=None, code_l2l=None, code_l2g=None,
+                        code_g2l=None, code_g2g=None, scale=None):
+    """ETC global-local attention with relative-position labels and per-instance masks.
+
+    ETC page, "Relative Position Encoding" (label l_ij per edge, one learnable
+    vector a^K_l per label and head) and "Global-Local Attention" (the four
+    pieces' logits e_ij = x_i W^Q (x_j W^K + a^K_ij)^T / sqrt(d_z) - (1 - M_ij) C
+    with C = 10000, l2l only for |i - j| <= r clamped to valid indices, and one
+    softmax over g2g + g2l for a global query and one over l2g + l2l for a long
+    query).  Here q_i = x_i W^Q etc. are the inputs, s the scale (1/sqrt(D) by
+    default), and e_ij = s q_i . (k_j + a_l) - C blocked_ij.  rel_k: [H, V, D]
+    (None: no relative term); codes per instance: code_l2l [B, L, 2r+1],
+    code_l2g [B, L, G], code_g2l [B, G, L], code_g2g [B, G, G] (see
+    ``etc_dense_codes``; None: all 0).  Returns (out_l, out_g, lse_l, lse_g), float64.
+    """
+    q_l = np.asarray(q_l, dtype=np.float64)
+    B, H, L, D = q_l.shape
+    G = np.asarray(q_g).shape[2]
+    s = default_scale(D, scale)
+    member = etc_mask(L, G, radius)
+    out_l = np.empty((B, H, L, D)); out_g = np.empty((B, H, G, D))
+    lse_l = np.empty((B, H, L)); lse_g = np.empty((B, H, G))
+    pick = lambda c, b: None if c is None else np.asarray(c)[b]
+    for b in range(B):
+        codes = etc_dense_codes(L, G, radius, pick(code_l2l, b), pick(code_l2g, b), pick(code_g2l, b),
+                                pick(code_g2g, b))
+        for h in range(H):
+            qq = np.concatenate([np.asarray(q_g[b, h], np.float64), q_l[b, h]], axis=0)
+            kk = np.concatenate([np.asarray(k_g[b, h], np.float64), np.asarray(k_l[b, h], np.float64)], axis=0)
+            vv = np.concatenate([np.asarray(v_g[b, h], np.float64), np.asarray(v_l[b, h], np.float64)], axis=0)
+            o, l = _etc_struct_row_block(qq, kk, vv, member, codes, None if rel_k is None else rel_k[h], s)
+            out_g[b, h], out_l[b, h] = o[:G], o[G:]
+            lse_g[b, h], lse_l[b, h] = l[:G], l[G:]
+    return out_l, out_g, lse_l, lse_g
+
+
+def etc_struct_attn_fwd_rows(q_l, k_l, v_l, q_g, k_g, v_g, radius, long_rows, rel_k=None, code_l2l=None,
+                             code_l2g=None, code_g2l=None, code_g2g=None, scale=None):
+    """``etc_struct_attn_fwd`` at sampled long rows (every global row is computed).
+
+    A long row i takes the G global keys (codes code_l2g[b, i]) and the long
+    keys j in [i - r, i + r] inside [0, L) (codes code_l2l[b, i, j - i + r]).
+    Returns (out_l_rows [B, H, R, D], out_g [B, H, G, D], lse_l_rows, lse_g).
+    """
+    q_l = np.asarray(q_l, dtype=np.float64)
+    B, H, L, D = q_l.shape
+    G = np.asarray(q_g).shape[2]
+    s = default_scale(D, scale)
+    long_rows = np.asarray(long_rows, dtype=np.int64)
+    out_l = np.empty((B, H, long_rows.size, D)); lse_l = np.empty((B, H, long_rows.size))
+    out_g = np.empty((B, H, G, D)); lse_g = np.empty((B, H, G))
+    for b in range(B):
+        gcodes = np.zeros((G, G + L), dtype=np.uint8)
+        if code_g2g is not None:
+            gcodes[:, :G] = np.asarray(code_g2g)[b]
+        if code_g2l is not None:
+            gcodes[:, G:] = np.asarray(code_g2l)[b]
+        for h in range(H):
+            a_h = None if rel_k is None else rel_k[h]
+            kk = np.concatenate([np.asarray(k_g[b, h], np.float64), np.asarray(k_l[b, h], np.float64)], axis=0)
+            vv = np.concatenate([np.asarray(v_g[b, h], np.float64), np.asarray(v_l[b, h], np.float64)], axis=0)
+            o, l = _etc_struct_row_block(np.asarray(q_g[b, h], np.float64), kk, vv, np.ones((G, G + L), bool),
+                                         gcodes, a_h, s)
+            out_g[b, h], lse_g[b, h] = o, l
+            for x, i in enumerate(long_rows):
+                lo, hi = max(0, i - radius), min(L - 1, i + radius)
+                keys = np.concatenate([np.arange(G), G + np.arange(lo, hi + 1)])
+                rc = np.zeros(keys.size, dtype=np.uint8)
+                if code_l2g is not None:
+                    rc[:G] = np.asarray(code_l2g)[b, i]
+                if code_l2l is not None:
+                    rc[G:] = np.asarray(code_l2l)[b, i, lo - i + radius: hi - i + radius + 1]
+                o, l = _etc_struct_row_block(q_l[b, h, i][None, :], kk[keys], vv[keys], np.ones((1, keys.size), bool),
+                                             rc[None, :], a_h, s)
+                out_l[b, h, x], lse_l[b, h, x] = o[0], l[0]
     return out_l, out_g, lse_l, lse_g
 
 

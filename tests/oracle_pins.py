@@ -441,6 +441,144 @@ def pin_longnet_counts(O):
         assert O.longnet_count_pairs(N, ws, rs, causal, h) == brute
 
 
+# ---------------------------------------------------------------- ETC structured attention
+
+def pin_golden_etc_struct(O):
+    """Hand-worked ETC relative labels and masks (tests/golden/etc_struct.txt)."""
+    one = lambda *x: np.array(x, dtype=np.float64).reshape(1, 1, -1, 1)
+    q_l, k_l, v_l = one(1, 1), one(0, 0), one(1, 3)
+    q_g, k_g, v_g = one(1), one(0), one(5)
+    rel = np.array([[[0.0], [np.log(2.0)]]])
+    n = 0
+    for case, l2l, l2g, g2l, g2g, row, o_ref, lse_a, lse_b in _golden_lines("etc_struct.txt"):
+        c_l2l = np.array([[int(x) for x in r.split(",")] for r in l2l.split("/")], dtype=np.uint8)[None]
+        c_l2g = np.array([[int(x)] for x in l2g.split("/")], dtype=np.uint8)[None]
+        c_g2l = np.array([[int(x) for x in g2l.split(",")]], dtype=np.uint8)[None]
+        c_g2g = np.array([[int(g2g)]], dtype=np.uint8)[None]
+        out_l, out_g, lse_l, lse_g = O.etc_struct_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, 1, rel, c_l2l, c_l2g,
+                                                           c_g2l, c_g2g, scale=1.0)
+        o, l = (out_g[0, 0, 0, 0], lse_g[0, 0, 0]) if row == "g0" else (out_l[0, 0, int(row[1]), 0],
+                                                                        lse_l[0, 0, int(row[1])])
+        assert abs(o - float(o_ref)) < 1e-12, (case, row, o)
+        assert abs(l - (np.log(float(lse_a)) + float(lse_b))) < 1e-9, (case, row, l)
+        n += 1
+    assert n == 4
+
+
+def _etc_inputs(rng, B=2, H=3, L=23, G=5, D=8):
+    x = lambda *s: _rand(rng, *s)
+    return x(B, H, L, D), x(B, H, L, D), x(B, H, L, D), x(B, H, G, D), x(B, H, G, D), x(B, H, G, D)
+
+
+def _etc_codes(rng, B, L, G, r, V, p_block=0.0):
+    def c(*shape):
+        lab = rng.integers(0, V, size=shape).astype(np.uint8)
+        return lab | ((rng.random(shape) < p_block).astype(np.uint8) << 7)
+    return c(B, L, 2 * r + 1), c(B, L, G), c(B, G, L), c(B, G, G)
+
+
+def pin_etc_struct_reductions(O, seed=31):
+    """No relative term and no blocked edge is plain ETC; one label on every edge of a row shifts
+    its logits by the same s q_i . a_l, which leaves O unchanged and adds s q_i . a_l to LSE."""
+    rng = np.random.default_rng(seed)
+    B, H, L, G, D, r = 2, 3, 23, 5, 8, 3
+    args = _etc_inputs(rng, B, H, L, G, D)
+    ref = O.etc_attn_fwd(*args, r)
+    got = O.etc_struct_attn_fwd(*args, r)
+    assert all(np.abs(a - b).max() < 1e-13 for a, b in zip(ref, got))
+    codes = _etc_codes(rng, B, L, G, r, 4)
+    got = O.etc_struct_attn_fwd(*args, r, np.zeros((H, 4, D)), *codes)
+    assert all(np.abs(a - b).max() < 1e-13 for a, b in zip(ref, got))
+    rel = _rand(rng, H, 4, D)
+    for lab in (0, 3):
+        codes = tuple(np.full_like(c, lab) for c in _etc_codes(rng, B, L, G, r, 4))
+        out_l, out_g, lse_l, lse_g = O.etc_struct_attn_fwd(*args, r, rel, *codes)
+        s = 1 / np.sqrt(D)
+        sh_l = s * np.einsum("bhid,hd->bhi", args[0], rel[:, lab])
+        sh_g = s * np.einsum("bhid,hd->bhi", args[3], rel[:, lab])
+        assert np.abs(out_l - ref[0]).max() < 1e-12 and np.abs(out_g - ref[1]).max() < 1e-12
+        assert np.abs(lse_l - ref[2] - sh_l).max() < 1e-12 and np.abs(lse_g - ref[3] - sh_g).max() < 1e-12
+
+
+def pin_etc_struct_unexpanded_form(O, seed=32):
+    """The page's unexpanded logit q_i (k_j + a_ij)^T, with a per-edge key materialised, blocked
+    edges minus C and the band by -inf, through torch softmax / logsumexp, equals the oracle."""
+    rng = np.random.default_rng(seed)
+    B, H, L, G, D, r, V = 2, 2, 19, 4, 8, 2, 6
+    args = _etc_inputs(rng, B, H, L, G, D)
+    codes = _etc_codes(rng, B, L, G, r, V, p_block=0.2)
+    rel = _rand(rng, H, V, D)
+    s = 0.37
+    out_l, out_g, lse_l, lse_g = O.etc_struct_attn_fwd(*args, r, rel, *codes, scale=s)
+    n = G + L
+    for b in range(B):
+        dense = np.zeros((n, n), dtype=np.int64)   # codes over [global; long], written out piece by piece
+        dense[:G, :G] = codes[3][b]; dense[:G, G:] = codes[2][b]; dense[G:, :G] = codes[1][b]
+        inband = np.zeros((n, n), dtype=bool); inband[:G, :] = True; inband[G:, :G] = True
+        for i in range(L):
+            for j in range(max(0, i - r), min(L, i + r + 1)):
+                dense[G + i, G + j] = codes[0][b, i, j - i + r]; inband[G + i, G + j] = True
+        for h in range(H):
+            q = torch.from_numpy(np.concatenate([args[3][b, h], args[0][b, h]]))
+            k = torch.from_numpy(np.concatenate([args[4][b, h], args[1][b, h]]))
+            v = torch.from_numpy(np.concatenate([args[5][b, h], args[2][b, h]]))
+            lab = torch.from_numpy(dense & 0x7F)
+            key_ij = k[None, :, :] + torch.from_numpy(rel[h])[lab]          # [n, n, D]: k_j + a_label(i, j)
+            e = s * torch.einsum("id,ijd->ij", q, key_ij) - O.ETC_MASK_C * torch.from_numpy((dense >> 7) & 1)
+            e = e.masked_fill(~torch.from_numpy(inband), float("-inf"))
+            o = (torch.softmax(e, dim=1) @ v).numpy()
+            l = torch.logsumexp(e, dim=1).numpy()
+            assert np.abs(o[:G] - out_g[b, h]).max() < 1e-12 and np.abs(o[G:] - out_l[b, h]).max() < 1e-12
+            assert np.abs(l[:G] - lse_g[b, h]).max() < 1e-10 and np.abs(l[G:] - lse_l[b, h]).max() < 1e-10
+
+
+def pin_etc_struct_masks(O, seed=33):
+    """A blocked edge (in a row that keeps an allowed key) weighs exactly nothing: the output equals
+    library SDPA over the allowed edges only.  A row whose every edge is blocked keeps the weights
+    it would have with none blocked (the -C is common to its logits), and its LSE is lower by C."""
+    rng = np.random.default_rng(seed)
+    B, H, L, G, D, r = 1, 2, 21, 4, 8, 3
+    args = _etc_inputs(rng, B, H, L, G, D)
+    codes = list(_etc_codes(rng, B, L, G, r, 1, p_block=0.35))
+    codes[3][0, :, 0] = 0           # every global row keeps global key 0
+    codes[1][0, :, 0] = 0           # every long row keeps global key 0
+    out_l, out_g, lse_l, lse_g = O.etc_struct_attn_fwd(*args, r, None, *codes)
+    n = G + L
+    allowed = O.etc_mask(L, G, r).copy()
+    blocked = (O.etc_dense_codes(L, G, r, codes[0][0], codes[1][0], codes[2][0], codes[3][0]) >> 7) == 1
+    allowed &= ~blocked
+    for h in range(H):
+        q = np.concatenate([args[3][0, h], args[0][0, h]]); k = np.concatenate([args[4][0, h], args[1][0, h]])
+        v = np.concatenate([args[5][0, h], args[2][0, h]])
+        o = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+            attn_mask=torch.from_numpy(allowed)[None], scale=1 / np.sqrt(D))[0].numpy()
+        assert np.abs(o[:G] - out_g[0, h]).max() < 1e-12 and np.abs(o[G:] - out_l[0, h]).max() < 1e-12
+    # long row 7 and global row 1: every edge blocked
+    full = [np.zeros_like(c) for c in codes]
+    blk = [c.copy() for c in full]
+    blk[0][0, 7, :] = 128; blk[1][0, 7, :] = 128; blk[2][0, 1, :] = 128; blk[3][0, 1, :] = 128
+    a = O.etc_struct_attn_fwd(*args, r, None, *full)
+    b = O.etc_struct_attn_fwd(*args, r, None, *blk)
+    assert np.abs(a[0] - b[0]).max() < 1e-9 and np.abs(a[1] - b[1]).max() < 1e-9
+    assert np.abs(b[2][:, :, 7] - a[2][:, :, 7] + O.ETC_MASK_C).max() < 1e-9
+    assert np.abs(b[3][:, :, 1] - a[3][:, :, 1] + O.ETC_MASK_C).max() < 1e-9
+
+
+def pin_etc_struct_rows_vs_full(O, seed=34):
+    """The sampled-row ETC structured oracle equals the whole-instance one."""
+    rng = np.random.default_rng(seed)
+    B, H, L, G, D, r, V = 2, 2, 29, 6, 8, 4, 5
+    args = _etc_inputs(rng, B, H, L, G, D)
+    codes = _etc_codes(rng, B, L, G, r, V, p_block=0.2)
+    rel = _rand(rng, H, V, D)
+    full = O.etc_struct_attn_fwd(*args, r, rel, *codes)
+    rows = [0, 3, 4, 17, 28]
+    got = O.etc_struct_attn_fwd_rows(*args, r, rows, rel, *codes)
+    assert np.abs(got[0] - full[0][:, :, rows]).max() < 1e-12 and np.abs(got[1] - full[1]).max() < 1e-12
+    assert np.abs(got[2] - full[2][:, :, rows]).max() < 1e-10 and np.abs(got[3] - full[3]).max() < 1e-10
+
+
 ALL_PINS = [
     pin_golden_windows, pin_golden_etc, pin_golden_counts, pin_closed_form_counts,
     pin_linear_in_n, pin_full_attention, pin_global_rows_are_full_rows, pin_rows_sum_to_one,
@@ -448,5 +586,6 @@ ALL_PINS = [
     pin_etc_permutation, pin_etc_rows, pin_rows_vs_dense, pin_merge,
     pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_invariants, pin_etc_bwd_finite_differences,
     pin_bwd_rows_cols_vs_dense, pin_gproj, pin_golden_longnet, pin_longnet_reductions, pin_longnet_counts,
-    pin_longnet_rows_vs_full,
+    pin_longnet_rows_vs_full, pin_golden_etc_struct, pin_etc_struct_reductions, pin_etc_struct_unexpanded_form,
+    pin_etc_struct_masks, pin_etc_struct_rows_vs_full,
 ]

@@ -172,12 +172,50 @@ def mut_longnet_plain_average(O):
     O.longnet_pattern = pattern
 
 
+def mut_etc_struct_bias_sign(O):
+    # relative term subtracted instead of added
+    orig = O._etc_struct_row_block
+    O._etc_struct_row_block = lambda qq, kk, vv, member, codes, a, s: orig(
+        qq, kk, vv, member, codes, None if a is None else -np.asarray(a), s)
+
+
+def mut_etc_struct_bias_unscaled(O):
+    # relative term q . a_l without the 1/sqrt(d) of the content term
+    orig = O._etc_struct_row_block
+    O._etc_struct_row_block = lambda qq, kk, vv, member, codes, a, s: orig(
+        qq, kk, vv, member, codes, None if a is None else np.asarray(a) / s, s)
+
+
+def mut_etc_struct_mask_excludes(O):
+    # a blocked edge dropped from the softmax (-inf) instead of -C
+    orig = O._etc_struct_row_block
+
+    def block(qq, kk, vv, member, codes, a, s):
+        return orig(qq, kk, vv, member & ((codes >> 7) == 0), codes & 0x7F, a, s)
+    O._etc_struct_row_block = block
+
+
+def mut_etc_struct_l2l_reversed(O):
+    # the l2l code of key j = i + t read at offset -t
+    orig = O.etc_dense_codes
+    O.etc_dense_codes = lambda L, G, r, c_ll=None, c_lg=None, c_gl=None, c_gg=None: orig(
+        L, G, r, None if c_ll is None else np.asarray(c_ll)[:, ::-1], c_lg, c_gl, c_gg)
+
+
+def mut_etc_struct_g2l_as_l2g(O):
+    # the global rows' long-key codes taken from the transposed long rows' global-key codes
+    orig = O.etc_dense_codes
+    O.etc_dense_codes = lambda L, G, r, c_ll=None, c_lg=None, c_gl=None, c_gg=None: orig(
+        L, G, r, c_ll, c_lg, None if c_lg is None else np.asarray(c_lg).T, c_gg)
+
+
 MUTANTS = [mut_swap_sides, mut_ignore_dilation, mut_span_not_steps, mut_causal_keeps_right,
            mut_no_global_columns, mut_no_scale, mut_transposed_logits, mut_lse_log2,
            mut_etc_radius_off_by_one, mut_etc_no_l2g, mut_closed_form_no_overlap, mut_merge_no_rescale,
            mut_bwd_no_delta, mut_bwd_no_scale, mut_bwd_dk_untransposed, mut_bwd_dv_untransposed,
            mut_gproj_local_keys, mut_bwd_cols_drop_global_rows, mut_longnet_no_offset,
-           mut_longnet_plain_average]
+           mut_longnet_plain_average, mut_etc_struct_bias_sign, mut_etc_struct_bias_unscaled,
+           mut_etc_struct_mask_excludes, mut_etc_struct_l2l_reversed, mut_etc_struct_g2l_as_l2g]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
