@@ -152,6 +152,21 @@ def device_inputs(w, dev, torch):
 def make_call(lg, w, t, torch):
     """Returns f() that runs one forward pass with preallocated outputs and workspace."""
     dev = t["q"].device
+    if w.is_etc and w.name.startswith("etc_struct"):
+        st = workloads.make_etc_structure(w)
+        codes = {n: torch.from_numpy(st[n]).to(dev) for n in ("code_l2l", "code_l2g", "code_g2l", "code_g2g")}
+        rel = st["rel_k"].to(dev)
+        B, H, L, D, G = w.B, w.H, w.N, w.D, w.etc_G
+        out_l, out_g = torch.empty_like(t["q"]), torch.empty_like(t["q_g"])
+        lse_l = torch.empty(B, H, L, device=dev); lse_g = torch.empty(B, H, G, device=dev)
+        ws = torch.empty(lg.etc_struct_attn_fwd_workspace_size(B, H, L, G, D, w.radius, rel.shape[1]),
+                         dtype=torch.uint8, device=dev)
+
+        def f():
+            lg.etc_struct_attn_fwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], w.radius, rel, **codes,
+                                   out_l=out_l, out_g=out_g, lse_l=lse_l, lse_g=lse_g, workspace=ws)
+        t.update(codes)
+        return f, (out_l, out_g, lse_l, lse_g), ws
     if w.is_longnet:
         out = torch.empty_like(t["q"])
         lse = torch.empty(w.B, w.H, w.N, device=dev)
@@ -187,6 +202,8 @@ def make_call(lg, w, t, torch):
 
 
 def launches_per_call(w):
+    if w.is_etc and w.name.startswith("etc_struct"):
+        return 3  # code packing + q . a^K + attention
     if w.is_longnet:
         # per pattern: unit table + tensor-core kernel (+ gather for the packed layout); then the mix
         packed = sum(1 for a, r in zip(w.seg_w, w.seg_r) if not (r <= 8 and a % r == 0))
@@ -397,7 +414,7 @@ def bench_backward(lg, torch, w, t, outs, flush, steps, peaks, peak_kind):
     CUDA events on the current stream, L2 flushed between steps when the
     inputs fit in it.
     """
-    if w.dtype != "bf16" or w.is_longnet:   # no LongNet backward
+    if w.dtype != "bf16" or w.is_longnet or w.name.startswith("etc_struct"):   # no backward for these
         return None
     gen = torch.Generator(device=t["q"].device)
     gen.manual_seed(w.seed + 7919)

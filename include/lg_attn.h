@@ -58,7 +58,7 @@ typedef struct CUstream_st* lg_stream_t;
 
 typedef enum {
   LG_OK = 0,
-  LG_ERR_INVALID_ARG = 1,   /* a pointer, size or value is out of its documented range */
+  LG_ERR_INVALID_ARG = 1,   /* a pointer, size or value is out of its documented range (ETC labels: found on the device) */
   LG_ERR_UNSUPPORTED = 2,   /* valid arguments this build does not run (e.g. bf16 with D not 64/128) */
   LG_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
   LG_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out; outputs are undefined */
@@ -281,6 +281,48 @@ lg_status lg_etc_attn_bwd(const void* q_l, const void* k_l, const void* v_l,
                           void* dq_l, void* dk_l, void* dv_l, void* dq_g, void* dk_g, void* dv_g,
                           lg_dtype dt, int B, int H, int L, int G, int D, int radius, float scale,
                           void* workspace, size_t workspace_bytes, lg_stream_t stream);
+
+/*
+ * ETC global-local attention with relative-position labels and per-instance
+ * masks ("ETC: Encoding Long and Structured Inputs in Transformers", section
+ * 3.4, "Relative Position Encoding" and "Global-Local Attention"): the four
+ * pieces' logits are
+ *   e_ij = s q_i . (k_j + a^K_{h, label_ij}) - C (1 - M_ij),  C = 10000,
+ * with one softmax over g2g + g2l for a global query and one over l2g + l2l
+ * for a long query; l2l only for |i - j| <= radius (clamped to [0, L)).
+ * Each edge carries a code byte: label_ij in bits 0..6, 1 - M_ij in bit 7
+ * (so 0 = label 0, allowed; 128 = label 0, blocked).  A row whose every edge
+ * is blocked keeps the weights it would have with none blocked (C is common
+ * to its logits) and an LSE lower by C, as the formula gives.
+ *
+ *  q_l, k_l, v_l, out_l  device [B, H, L, D];  q_g, k_g, v_g, out_g  device
+ *              [B, H, G, D]; bf16, D in {64, 128}; lse_l [B, H, L], lse_g
+ *              [B, H, G] fp32.  G >= 1.
+ *  rel_k       device [H, n_labels, D] bf16 (a^K per head and label), or NULL
+ *              with n_labels = 0 (no relative term; labels ignored).
+ *  n_labels    0..64.  A label >= n_labels on an edge is reported by
+ *              lg_query_status as LG_ERR_INVALID_ARG (found on the device).
+ *  code_l2l    device uint8 [B, L, 2*radius + 1]: entry [b, i, t + radius] is
+ *              the code of long key j = i + t (entries with j outside [0, L)
+ *              are ignored);  code_l2g [B, L, G];  code_g2l [B, G, L];
+ *              code_g2g [B, G, G].  Any of them may be NULL: code 0 on every
+ *              edge of that piece.  Read during the call only.
+ *  workspace   >= lg_etc_struct_attn_fwd_workspace_size(...) bytes, 256-byte
+ *              aligned: the status word, the codes laid out per (query tile,
+ *              key tile) block, and q . a^K per row and label.
+ * fp32 returns LG_ERR_UNSUPPORTED.  Other arguments, errors and asynchrony as
+ * for lg_etc_attn_fwd.
+ */
+size_t lg_etc_struct_attn_fwd_workspace_size(int B, int H, int L, int G, int D, int radius, int n_labels,
+                                             lg_dtype dt);
+lg_status lg_etc_struct_attn_fwd(const void* q_l, const void* k_l, const void* v_l,
+                                 const void* q_g, const void* k_g, const void* v_g,
+                                 void* out_l, void* out_g, float* lse_l, float* lse_g,
+                                 const void* rel_k, int n_labels,
+                                 const uint8_t* code_l2l, const uint8_t* code_l2g,
+                                 const uint8_t* code_g2l, const uint8_t* code_g2g,
+                                 lg_dtype dt, int B, int H, int L, int G, int D, int radius, float scale,
+                                 void* workspace, size_t workspace_bytes, lg_stream_t stream);
 
 /*
  * LongNet mixture of dilated attentions ("LONGNET: Scaling Transformers to

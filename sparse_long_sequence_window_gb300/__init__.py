@@ -19,6 +19,7 @@ __all__ = [
     "LgError", "load", "attn_fwd", "attn_fwd_host", "etc_attn_fwd", "attn_fwd_workspace_size",
     "attn_bwd", "etc_attn_bwd", "attn_bwd_workspace_size", "etc_attn_bwd_workspace_size",
     "longnet_attn_fwd", "longnet_count_pairs", "longnet_attn_fwd_workspace_size",
+    "etc_struct_attn_fwd", "etc_struct_attn_fwd_workspace_size",
     "etc_attn_fwd_workspace_size", "query_status", "count_pairs", "etc_count_pairs",
     "profile_begin", "profile_end", "status_string", "debug_timeout_test", "LIB_PATH",
 ]
@@ -83,6 +84,10 @@ def load() -> ctypes.CDLL:
     lib.lg_longnet_attn_fwd.argtypes = [vp] * 5 + [i32] * 6 + [vp, vp, i32, f32, vp, sz, vp]
     lib.lg_longnet_count_pairs.restype = ctypes.c_int64
     lib.lg_longnet_count_pairs.argtypes = [i32, i32, vp, vp, i32, i32]
+    lib.lg_etc_struct_attn_fwd_workspace_size.restype = sz
+    lib.lg_etc_struct_attn_fwd_workspace_size.argtypes = [i32] * 8
+    lib.lg_etc_struct_attn_fwd.restype = i32
+    lib.lg_etc_struct_attn_fwd.argtypes = [vp] * 11 + [i32] + [vp] * 4 + [i32] * 7 + [f32, vp, sz, vp]
     lib.lg_debug_timeout_test.restype = i32
     lib.lg_debug_timeout_test.argtypes = [i32, ctypes.c_longlong]
     lib.lg_profile_begin.restype = i32
@@ -403,6 +408,66 @@ def etc_attn_bwd(q_l, k_l, v_l, q_g, k_g, v_g, out_l, out_g, lse_l, lse_g, dout_
         _keep_for(stream, ws)
     etc_attn_bwd.last_workspace = ws
     return tuple(grads)
+
+
+def etc_struct_attn_fwd(q_l, k_l, v_l, q_g, k_g, v_g, radius, rel_k=None, code_l2l=None, code_l2g=None,
+                        code_g2l=None, code_g2g=None, scale: Optional[float] = None, out_l=None, out_g=None,
+                        lse_l=None, lse_g=None, workspace=None, stream=None):
+    """ETC attention with relative-position labels and per-instance masks (lg_etc_struct_attn_fwd).
+
+    Long tensors [B, H, L, D], global [B, H, G, D] (bf16 CUDA); rel_k [H, V, D] or None; codes uint8
+    CUDA tensors code_l2l [B, L, 2r+1], code_l2g [B, L, G], code_g2l [B, G, L], code_g2g [B, G, G]
+    (label in bits 0..6, 128 = blocked) or None.  Returns (out_l, out_g, lse_l, lse_g)."""
+    import torch
+    lib = load()
+    if q_l.dim() != 4 or not q_l.is_cuda:
+        raise ValueError("q_l must be a CUDA tensor [B, H, L, D]")
+    _same(q_l, "k_l", k_l, v_l)
+    _same(q_g, "k_g", k_g, v_g)
+    B, H, L, D = q_l.shape
+    G = q_g.shape[2]
+    if tuple(q_g.shape) != (B, H, G, D) or q_g.dtype != q_l.dtype or q_g.device != q_l.device:
+        raise ValueError("q_g must be [B, H, G, D] with q_l's dtype and device")
+    dt = _dtype_code(q_l)
+    n_labels = 0
+    if rel_k is not None:
+        if rel_k.dim() != 3 or rel_k.shape[0] != H or rel_k.shape[2] != D or rel_k.dtype != q_l.dtype \
+                or rel_k.device != q_l.device or not rel_k.is_contiguous():
+            raise ValueError("rel_k must be a contiguous [H, V, D] tensor of q_l's dtype and device")
+        n_labels = int(rel_k.shape[1])
+    shapes = {"code_l2l": (B, L, 2 * int(radius) + 1), "code_l2g": (B, L, G), "code_g2l": (B, G, L),
+              "code_g2g": (B, G, G)}
+    codes = {"code_l2l": code_l2l, "code_l2g": code_l2g, "code_g2l": code_g2l, "code_g2g": code_g2g}
+    for name, c in codes.items():
+        if c is not None and (tuple(c.shape) != shapes[name] or c.dtype != torch.uint8 or c.device != q_l.device
+                              or not c.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous uint8 tensor {shapes[name]} on {q_l.device}")
+    out_l = torch.empty_like(q_l) if out_l is None else out_l
+    out_g = torch.empty_like(q_g) if out_g is None else out_g
+    lse_l = torch.empty((B, H, L), dtype=torch.float32, device=q_l.device) if lse_l is None else lse_l
+    lse_g = torch.empty((B, H, G), dtype=torch.float32, device=q_l.device) if lse_g is None else lse_g
+    _check_out(out_l, q_l.shape, q_l.dtype, q_l.device, "out_l")
+    _check_out(out_g, q_g.shape, q_g.dtype, q_g.device, "out_g")
+    _check_out(lse_l, (B, H, L), torch.float32, q_l.device, "lse_l")
+    _check_out(lse_g, (B, H, G), torch.float32, q_l.device, "lse_g")
+    need = int(lib.lg_etc_struct_attn_fwd_workspace_size(B, H, L, G, D, int(radius), n_labels, dt))
+    if need == 0:
+        raise NotImplementedError("lg_etc_struct_attn_fwd: unsupported shape, dtype or label count")
+    ws = _workspace(need, q_l.device, workspace)
+    cp = [None if c is None else _ptr(c) for c in codes.values()]
+    st = lib.lg_etc_struct_attn_fwd(_ptr(q_l), _ptr(k_l), _ptr(v_l), _ptr(q_g), _ptr(k_g), _ptr(v_g), _ptr(out_l),
+                                    _ptr(out_g), _ptr(lse_l), _ptr(lse_g), None if rel_k is None else _ptr(rel_k),
+                                    n_labels, *cp, dt, B, H, L, G, D, int(radius),
+                                    float(scale) if scale else 0.0, ws.data_ptr(), _nbytes(ws), _stream(stream))
+    _check(st, "lg_etc_struct_attn_fwd")
+    if workspace is None:
+        _keep_for(stream, ws)
+    etc_struct_attn_fwd.last_workspace = ws
+    return out_l, out_g, lse_l, lse_g
+
+
+def etc_struct_attn_fwd_workspace_size(B, H, L, G, D, radius, n_labels, dtype=LG_BF16) -> int:
+    return int(load().lg_etc_struct_attn_fwd_workspace_size(B, H, L, G, D, radius, n_labels, int(dtype)))
 
 
 def longnet_attn_fwd(q, k, v, seg_w: Sequence[int], seg_r: Sequence[int], causal: bool = False,

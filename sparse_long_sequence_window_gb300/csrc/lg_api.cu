@@ -584,6 +584,7 @@ lg_status lg_query_status(const void* workspace, lg_stream_t stream_) {
   if (word & ST_INTERNAL) return LG_ERR_CUDA;
   if (word & ST_TIMEOUT) return LG_ERR_TIMEOUT;
   if (word & ST_GLOBAL_IDX) return LG_ERR_GLOBAL_IDX;
+  if (word & ST_BAD_CODE) return LG_ERR_INVALID_ARG;
   return LG_OK;
 }
 

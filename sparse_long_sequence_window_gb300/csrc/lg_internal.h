@@ -20,6 +20,7 @@ enum : int {
   ST_GLOBAL_IDX = 1 << 0,
   ST_TIMEOUT = 1 << 1,
   ST_INTERNAL = 1 << 2,   // an internal invariant failed on the device; the work was abandoned
+  ST_BAD_CODE = 1 << 3,   // an ETC relative-position label outside the vocabulary
 };
 
 constexpr size_t kStatusBytes = 256;     // status area at the head of every workspace

@@ -81,6 +81,8 @@ PRESETS = {
                         1, 16, 8192, 128, 512, 512, (), False, None, 128, seed=5),
     "long_32k": Workload("long_scale bf16 B1 H16 N32768 D128 w512/512 G=128 random", "bf16",
                          1, 16, 32768, 128, 512, 512, (), False, None, 128, seed=5),
+    "etc_struct": Workload("etc_struct bf16 B2 H12 L4096 G256 D64 r84, 32 relation labels, 4 documents, hard g2l",
+                           "bf16", 2, 12, 4096, 64, etc_G=256, radius=84, seed=7),
     "longnet_lm": Workload("longnet_lm bf16 B1 H12 N32768 D64 causal w=2K..32K r=1,2,4,6,12", "bf16",
                            1, 12, 32768, 64, causal=True, seg_w=(2048, 4096, 8192, 16384, 32768),
                            seg_r=(1, 2, 4, 6, 12), seed=6),
@@ -142,6 +144,76 @@ def make_grad_out(w: Workload) -> dict:
     if w.is_etc:
         out["dout_g"] = _round(rng.standard_normal((w.B, w.H, w.etc_G, w.D), dtype=np.float32), w.dtype)
     return out
+
+
+# Relation labels of the structured ETC workload (a vocabulary of 32): the
+# clipped relative distances -k..k (k = 12) within a sentence, then a few
+# structural relations.
+ETC_REL_K = 12
+ETC_LABEL_OTHER_SENTENCE = 2 * ETC_REL_K + 1   # l2l: key in another sentence
+ETC_LABEL_OWN_SUMMARY = 26                     # l2g: the summary token of the query's sentence
+ETC_LABEL_OTHER_SUMMARY = 27                   # l2g: another sentence's summary token
+ETC_LABEL_CLS = 28                             # edges to or from the global CLS token (global 0)
+ETC_LABEL_OWN_TOKEN = 29                       # g2l: a token of the summary's own sentence
+ETC_LABEL_OTHER_TOKEN = 30                     # g2l: a token of another sentence
+ETC_N_LABELS = 32
+
+
+def make_etc_structure(w: Workload, n_docs: int = 4, hard_g2l: bool = True) -> dict:
+    """Per-instance structure for ETC attention with relation labels and masks, following the ETC
+    page's recipe for long documents: the long input split into sentences, one summary token per
+    sentence in the global input after a CLS token (global 0), several documents per instance.
+
+    Sentence lengths are drawn from ``default_rng(seed + 5557)`` (uniform in [4, 2 L / (G - 1)],
+    the last sentence taking the rest); sentences are dealt to ``n_docs`` documents in order.  Codes
+    (uint8, label in bits 0..6, 128 = blocked):
+      * l2l: clip(j - i, -k, k) + k inside a sentence, ETC_LABEL_OTHER_SENTENCE across sentences;
+        blocked across documents;
+      * l2g: CLS label to global 0, own / other summary label; blocked to summaries of other documents;
+      * g2l: CLS label from global 0; own / other token label; with hard_g2l a summary token is
+        blocked from every token outside its sentence, else only from other documents;
+      * g2g: clip(j - i, -k, k) + k; blocked between summaries of different documents.
+    rel_k [H, 32, D] is iid N(0, 1) from the same generator, rounded like the inputs.
+    Returns numpy arrays code_l2l [B, L, 2r+1], code_l2g [B, L, G], code_g2l [B, G, L],
+    code_g2g [B, G, G], rel_k, and the per-instance sentence and document ids.
+    """
+    B, H, L, G, D, r = w.B, w.H, w.N, w.etc_G, w.D, w.radius
+    k = ETC_REL_K
+    rng = np.random.default_rng(w.seed + 5557)
+    n_sent = max(1, G - 1)
+    c_ll = np.zeros((B, L, 2 * r + 1), np.uint8); c_lg = np.zeros((B, L, G), np.uint8)
+    c_gl = np.zeros((B, G, L), np.uint8); c_gg = np.zeros((B, G, G), np.uint8)
+    sent_ids = np.zeros((B, L), np.int64); doc_of_sent = np.zeros((B, n_sent), np.int64)
+    for b in range(B):
+        hi = max(4, 2 * L // n_sent)
+        lens = rng.integers(4, hi + 1, size=n_sent)
+        starts = np.minimum(np.concatenate([[0], np.cumsum(lens)[:-1]]), L)
+        sent = np.searchsorted(starts, np.arange(L), side="right") - 1    # sentence of each token
+        doc_s = (np.arange(n_sent) * n_docs) // n_sent                    # document of each sentence
+        doc_t = doc_s[sent]
+        sent_ids[b], doc_of_sent[b] = sent, doc_s
+        i = np.arange(L)[:, None]; t = np.arange(-r, r + 1)[None, :]; j = i + t
+        jc = np.clip(j, 0, L - 1)
+        same_s = sent[i[:, 0]][:, None] == sent[jc]
+        lab = np.where(same_s, np.clip(t, -k, k) + k, ETC_LABEL_OTHER_SENTENCE)
+        blk = doc_t[i[:, 0]][:, None] != doc_t[jc]
+        c_ll[b] = (lab | (blk.astype(np.int64) << 7)).astype(np.uint8)
+        gs = np.arange(G) - 1                                             # sentence of each global (-1: CLS)
+        own = sent[:, None] == gs[None, :]
+        lab = np.where(own, ETC_LABEL_OWN_SUMMARY, ETC_LABEL_OTHER_SUMMARY); lab[:, 0] = ETC_LABEL_CLS
+        gdoc = np.where(gs >= 0, doc_s[np.clip(gs, 0, n_sent - 1)], -1)
+        blk = (gdoc[None, :] != doc_t[:, None]) & (gs[None, :] >= 0)
+        c_lg[b] = (lab | (blk.astype(np.int64) << 7)).astype(np.uint8)
+        lab = np.where(own.T, ETC_LABEL_OWN_TOKEN, ETC_LABEL_OTHER_TOKEN); lab[0, :] = ETC_LABEL_CLS
+        blk = (~own.T if hard_g2l else (gdoc[:, None] != doc_t[None, :])) & (gs[:, None] >= 0)
+        c_gl[b] = (lab | (blk.astype(np.int64) << 7)).astype(np.uint8)
+        tg = np.arange(G)[None, :] - np.arange(G)[:, None]
+        lab = np.clip(tg, -k, k) + k
+        blk = (gdoc[:, None] != gdoc[None, :]) & (gs[:, None] >= 0) & (gs[None, :] >= 0)
+        c_gg[b] = (lab | (blk.astype(np.int64) << 7)).astype(np.uint8)
+    rel = _round(rng.standard_normal((H, ETC_N_LABELS, D), dtype=np.float32), w.dtype)
+    return {"code_l2l": c_ll, "code_l2g": c_lg, "code_g2l": c_gl, "code_g2g": c_gg, "rel_k": rel,
+            "sent_ids": sent_ids, "doc_of_sent": doc_of_sent}
 
 
 def make_global_projections(w: Workload) -> dict:

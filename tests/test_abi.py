@@ -190,6 +190,43 @@ def test_longnet_workspace_and_counts(lib):
         lg.longnet_count_pairs(100, [0], [1], False, 0)
 
 
+def call_etc_struct(lib, **over):
+    a = dict(t=[FAKE] * 10, rel=FAKE, V=8, codes=[FAKE, None, FAKE, None], dt=lg.LG_BF16, B=1, H=2, L=300, G=4,
+             D=64, r=8, scale=0.0, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.lg_etc_struct_attn_fwd(*a["t"], a["rel"], a["V"], *a["codes"], a["dt"], a["B"], a["H"], a["L"],
+                                      a["G"], a["D"], a["r"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(t=[None] + [FAKE] * 9), lg.LG_ERR_INVALID_ARG),
+    (dict(t=[FAKE] * 7 + [FAKE + 8] + [FAKE] * 2), lg.LG_ERR_INVALID_ARG),
+    (dict(t=[FAKE] * 9 + [FAKE + 2]), lg.LG_ERR_INVALID_ARG),
+    (dict(G=0), lg.LG_ERR_INVALID_ARG),
+    (dict(r=-1), lg.LG_ERR_INVALID_ARG),
+    (dict(rel=None), lg.LG_ERR_INVALID_ARG),          # labels without vectors
+    (dict(V=0), lg.LG_ERR_INVALID_ARG),               # vectors without labels
+    (dict(V=65), lg.LG_ERR_UNSUPPORTED),
+    (dict(dt=lg.LG_F32), lg.LG_ERR_UNSUPPORTED),
+    (dict(D=32), lg.LG_ERR_UNSUPPORTED),
+    (dict(ws=None), lg.LG_ERR_WORKSPACE),
+    (dict(wsb=4096), lg.LG_ERR_WORKSPACE),
+])
+def test_etc_struct_argument_errors_return_before_launch(lib, over, expect):
+    assert call_etc_struct(lib, **over) == expect
+
+
+def test_etc_struct_workspace_size(lib):
+    f = lib.lg_etc_struct_attn_fwd_workspace_size
+    base = f(2, 12, 4096, 256, 64, 84, 0, lg.LG_BF16)
+    # one 16 KB code block per (query tile, key tile) visited: per instance 2 global query tiles x
+    # (2 + 32) key tiles and 32 long query tiles x (3 band + 2 global) key tiles
+    assert base >= 256 + 2 * (2 * 34 + 32 * 5) * 16384
+    # q . a^K per row and label: 4 bytes per (head, row, label)
+    assert f(2, 12, 4096, 256, 64, 84, 32, lg.LG_BF16) - base >= 2 * 12 * (4096 + 256) * 32 * 4
+    assert f(2, 12, 4096, 256, 64, 84, 0, lg.LG_F32) == 0 and f(2, 12, 4096, 0, 64, 84, 0, lg.LG_BF16) == 0
+
+
 def test_count_pairs_rejects_bad_lists(lib):
     with pytest.raises(ValueError):
         lg.count_pairs(10, 1, 1, 1, False, [3, 3])
