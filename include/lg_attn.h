@@ -300,7 +300,8 @@ lg_status lg_etc_attn_bwd(const void* q_l, const void* k_l, const void* v_l,
  *              [B, H, G] fp32.  G >= 1.
  *  rel_k       device [H, n_labels, D] bf16 (a^K per head and label), or NULL
  *              with n_labels = 0 (no relative term; labels ignored).
- *  n_labels    0..64.  A label >= n_labels on an edge is reported by
+ *  n_labels    0..64 for D = 64, 0..40 for D = 128 (LG_ERR_UNSUPPORTED
+ *              above).  A label >= n_labels on an edge is reported by
  *              lg_query_status as LG_ERR_INVALID_ARG (found on the device).
  *  code_l2l    device uint8 [B, L, 2*radius + 1]: entry [b, i, t + radius] is
  *              the code of long key j = i + t (entries with j outside [0, L)
@@ -308,8 +309,8 @@ lg_status lg_etc_attn_bwd(const void* q_l, const void* k_l, const void* v_l,
  *              code_g2g [B, G, G].  Any of them may be NULL: code 0 on every
  *              edge of that piece.  Read during the call only.
  *  workspace   >= lg_etc_struct_attn_fwd_workspace_size(...) bytes, 256-byte
- *              aligned: the status word, the codes laid out per (query tile,
- *              key tile) block, and q . a^K per row and label.
+ *              aligned: the status word and the codes laid out per (query
+ *              tile, key tile) block (q . a^K is formed in tensor memory).
  * fp32 returns LG_ERR_UNSUPPORTED.  Other arguments, errors and asynchrony as
  * for lg_etc_attn_fwd.
  */

@@ -10,25 +10,29 @@
 // long query; per-instance binary masks M).
 //
 // Each edge carries one code byte: the label in bits 0..6 and 1 - M_ij in
-// bit 7.  Three kernels:
+// bit 7.  Two kernels:
 //  * es_pack_kernel lays the caller's four code arrays out as one 128 x 128
 //    byte block per (query tile, key tile) in the order the attention kernel
 //    visits them (rows of 128 bytes, 16-byte chunks XOR-swizzled by the row,
 //    so that the softmax threads read them from shared memory without bank
 //    conflicts), and checks the labels against the vocabulary;
-//  * es_qa_kernel computes qa_il = s log2(e) q_i . a^K_l for every query row
-//    and label, stored label-major per 128-row tile (qa[l][row]), so that a
-//    softmax thread gathers its row's value of any label conflict-free;
 //  * es_attn_kernel: one CTA per (instance, head, 128-row query tile) with
-//    warp 0 loading tiles (TMA for q, k, v; bulk copies for the code blocks
-//    and qa), warp 1 owning tensor memory and issuing the MMAs from one lane,
-//    and warps 4..7 the softmax (one thread per row).  S = Q K^T lands in one
+//    warp 0 loading tiles (TMA for q, k, v and a^K; bulk copies for the code
+//    blocks), warp 1 owning tensor memory and issuing the MMAs from one lane,
+//    and warps 4..11 the softmax: two threads per row, one per 64-column half
+//    of the tile, which exchange their tile maxima through shared memory
+//    (two warps per sub-partition, half the serial work each).  S = Q K^T lands in one
 //    of two TMEM buffers, so the QK of tile j + 2 is issued right after the PV
 //    of tile j and runs while the softmax works on tile j + 1; the softmax adds
 //    qa[label], applies the blocked edges' -C (exactly, see the softmax),
 //    keeps a running maximum (O rescaled in TMEM only when it grows by more
 //    than 2^8), writes P (bf16) over its S and the MMA warp accumulates
-//    O += P V with P read from TMEM.
+//    O += P V with P read from TMEM.  With a relative term, one more MMA per
+//    unit gives qa_il = q_i . a^K_l for the tile's rows and every label (the
+//    appendix's q a^K table, M = 128, N = labels rounded up to 16, K = D); the
+//    softmax threads move it, times s log2(e), from TMEM into a shared-memory
+//    table stored label-major ([label][row]), so a thread gathers its row's
+//    value of any label without bank conflicts.
 // Long query tiles visit the band key tiles [t0 - r, t0 + 127 + r] and then
 // the global key tiles; global query tiles the global key tiles and then every
 // long key tile.  Global query tiles come first in the grid (they are the
@@ -44,7 +48,7 @@
 namespace lg {
 namespace {
 
-constexpr int kEsThreads = 256;
+constexpr int kEsThreads = 384;   // warp 0 loads, warp 1 MMA, warps 4..11 softmax (two column halves)
 constexpr int kEsMaxDevices = 64;
 constexpr int kEsMaxLabels = 64;
 constexpr int kCodeTile = 128 * 128;                // bytes of one (query tile, key tile) code block
@@ -105,25 +109,26 @@ struct EsPackParams {
   int* status;
 };
 
-// One thread per 16-byte chunk of a block (16 edges of one row).
+// One thread per 16-byte chunk of a block (16 edges of one row); four CTAs of
+// 256 threads per block, so the block index is blockIdx.x / 4.
 __global__ void __launch_bounds__(256) es_pack_kernel(const EsPackParams p) {
   const EsGeom& g = p.g;
-  const long long total = static_cast<long long>(g.B) * g.blocks_per_b * (kCodeTile / 16);
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int chunk = static_cast<int>(idx % (kCodeTile / 16));
-    const long long blk = idx / (kCodeTile / 16);
-    const int b = static_cast<int>(blk / g.blocks_per_b);
-    long long rem = blk % g.blocks_per_b;
+  {
+    const int blk = static_cast<int>(blockIdx.x >> 2);
+    const int chunk = static_cast<int>((blockIdx.x & 3) * 256 + threadIdx.x);
+    const long long idx = static_cast<long long>(blk) * (kCodeTile / 16) + chunk;
+    const int bpb = static_cast<int>(g.blocks_per_b);
+    const int b = blk / bpb;
+    int rem = blk - b * bpb;
     const int row = chunk >> 3;
     const int k = (chunk & 7) ^ (row & 7);   // logical 16-column group stored in this physical chunk
-    const bool glob = rem < static_cast<long long>(g.n_gq) * g.steps_g;
+    const bool glob = rem < g.n_gq * g.steps_g;
     int tq, j;
     if (glob) {
-      tq = static_cast<int>(rem / g.steps_g); j = static_cast<int>(rem % g.steps_g);
+      tq = rem / g.steps_g; j = rem - tq * g.steps_g;
     } else {
-      rem -= static_cast<long long>(g.n_gq) * g.steps_g;
-      tq = static_cast<int>(rem / g.steps_l); j = static_cast<int>(rem % g.steps_l);
+      rem -= g.n_gq * g.steps_g;
+      tq = rem / g.steps_l; j = rem - tq * g.steps_l;
     }
     // piece: 0 none, 1 l2l, 2 l2g, 3 g2l, 4 g2g; key0: first key of the tile
     int piece = 0, key0 = 0, key_n = 0;
@@ -164,62 +169,20 @@ __global__ void __launch_bounds__(256) es_pack_kernel(const EsPackParams p) {
   }
 }
 
-// ---------------------------------------------------------------- qa = s log2(e) q . a^K_l
-
-struct EsQaParams {
-  const __nv_bfloat16* q_l;   // [BH, L, D]
-  const __nv_bfloat16* q_g;   // [BH, G, D]
-  const __nv_bfloat16* rel;   // [H, V, D]
-  float* qa;                  // [BH][n_gq + n_lq][V][128]
-  int H, L, G, D, V, n_gq, n_lq;
-  long long total;            // BH * (n_gq + n_lq) * V * 128
-  float c;
-};
-
-__global__ void __launch_bounds__(256) es_qa_kernel(const EsQaParams p) {
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < p.total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(idx & 127);
-    long long t = idx >> 7;
-    const int l = static_cast<int>(t % p.V); t /= p.V;
-    const int tile = static_cast<int>(t % (p.n_gq + p.n_lq));
-    const long long bh = t / (p.n_gq + p.n_lq);
-    const bool glob = tile < p.n_gq;
-    const int row = (glob ? tile : tile - p.n_gq) * 128 + r;
-    float acc = 0.f;
-    if (row < (glob ? p.G : p.L)) {
-      const uint4* q = reinterpret_cast<const uint4*>(glob ? p.q_g + (bh * p.G + row) * p.D : p.q_l + (bh * p.L + row) * p.D);
-      const uint4* a = reinterpret_cast<const uint4*>(p.rel + (static_cast<size_t>(bh % p.H) * p.V + l) * p.D);
-      for (int x = 0; x < p.D / 8; ++x) {
-        const uint4 qv = __ldg(q + x), av = __ldg(a + x);
-        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, aw[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[e]));
-          const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
-          acc = fmaf(qf.x, af.x, acc);
-          acc = fmaf(qf.y, af.y, acc);
-        }
-      }
-    }
-    p.qa[idx] = acc * p.c;
-  }
-}
-
 // ---------------------------------------------------------------- attention
 
 struct EsParams {
   CUtensorMap mQl, mKl, mVl, mQg, mKg, mVg;   // {D, rows, BH}, 128-row boxes
   CUtensorMap sOl, sOg;                       // output stores, 32-row boxes
   EsGeom g;
+  CUtensorMap mA;                             // a^K viewed as {D, V, H}, boxes of Vp rows
   const uint8_t* codes;
-  const float* qa;
   float* lse_l;
   float* lse_g;
   int* status;
   long long wait_cap;
   int withhold;
-  int V;
+  int V, Vp;                                  // labels, and labels rounded up to 16 (the MMA's N)
   float scale_log2;
 };
 
@@ -228,9 +191,11 @@ struct EsCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kStage = 2 * kTile + kCodeTile;   // K, V, code block
   static constexpr int kOffStage = kTile;                // after Q
-  static constexpr int kOffQa = kTile + 2 * kStage;
-  static constexpr int kOffMisc = kOffQa + kEsMaxLabels * 512;
-  static constexpr int kSmem = kOffMisc + 256 + 1024;    // + alignment slack
+  static constexpr int kOffMisc = kTile + 2 * kStage;    // barriers, then the softmax halves' exchange area
+  static constexpr int kMisc = 8192;
+  static constexpr int kOffQa = kOffMisc + kMisc;        // q . a^K of the tile's rows, [label][row]
+  static constexpr int kMaxLabels = D == 64 ? kEsMaxLabels : 40;   // what fits in 227 KB next to D = 128 tiles
+  static constexpr int kSmem = kOffQa + kMaxLabels * 512 + 1024;   // + alignment slack
 };
 
 template <int D>
@@ -250,13 +215,18 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
   auto stage = [&](int st) { return sb + C::kOffStage + st * C::kStage; };
   unsigned char* misc = smem + C::kOffMisc;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
-  enum { B_QF = 0, B_KVF = 1, B_KVE = 3, B_SF = 5, B_PF = 7, B_PV = 9, B_DONE = 10, NB = 11 };
+  enum { B_QF = 0, B_KVF = 1, B_KVE = 3, B_SF = 5, B_PF = 7, B_PV = 9, B_DONE = 10, B_QAF = 11, NB = 12 };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
+  // exchange between the two column halves of a row: tile maxima [parity][half][row] (allowed
+  // edges, all edges), and the final partial sums [half][row]
+  float* x_allowed = reinterpret_cast<float*>(misc + 256);
+  float* x_all = x_allowed + 512;
+  float* x_sum = x_all + 512;
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) mbar_init(bar(i), (i == B_PF || i == B_PF + 1) ? 128 : 1);
+    for (int i = 0; i < NB; ++i) mbar_init(bar(i), (i == B_PF || i == B_PF + 1) ? 256 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -287,22 +257,25 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
   if (!glob) es_band(g.L, g.r, tq, band_lo, n_band);
   const int n_steps = glob ? g.steps_g : n_band + g.n_gq;
   const uint8_t* codes = p.codes + es_block(g, b, glob, tq) * kCodeTile;
-  constexpr uint32_t kTS = 0, kTO = 256;   // S buffers at columns 0 and 128, O at 256
+  // TMEM: S buffers at columns 0 and 128 (P of keys 0..63 over columns 0..31, of keys 64..127 over
+  // columns 64..95, each inside the S columns its own softmax half reads), O at 256
+  constexpr uint32_t kTS = 0, kTO = 256, kTQA = 256 + D;   // q . a^K of the tile's rows after O
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
     if (lane == 0 && !p.withhold) {
       int issued = 0;
-      bool ok = true;
-      mbar_arrive_expect_tx(bar(B_QF), C::kTile + (BIAS ? p.V * 512 : 0));
+      mbar_arrive_expect_tx(bar(B_QF), C::kTile + (BIAS ? p.Vp * D * 2 : 0));
       es_load_tile<D>(glob ? &p.mQg : &p.mQl, tq * 128, bh, sQ, bar(B_QF));
       if (BIAS) {
-        const float* qa = p.qa + (static_cast<size_t>(bh) * (g.n_gq + g.n_lq) + (glob ? tq : g.n_gq + tq)) * p.V * 128;
-        bulk_load_1d(sQa, qa, p.V * 512, bar(B_QF));
+        // a^K of this head, Vp rows (rows past V zero-filled), staged in the q . a^K region until
+        // the MMA that reads it has completed
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk) tma_load_3d(sQa + blk * p.Vp * 128, &p.mA, bar(B_QF), blk * 64, 0, bh % g.H);
       }
       for (int j = 0; j < n_steps; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(bar(B_KVE + st), ((j >> 1) - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+        if (j >= 2 && !mbar_wait(bar(B_KVE + st), ((j >> 1) - 1) & 1, abort_flag, cap)) { fail(); break; }
         bool kglob;
         int y;
         if (glob) { kglob = j < g.n_gq; y = kglob ? j * 128 : (j - g.n_gq) * 128; }
@@ -347,16 +320,34 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
       __syncwarp();
       return true;
     };
-    if (wait_or_fail(B_QF, 0) && issue_qk(0) && (n_steps < 2 || issue_qk(1))) {
+    bool q_ready = wait_or_fail(B_QF, 0);
+    if (BIAS && q_ready) {
+      // qa = Q a^K^T (M = 128, N = Vp, K = D) into TMEM columns kTQA..kTQA + Vp
+      tc_fence_after();
+      if (leader) {
+        const uint32_t kIdQA = idesc_bf16_f32(128, p.Vp, false);
+        const uint64_t dA = sdesc_sw128(sQa, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t oq = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * (p.Vp * 128) + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(tmem + kTQA, dQd + oq, dA + oa, kIdQA, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_QAF));
+      }
+      __syncwarp();
+    }
+    if (q_ready && issue_qk(0) && (n_steps < 2 || issue_qk(1))) {
       for (int j = 0; j < n_steps; ++j) {
         if (!wait_or_fail(B_PF + (j & 1), (j >> 1) & 1)) break;
         tc_fence_after();
         if (leader) {
-          // O += P_j V_j, P_j (bf16) read from the first 64 columns of S_{j mod 2}
+          // O += P_j V_j; keys 16 kk .. 16 kk + 15 of P at columns 8 kk (kk < 4) or 64 + 8 (kk - 4)
           const uint64_t dv = sdesc_sw128(stage(j & 1) + C::kTile, 128 * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTO, tmem + kTS + 128 * (j & 1) + kk * 8, dv + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTO, tmem + kTS + 128 * (j & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), dv + kk * 128,
+                         kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_PV));
           umma_commit(bar(B_KVE + (j & 1)));
         }
@@ -368,7 +359,8 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
     __syncwarp();
     if (!ok) mbar_wait(bar(B_DONE), 0, nullptr, kEsDrainCap);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
+    // ------------------------------------------------------------ softmax (two column halves per row) + epilogue
+    const int half = (warp - 4) >> 2;        // warps 4..7: columns 0..63; warps 8..11: columns 64..127
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int qi = tq * 128 + r;
@@ -381,12 +373,28 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
     // edge, blocked edges weigh exp(-10000 + ...) = 0 and the mass gathered in
     // the blocked frame is scaled by exp(-C) = 0.  C is subtracted from the
     // LSE of a row whose every edge is blocked.  Blocked edges are tagged in
-    // the lowest mantissa bit of their logit (a 1-ulp change).
-    bool has_allowed = false;
-    float m_use = -INFINITY, l_run = 0.f;
+    // the lowest mantissa bit of their logit (a 1-ulp change).  Both halves of
+    // a row take the same decisions from the exchanged tile maxima.
+    bool has_allowed = false, has_mass = false;
+    float m_use = -INFINITY, l_half = 0.f;
     bool ok = true;
+    if (BIAS) {
+      // this row's q . a^K from TMEM, times s log2(e), into the table [label][row] that replaces a^K
+      // in shared memory (the MMA that read a^K has completed); half h moves labels 32 h .. 32 h + 31
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_QAF), 0, abort_flag, cap))) { fail(); ok = false; }
+      if (ok && 32 * half < p.Vp) {
+        tc_fence_after();
+        float qa[32];
+        tmem_ld32(tmem + lane_off + kTQA + 32 * half, qa);
+        float* tab = reinterpret_cast<float*>(smem + C::kOffQa);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (32 * half + e < p.V) tab[(32 * half + e) * 128 + r] = qa[e] * cs;
+      }
+      named_bar_sync(1, 256);
+    }
     for (int j = 0; j < n_steps; ++j) {
-      // this row's keys in tile j: columns [lo, hi]
+      // this row's keys in tile j: columns [lo, hi] of the full tile
       int lo = 0, hi;
       if (glob) {
         hi = j < g.n_gq ? min(127, g.G - 1 - j * 128) : min(127, g.L - 1 - (j - g.n_gq) * 128);
@@ -398,16 +406,19 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
         hi = min(127, g.G - 1 - (j - n_band) * 128);
       }
       if (!valid) { lo = 1; hi = 0; }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SF + (j & 1)), (j >> 1) & 1, abort_flag, cap))) {
-        fail(); ok = false; break;
+      // After a failed wait a warp keeps taking the named barriers below (without waits or work),
+      // so that every softmax thread takes each of them the same number of times.
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_SF + (j & 1)), (j >> 1) & 1, abort_flag, cap))) {
+        fail(); ok = false;
       }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + kTS + 128 * (j & 1);
       const uint32_t crow = stage(j & 1) + 2 * C::kTile + r * 128;
-      float x[128];
-      float ta = -INFINITY, tb = -INFINITY;   // tile maxima over allowed / blocked edges
+      float x[64];
+      float ta = -INFINITY, tall = -INFINITY;   // maxima over this half's allowed / member edges
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2 && ok; ++c2) {
+        const int c4 = 2 * half + c2;          // 32-column chunk of the tile
         float s[32];
         tmem_ld32(tS + 32 * c4, s);
         uint32_t cw[8];
@@ -418,9 +429,9 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
                        : "=r"(cw[4 * h]), "=r"(cw[4 * h + 1]), "=r"(cw[4 * h + 2]), "=r"(cw[4 * h + 3])
                        : "r"(a));
         }
+        const int clo = lo - 32 * c4, chi = hi - 32 * c4;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int col = 32 * c4 + e;
           const uint32_t code = (cw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
           float v = s[e] * cs;
           if (BIAS) {
@@ -431,43 +442,53 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
           }
           const uint32_t blk = code >> 7;
           v = __uint_as_float((__float_as_uint(v) & ~1u) | blk);
-          const bool member = col >= lo && col <= hi;
-          x[col] = member ? v : -INFINITY;
-          ta = fmaxf(ta, (member && !blk) ? v : -INFINITY);
-          tb = fmaxf(tb, (member && blk) ? v : -INFINITY);
+          const float xv = (e >= clo && e <= chi) ? v : -INFINITY;
+          x[32 * c2 + e] = xv;
+          tall = fmaxf(tall, xv);
+          ta = fmaxf(ta, blk ? -INFINITY : xv);
         }
       }
+      // combine the two halves' maxima
+      x_allowed[(j & 1) * 256 + half * 128 + r] = ta;
+      x_all[(j & 1) * 256 + half * 128 + r] = tall;
+      named_bar_sync(1, 256);
+      ta = fmaxf(ta, x_allowed[(j & 1) * 256 + (1 - half) * 128 + r]);
+      tall = fmaxf(tall, x_all[(j & 1) * 256 + (1 - half) * 128 + r]);
+      if (!ok) continue;
       const bool now_allowed = has_allowed || ta > -INFINITY;
-      const float tmax = now_allowed ? ta : tb;
-      const bool leave_blocked_frame = now_allowed && !has_allowed && l_run > 0.f;
+      const float tmax = now_allowed ? ta : tall;   // in the blocked frame every member is blocked
+      const bool leave_blocked_frame = now_allowed && !has_allowed && has_mass;
       // lazy rescale: move the running maximum only when it grows by more than 2^8
       const bool grow = leave_blocked_frame || tmax > m_use + 8.f;
       const float m_new = grow ? tmax : m_use;
       const float f = grow ? (leave_blocked_frame ? 0.f : exp2f(m_use - m_new)) : 1.f;   // 0 when m_use is -inf
-      const bool rescale_o = grow && l_run > 0.f;
-      l_run *= f;
+      const bool rescale_o = grow && has_mass;
+      l_half *= f;
       m_use = m_new;
       has_allowed = now_allowed;
+      has_mass = has_mass || tall > -INFINITY;
       if (__any_sync(0xffffffffu, rescale_o)) {
-        // PV_{j-1} must have completed before O is read and written (PV_{j-2} has: QK_j came after it)
+        // PV_{j-1} must have completed before O is read and written (PV_{j-2} has: QK_j came after it);
+        // each half rescales its own D / 2 columns of O
         if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_PV), (j - 1) & 1, abort_flag, cap))) {
-          fail(); ok = false; break;
+          fail(); ok = false; continue;
         }
         tc_fence_after();
         const float fo = rescale_o ? f : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           float o[32];
-          tmem_ld32(tmem + lane_off + kTO + 32 * c, o);
+          const uint32_t ta_o = tmem + lane_off + kTO + half * (D / 2) + 32 * c;
+          tmem_ld32(ta_o, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= fo;
-          tmem_st32(tmem + lane_off + kTO + 32 * c, o);
+          tmem_st32(ta_o, o);
         }
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
       float sum = 0.f;
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
+      for (int wd = 0; wd < 2; ++wd) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -478,47 +499,50 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
           sum += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16_nowait(tS + 16 * wd, pk);   // P over the S columns already read
+        tmem_st16_nowait(tS + 64 * half + 16 * wd, pk);   // P of this half's keys over its own S columns
       }
-      l_run += sum;
+      l_half += sum;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PF + (j & 1)));
     }
+    // the row's sum: both halves' partial sums
+    x_sum[half * 128 + r] = l_half;
+    named_bar_sync(1, 256);
+    const float l_run = l_half + x_sum[(1 - half) * 128 + r];
     if (ok) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, abort_flag, cap))) {
         fail();
-      } else {
+      } else if (D == 128 || half == 0) {
         tc_fence_after();
         const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
-        // stage 32 rows x 64 columns per warp in the (now idle) first K tile and store with TMA
+        // stage 32 rows x 64 columns per warp in the (now idle) first K tile and store with TMA;
+        // D = 128: half h stores columns 64 h .. 64 h + 63
         const uint32_t st = stage(0) + (warp - 4) * 4096;
         const int y0 = tq * 128 + 32 * (warp & 3);
+        const int col0 = D == 128 ? 64 * half : 0;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll 1
-        for (int half = 0; half < D / 64; ++half) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-#pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            float o[32];
-            tmem_ld32(tmem + lane_off + kTO + half * 64 + cc * 32, o);
+        for (int cc = 0; cc < 2; ++cc) {
+          float o[32];
+          tmem_ld32(tmem + lane_off + kTO + col0 + cc * 32, o);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int ci = cc * 4 + c;
-              st_shared_v4(st + lane * 128 + ((ci ^ (lane & 7)) << 4), pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                           pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                           pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                           pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(glob ? &p.sOg : &p.sOl, st, half * 64, y0, bh);
-            bulk_commit_group();
+          for (int c = 0; c < 4; ++c) {
+            const int ci = cc * 4 + c;
+            st_shared_v4(st + lane * 128 + ((ci ^ (lane & 7)) << 4), pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                         pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                         pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                         pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
           }
         }
-        if (valid) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(glob ? &p.sOg : &p.sOl, st, col0, y0, bh);
+          bulk_commit_group();
+        }
+        if (valid && half == 0) {
           const float lse = (m_use + __log2f(l_run)) * 0.6931471805599453f - (has_allowed ? 0.f : kEsMaskC);
           if (glob) p.lse_g[static_cast<size_t>(bh) * g.G + qi] = lse;
           else p.lse_l[static_cast<size_t>(bh) * g.L + qi] = lse;
@@ -562,27 +586,44 @@ bool es_aligned(const void* x, size_t a) { return (reinterpret_cast<uintptr_t>(x
 size_t es_rup(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct EsLayout {
-  size_t codes = 0, qa = 0, total = 0;
+  size_t codes = 0, total = 0;
 };
 
-EsLayout es_layout(const EsGeom& g, int n_labels) {
+EsLayout es_layout(const EsGeom& g) {
   EsLayout w;
   size_t off = kStatusBytes;
   w.codes = off;
   off += es_rup(static_cast<size_t>(g.B) * g.blocks_per_b * kCodeTile, 256);
-  w.qa = off;
-  if (n_labels > 0)
-    off += es_rup(static_cast<size_t>(g.B) * g.H * (g.n_gq + g.n_lq) * n_labels * 128 * 4, 256);
   w.total = off;
   return w;
+}
+
+// a^K [H, V, D] bf16 viewed as {D, V, H} for loads of Vp rows x 64 columns
+// (rows past V zero-filled), the B operand of the q . a^K contraction.
+bool es_encode_rel(CUtensorMap* m, const void* rel, int D, int V, int Vp, int H) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(V) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(Vp), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(rel), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 lg_status es_check(int B, int H, int L, int G, int D, int radius, int n_labels, lg_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || G < 1 || radius < 0 || n_labels < 0) return LG_ERR_INVALID_ARG;
   if (dt != LG_BF16 && dt != LG_F32) return LG_ERR_INVALID_ARG;
-  if (dt != LG_BF16 || (D != 64 && D != 128) || n_labels > kEsMaxLabels) return LG_ERR_UNSUPPORTED;
+  if (dt != LG_BF16 || (D != 64 && D != 128)) return LG_ERR_UNSUPPORTED;
+  if (n_labels > (D == 64 ? EsCfg<64>::kMaxLabels : EsCfg<128>::kMaxLabels)) return LG_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * (static_cast<long long>(L) + G) > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * ((L + 127) / 128 + (G + 127) / 128) > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
+  {
+    // the code blocks of one call are indexed with 32-bit integers, four packing CTAs per block
+    const EsGeom g = es_geom(B, H, L, G, radius);
+    if (static_cast<long long>(B) * g.blocks_per_b * 4 > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
+  }
   return LG_OK;
 }
 
@@ -595,7 +636,7 @@ extern "C" {
 
 size_t lg_etc_struct_attn_fwd_workspace_size(int B, int H, int L, int G, int D, int radius, int n_labels, lg_dtype dt) {
   if (es_check(B, H, L, G, D, radius, n_labels, dt) != LG_OK) return 0;
-  return es_layout(es_geom(B, H, L, G, radius), n_labels).total;
+  return es_layout(es_geom(B, H, L, G, radius)).total;
 }
 
 lg_status lg_etc_struct_attn_fwd(const void* q_l, const void* k_l, const void* v_l, const void* q_g, const void* k_g,
@@ -614,7 +655,7 @@ lg_status lg_etc_struct_attn_fwd(const void* q_l, const void* k_l, const void* v
   if (!lse_l || !lse_g || !es_aligned(lse_l, 4) || !es_aligned(lse_g, 4)) return LG_ERR_INVALID_ARG;
   if (rel_k != nullptr && !es_aligned(rel_k, 16)) return LG_ERR_INVALID_ARG;
   const EsGeom geom = es_geom(B, H, L, G, radius);
-  const EsLayout lay = es_layout(geom, n_labels);
+  const EsLayout lay = es_layout(geom);
   if (workspace == nullptr || !es_aligned(workspace, 256) || workspace_bytes < lay.total) return LG_ERR_WORKSPACE;
   if (!encode_fn()) return LG_ERR_CUDA;
 
@@ -629,7 +670,6 @@ lg_status lg_etc_struct_attn_fwd(const void* q_l, const void* k_l, const void* v
       !encode_store_map(&p.sOl, out_l, D, L, BH, 1) || !encode_store_map(&p.sOg, out_g, D, G, BH, 1))
     return LG_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return LG_ERR_CUDA;
-  const long long cap_blocks = 16LL * device_sm_count();
 
   EsPackParams pp{};
   pp.g = geom;
@@ -637,32 +677,20 @@ lg_status lg_etc_struct_attn_fwd(const void* q_l, const void* k_l, const void* v
   pp.codes = reinterpret_cast<uint8_t*>(ws + lay.codes);
   pp.n_labels = n_labels;
   pp.status = status;
-  const long long pack_threads = static_cast<long long>(B) * geom.blocks_per_b * (kCodeTile / 16);
-  if (launch_kernel(es_pack_kernel, dim3(static_cast<unsigned>(std::min((pack_threads + 255) / 256, cap_blocks))),
-                    dim3(256), 0, stream, false, pp) != cudaSuccess)
+  const long long pack_ctas = static_cast<long long>(B) * geom.blocks_per_b * 4;
+  if (launch_kernel(es_pack_kernel, dim3(static_cast<unsigned>(pack_ctas)), dim3(256), 0, stream, false, pp) !=
+      cudaSuccess)
     return LG_ERR_CUDA;
-  if (n_labels > 0) {
-    EsQaParams qp{};
-    qp.q_l = static_cast<const __nv_bfloat16*>(q_l);
-    qp.q_g = static_cast<const __nv_bfloat16*>(q_g);
-    qp.rel = static_cast<const __nv_bfloat16*>(rel_k);
-    qp.qa = reinterpret_cast<float*>(ws + lay.qa);
-    qp.H = H; qp.L = L; qp.G = G; qp.D = D; qp.V = n_labels; qp.n_gq = geom.n_gq; qp.n_lq = geom.n_lq;
-    qp.total = static_cast<long long>(BH) * (geom.n_gq + geom.n_lq) * n_labels * 128;
-    qp.c = s * 1.4426950408889634f;
-    if (launch_kernel(es_qa_kernel, dim3(static_cast<unsigned>(std::min((qp.total + 255) / 256, cap_blocks))),
-                      dim3(256), 0, stream, false, qp) != cudaSuccess)
-      return LG_ERR_CUDA;
-  }
   p.g = geom;
   p.codes = pp.codes;
-  p.qa = reinterpret_cast<const float*>(ws + lay.qa);
   p.lse_l = lse_l;
   p.lse_g = lse_g;
   p.status = status;
   p.wait_cap = wait_cap_cycles();
   p.withhold = withhold_for_test();
   p.V = n_labels > 0 ? n_labels : 1;
+  p.Vp = (p.V + 15) / 16 * 16;
+  if (n_labels > 0 && !es_encode_rel(&p.mA, rel_k, D, n_labels, p.Vp, H)) return LG_ERR_CUDA;
   p.scale_log2 = s * 1.4426950408889634f;
   const int units = BH * (geom.n_gq + geom.n_lq);
   cudaError_t e = prof_mark(stream, true);

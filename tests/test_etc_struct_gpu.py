@@ -72,6 +72,7 @@ CASES = [
     (E("radius 0", 1, 2, 260, 3, 64, 0), 4, 0.1),
     (E("radius beyond L", 1, 2, 150, 4, 64, 400), 6, 0.2),
     (E("64 labels", 1, 2, 333, 9, 64, 20), 64, 0.25),
+    (E("40 labels D128 two global tiles", 1, 2, 260, 140, 128, 9), 40, 0.25),
     (E("single token", 1, 1, 1, 1, 64, 3), 2, 0.0),
 ]
 
