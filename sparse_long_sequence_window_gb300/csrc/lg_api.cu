@@ -67,6 +67,13 @@ bool encode_store_map(CUtensorMap* m, void* base, int D, int rows, int BH, int d
 // Band units at the end of a launch of `units` units to split in two
 // one-tile units each: the last round of a persistent launch (units mod grid
 // units) when splitting it still leaves at most one item per CTA; 0 otherwise.
+long long grow_tail_cap(const TcParams& tp) {
+  if (tp.n_grow_units == 0 || !tp.grow_interleave) return 1LL << 40;
+  // the units after the last key split's global-row units in the last (batch, head) block
+  const long long nb = tp.head_unit_start[tp.H] - tp.head_unit_start[tp.H - 1];
+  return nb > 0 ? nb - nb * (tp.n_splits - 1) / tp.n_splits : 0;
+}
+
 long long tail_split(long long units, long long band_units) {
   const long long grid = std::min<long long>(units, device_sm_count());
   if (grid <= 0 || units <= grid) return 0;
@@ -348,14 +355,18 @@ lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void*
   // ---- bf16 tensor-core path
   if (!encode_fn()) return LG_ERR_CUDA;
   GrowPlan gp;
+  const bool interleave = grow_interleave_for(4LL * BH * N * D);   // K and V, bf16
   if (n_global > 0) {
     long long band_units = 0;
     for (int h = 0; h < H; ++h) band_units += band_units_for(N, dilation[h]);
     band_units *= B;
     const int band_tiles = std::min(cdiv(static_cast<long long>(wl) + wr + kTileM, kTileN) + 1, cdiv(N, kTileN)) + cdiv(n_global, kTileN);
+    // interleaved global-row units are sized like a band unit (2 x band_tiles key tiles), so that
+    // the rounds stay even; first-placed ones may be longer
     gp = grow_plan(n_global, cdiv(N, kTileN),
-                   choose_grow_split(band_units, band_tiles, static_cast<long long>(BH) * cdiv(n_global, kTileM),
-                                     cdiv(N, kTileN)));
+                   interleave ? 2 * band_tiles
+                              : choose_grow_split(band_units, band_tiles, static_cast<long long>(BH) * cdiv(n_global, kTileM),
+                                                  cdiv(N, kTileN)));
   }
   const WsLayout lay = ws_layout(BH, n_global, D, gp.n_parts, true, N, max_units(BH, N, LG_MAX_BF16_DILATION, gp));
   __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(ws + lay.qg);
@@ -434,8 +445,9 @@ lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void*
     tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
     tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
     tp.n_grow_units = (grp == 0 && n_global > 0) ? BH * gp.n_gtiles * gp.n_splits : 0;
+    tp.grow_interleave = interleave ? 1 : 0;
     const long long base_units = static_cast<long long>(tp.n_grow_units) + static_cast<long long>(B) * start;
-    tp.n_tail_split = static_cast<int>(tail_split(base_units, static_cast<long long>(B) * start));
+    tp.n_tail_split = static_cast<int>(std::min(tail_split(base_units, static_cast<long long>(B) * start), grow_tail_cap(tp)));
     const long long units = base_units + tp.n_tail_split;
     if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
     if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
@@ -519,9 +531,12 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   if (!encode_fn()) return LG_ERR_CUDA;
   const int key_tiles_g = cdiv(G, kTileN) + cdiv(L, kTileN);
   const int band_tiles = std::min(cdiv(2LL * r + kTileM, kTileN) + 1, cdiv(L, kTileN)) + cdiv(G, kTileN);
+  const bool interleave = grow_interleave_for(4LL * BH * (static_cast<long long>(L) + G) * D);
   const GrowPlan gp = grow_plan(G, key_tiles_g,
-                                choose_grow_split(static_cast<long long>(BH) * band_units_for(L, 1), band_tiles,
-                                                  static_cast<long long>(BH) * cdiv(G, kTileM), key_tiles_g));
+                                interleave ? 2 * band_tiles
+                                           : choose_grow_split(static_cast<long long>(BH) * band_units_for(L, 1),
+                                                               band_tiles, static_cast<long long>(BH) * cdiv(G, kTileM),
+                                                               key_tiles_g));
   const WsLayout lay = ws_layout(BH, G, D, gp.n_parts, false, 0, max_units(BH, L, 1, gp));
   TcParams tp{};
   if (!encode_map(&tp.mapQ[0], q_l, D, L, BH, 1) || !encode_map(&tp.mapK[0], k_l, D, L, BH, 1) ||
@@ -556,8 +571,10 @@ lg_status lg_etc_attn_fwd(const void* q_l, const void* k_l, const void* v_l, con
   tp.n_gtiles = gp.n_gtiles; tp.n_splits = gp.n_splits; tp.n_parts = gp.n_parts;
   tp.n_key_tiles_grow = gp.n_key_tiles; tp.grow_split = std::max(1, gp.split);
   tp.n_grow_units = BH * gp.n_gtiles * gp.n_splits;
+  tp.grow_interleave = interleave ? 1 : 0;
   const long long band_units = static_cast<long long>(B) * tp.band_units_per_batch;
-  tp.n_tail_split = static_cast<int>(tail_split(static_cast<long long>(tp.n_grow_units) + band_units, band_units));
+  tp.n_tail_split = static_cast<int>(
+      std::min(tail_split(static_cast<long long>(tp.n_grow_units) + band_units, band_units), grow_tail_cap(tp)));
   const long long units = static_cast<long long>(tp.n_grow_units) + band_units + tp.n_tail_split;
   if (units > (1LL << 31) - 1) return LG_ERR_UNSUPPORTED;
   if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;

@@ -118,6 +118,7 @@ struct TcParams {
   int* unit_counter;              // units claimed so far (zeroed before the launch)
   int grow_split;                 // key tiles per split of a global-query row block
   int n_tail_split;               // last band units split into two one-tile units each
+  int grow_interleave;            // 1: global-row units interleaved with their head's band units
   long long wait_cap;             // clock64 cycles a bounded wait may spin
   int withhold;                   // test of the timeout path: issue no TMA load and no MMA
   float scale_log2;               // scale * log2(e)
@@ -275,8 +276,17 @@ lg_status validate_fwd(const void* q, const void* k, const void* v, const void* 
                        int causal, const int32_t* global_idx, int n_global, const void* workspace,
                        size_t workspace_bytes, bool per_call_head_limit);
 int device_sm_count();
+long long device_l2_bytes();
+// Whether a launch interleaves its global-row units with the band units: when
+// K and V of the launch (kv_bytes) are over four times the L2, the global rows'
+// own pass over every key would otherwise be read from HBM a second time.  (At
+// about twice the L2, measured, placing the long global-row units first wins.)
+inline bool grow_interleave_for(long long kv_bytes) { return kv_bytes > 4 * device_l2_bytes(); }
 // Band units of a launch of `units` units to split into one-tile halves (the last round).
 long long tail_split(long long units, long long band_units);
+// The tail split may only take band units: with global-row units interleaved,
+// at most the band units after the last head's last key split.
+long long grow_tail_cap(const TcParams& tp);
 // Profiling of the tensor-core launches (lg_profile_begin/end): events around a launch.
 cudaError_t prof_mark(cudaStream_t s, bool start);  // SMs of the current device (cached per device)
 

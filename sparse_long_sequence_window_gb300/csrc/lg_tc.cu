@@ -122,7 +122,14 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
     half = (u - n_full) & 1;
     u = n_full + ((u - n_full) >> 1);
   }
-  if (u < p.n_grow_units) {
+  // Two orders.  Global-row units first (the longest units start first), when
+  // the launch's K and V fit in L2 anyway.  Otherwise, per (batch, head) block,
+  // the head's band units with its global-row units interleaved in key order
+  // (the n_gtiles units of key split s before band unit floor(nb s / n_splits)),
+  // so that units reading the same K/V tiles run in the same round and share
+  // them through L2 instead of reading them from HBM twice.
+  const bool first = p.n_grow_units > 0 && !p.grow_interleave;
+  if (first && u < p.n_grow_units) {
     w.grow = 1;
     const int split = u % p.n_splits;
     const int r = u / p.n_splits;
@@ -134,12 +141,34 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
     w.active[0] = 1; w.active[1] = w.n_tiles > 1;
     return w;
   }
-  const int v = u - p.n_grow_units;
-  const int b = v / p.band_units_per_batch;
-  int rem = v % p.band_units_per_batch;
+  if (first) u -= p.n_grow_units;
+  const int gu = (p.n_grow_units > 0 && !first) ? p.n_gtiles * p.n_splits : 0;   // interleaved units per (b, h)
+  const int per_batch = p.band_units_per_batch + p.H * gu;
+  const int b = u / per_batch;
+  int rem = u - b * per_batch;
   int h = 0;
-  while (h + 1 < p.H && p.head_unit_start[h + 1] <= rem) ++h;
-  rem -= p.head_unit_start[h];
+  while (h + 1 < p.H && p.head_unit_start[h + 1] + (h + 1) * gu <= rem) ++h;
+  rem -= p.head_unit_start[h] + h * gu;
+  if (gu > 0) {
+    const long long nb = p.head_unit_start[h + 1] - p.head_unit_start[h];
+    int split = -1, gt = 0, band = rem - p.n_splits * p.n_gtiles;
+    for (int sp = 0; sp < p.n_splits; ++sp) {
+      const int st = static_cast<int>(nb * sp / p.n_splits) + sp * p.n_gtiles;
+      if (rem < st) { band = rem - sp * p.n_gtiles; break; }
+      if (rem < st + p.n_gtiles) { split = sp; gt = rem - st; break; }
+    }
+    if (split >= 0) {
+      w.grow = 1;
+      w.grow0 = gt * kTileM;
+      w.bh = b * p.H + h;
+      w.kt0 = split * p.grow_split;
+      w.n_tiles = min(p.grow_split, p.n_key_tiles_grow - w.kt0);
+      w.slot = 0; w.d = 1;
+      w.active[0] = 1; w.active[1] = w.n_tiles > 1;
+      return w;
+    }
+    rem = band;
+  }
   w.grow = 0;
   w.bh = b * p.H + h;
   w.slot = p.head_slot[h];
@@ -1007,6 +1036,19 @@ cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain
   if (i == 0)
     return launch_kernel(tc_attn_kernel<64>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<64>::kSmem, s, true, p, n_units);
   return launch_kernel(tc_attn_kernel<128>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<128>::kSmem, s, true, p, n_units);
+}
+
+long long device_l2_bytes() {
+  static std::atomic<long long> l2[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  long long v = l2[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int x = 0;
+    v = (cudaDeviceGetAttribute(&x, cudaDevAttrL2CacheSize, dev) == cudaSuccess && x > 0) ? x : (128LL << 20);
+    l2[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
 }
 
 int device_sm_count() {
