@@ -209,7 +209,7 @@ def launches_per_call(w):
         packed = sum(1 for a, r in zip(w.seg_w, w.seg_r) if not (r <= 8 and a % r == 0))
         return 2 * len(w.seg_w) + packed + 1
     if w.dtype == "f32":
-        return 2 if (not w.is_etc and (w.global_positions or w.n_random_global)) else 1
+        return 1  # one CUDA-core kernel (it also checks the global list)
     if w.is_etc:
         return 3  # unit table + tensor-core kernel + merge
     dil = [d for d in set(w.dilations()) if d != 1]

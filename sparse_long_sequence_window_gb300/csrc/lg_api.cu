@@ -336,10 +336,8 @@ lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void*
   if (e != cudaSuccess) return LG_ERR_CUDA;
 
   if (dt == LG_F32) {
-    PrepParams pp{};
-    pp.gidx = global_idx; pp.n_glob = n_global; pp.N = N; pp.status = status; pp.BH = BH; pp.D = D;
-    if ((e = launch_prep(pp, stream)) != cudaSuccess) return LG_ERR_CUDA;
-    SimtParams sp{};
+    SimtParams sp{};   // the kernel itself checks the global list (one launch per call)
+    sp.status = status;
     sp.q = static_cast<const float*>(q); sp.k = static_cast<const float*>(k); sp.v = static_cast<const float*>(v);
     sp.out = static_cast<float*>(out); sp.lse = lse; sp.gidx = global_idx;
     sp.qgl = static_cast<const float*>(qgl); sp.kgl = static_cast<const float*>(kgl);

@@ -74,6 +74,8 @@ struct SimtParams {
   int etc;
   float scale;
   int dil[LG_MAX_HEADS];
+  int tile_start[LG_MAX_HEADS + 1];  // prefix over heads of the band-row tiles of one batch
+  int* status;                       // device status word (Longformer: a bad global list is reported here)
 };
 
 // fp32 backward on the CUDA cores: one warp per query row; dQ written, dK and
