@@ -82,41 +82,72 @@ struct MixParams {
   float* lse;
 };
 
-// One warp per row; lane x takes D / 32 consecutive columns.  The patterns
-// that keep the row are merged online (running max of LSE_k).
-__global__ void __launch_bounds__(256) longnet_mix_kernel(const MixParams p) {
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One thread per row and 64 columns (D / 64 threads per row): the pattern
+// membership arithmetic once per pattern in 32-bit integers, then eight
+// 16-byte loads of the pattern's output.  The patterns that keep the row are
+// merged online (running max of LSE_k).  The parameter block is read in place
+// (__grid_constant__): its per-pattern arrays are indexed by a runtime k.
+template <int D>
+__global__ void __launch_bounds__(256) longnet_mix_kernel(const __grid_constant__ MixParams p) {
   grid_dep_wait();   // the patterns' kernels came before
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(p.BH) * p.N) return;
-  const int i = static_cast<int>(row % p.N);
-  const long long bh = row / p.N;
-  const int h = static_cast<int>(bh % p.H);
-  const int per = p.D / 32;   // 2 or 4 columns per lane
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr int kParts = D / 64;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (tid >= static_cast<long long>(p.BH) * p.N * kParts) return;
+  const int part = static_cast<int>(tid % kParts);
+  const int row = static_cast<int>(tid / kParts);   // BH * N < 2^31
+  const int i = row % p.N;
+  const int bh = row / p.N;
+  const int h = bh % p.H;
+  float acc[64];
+#pragma unroll
+  for (int c = 0; c < 64; ++c) acc[c] = 0.f;
   float m = -INFINITY, l = 0.f;
   for (int k = 0; k < p.n_pat; ++k) {
     const int w = p.w[k], r = p.r[k], s = h % r;
     const int seg = i / w, rel = i - seg * w - s;
     if (rel < 0 || rel % r != 0) continue;
-    const long long src = p.packed[k] ? bh * p.rows[k] + static_cast<long long>(seg) * seg_block(w, r, s) + rel / r
+    const long long src = p.packed[k] ? static_cast<long long>(bh) * p.rows[k] +
+                                            static_cast<long long>(seg) * seg_block(w, r, s) + rel / r
                                       : row;
-    const float lk = p.l[k][src];
+    const float lk = __ldg(p.l[k] + src);
     if (lk > m) {   // new running maximum: rescale what is accumulated
       const float f = exp2f((m - lk) * 1.4426950408889634f);
       l *= f;
-      for (int c = 0; c < per; ++c) acc[c] *= f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) acc[c] *= f;
       m = lk;
     }
     const float wgt = exp2f((lk - m) * 1.4426950408889634f);
     l += wgt;
-    const __nv_bfloat16* o = p.o[k] + src * p.D + lane * per;
-    for (int c = 0; c < per; ++c) acc[c] = fmaf(wgt, __bfloat162float(o[c]), acc[c]);
+    const uint4* o = reinterpret_cast<const uint4*>(p.o[k] + src * D + part * 64);
+    uint4 v[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v[x] = __ldg(o + x);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint32_t vw[4] = {v[x].x, v[x].y, v[x].z, v[x].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[e]));
+        acc[8 * x + 2 * e] = fmaf(wgt, f2.x, acc[8 * x + 2 * e]);
+        acc[8 * x + 2 * e + 1] = fmaf(wgt, f2.y, acc[8 * x + 2 * e + 1]);
+      }
+    }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat16* dst = p.out + row * p.D + lane * per;
-  for (int c = 0; c < per; ++c) dst[c] = __float2bfloat16_rn(acc[c] * inv);
-  if (lane == 0) p.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<long long>(row) * D + part * 64);
+#pragma unroll
+  for (int x = 0; x < 8; ++x)
+    dst[x] = make_uint4(pack_bf16x2_rn(acc[8 * x] * inv, acc[8 * x + 1] * inv),
+                        pack_bf16x2_rn(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
+                        pack_bf16x2_rn(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
+                        pack_bf16x2_rn(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
+  if (part == 0) p.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 bool aligned_ln(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -292,8 +323,9 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
   mp.out = static_cast<__nv_bfloat16*>(out);
   mp.lse = lse;
   const long long rows = static_cast<long long>(BH) * N;
-  const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-  if (launch_kernel(longnet_mix_kernel, dim3(blocks), dim3(256), 0, stream, true, mp) != cudaSuccess)
+  const unsigned blocks = static_cast<unsigned>((rows * (D / 64) + 255) / 256);
+  if (launch_kernel(D == 64 ? longnet_mix_kernel<64> : longnet_mix_kernel<128>, dim3(blocks), dim3(256), 0, stream, true,
+                    mp) != cudaSuccess)
     return LG_ERR_CUDA;
   return LG_OK;
 }
