@@ -56,7 +56,7 @@ int bwd_cm(int N) { return (N + 4 * LG_MAX_BF16_DILATION + 128 + 3) / 4 * 4; }
 
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4..11 elementwise (two column halves)
 constexpr long long kBwdDrainCap = 4000000000LL;   // fixed bound of waits for already-issued async work
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -242,9 +242,10 @@ struct BwdCfg {
 // and out through a TMA store.
 template <int D>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t stage, uint32_t tacc, float mul,
-                                               int y0, int bh, int lane) {
+                                               int y0, int bh, int lane, int col_half) {
+  // D = 128: this warp stores the 64 columns of col_half; D = 64: all 64 columns
 #pragma unroll 1
-  for (int half = 0; half < D / 64; ++half) {
+  for (int half = D == 128 ? col_half : 0; half < (D == 128 ? col_half + 1 : 1); ++half) {
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();
 #pragma unroll 1
@@ -276,9 +277,9 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* map, uint32_t 
 // accumulators in two separate loops gave the first one's values twice.)
 template <int D>
 __device__ __forceinline__ void store_partial_rows(float* dst_a, uint32_t tacc_a, float* dst_b, uint32_t tacc_b,
-                                                   bool valid) {
+                                                   bool valid, int c_begin, int c_end) {
 #pragma unroll 1
-  for (int cc = 0; cc < D / 32; ++cc) {
+  for (int cc = c_begin; cc < c_end; ++cc) {
     float oa[32], ob[32];
     tmem_ld32(tacc_a + cc * 32, oa);
     if (dst_b != nullptr) tmem_ld32(tacc_b + cc * 32, ob);
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) mbar_init(bar(i), i == B_PR ? 128 : 1);
+    for (int i = 0; i < NB; ++i) mbar_init(bar(i), i == B_PR ? 256 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
           const uint64_t dkm = dKmn0 + st * kStage;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdQ, tmem + kTS + kk * 8, dkm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTdQ, tmem + kTS + kk * 8 + (kk >= 4 ? 32 : 0), dkm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_KVE + st));
         }
         __syncwarp();
@@ -415,7 +416,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
     __syncwarp();
     if (!ok) mbar_wait(bar(B_DONE), 0, nullptr, kBwdDrainCap);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ elementwise warpgroup + epilogue
+    // ------------------------------------------------------------ elementwise warpgroups + epilogue
+    // Two threads per row: warps 4..7 take columns 0..63, warps 8..11 columns 64..127 (every
+    // element is independent: P and dS need only per-row and per-column constants).  Each half
+    // writes its packed bf16 results inside its own S / dP columns (columns 32 h.. + 0..31).
+    const int half = (warp - 4) >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off + kTS, tdP = tmem + lane_off + kTdP, tdQ = tmem + lane_off + kTdQ;
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SR), j & 1, abort_flag, cap))) { fail(); ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int wd = 0; wd < 4; ++wd) {
+      for (int wd = 2 * half; wd < 2 * half + 2; ++wd) {
         uint32_t sr[32], dr[32];
         tmem_ld32_nowait(tS + 32 * wd, sr);
         tmem_ld32_nowait(tdP + 32 * wd, dr);
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
           }
           pk[i] = pack_bf16x2(d0, d1);
         }
-        tmem_st16_nowait(tS + 16 * wd, pk);   // dS over S columns already read
+        tmem_st16_nowait(tS + 16 * wd + 32 * half, pk);   // dS over this half's S columns, already read
       }
       tmem_wait_st();
       tc_fence_before();
@@ -496,11 +501,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
         tc_fence_after();
         if (w.grow) {
           const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.gt * 128 + r) * p.ns_stride + w.x0 / p.split;
-          store_partial_rows<D>(p.part_a + prow * D, tdQ, nullptr, 0u, valid);
+          const int c0 = half * (D / 64), c1 = c0 + D / 64;   // this half's 32-column chunks
+          store_partial_rows<D>(p.part_a + prow * D, tdQ, nullptr, 0u, valid, c0, c1);
         } else {
           const uint32_t stage = sKV + (warp - 4) * 4096;
           const int y0 = w.c + p.d * (w.t0 + 32 * (warp & 3));
-          store_rows_tma<D>(&p.sA, stage, tdQ, p.scale, y0, w.bh, lane);
+          if (D == 128 || half == 0) store_rows_tma<D>(&p.sA, stage, tdQ, p.scale, y0, w.bh, lane, half);
         }
       }
     }
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) mbar_init(bar(i), i == B_PR ? 128 : 1);
+    for (int i = 0; i < NB; ++i) mbar_init(bar(i), i == B_PR ? 256 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -630,10 +636,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
           const uint64_t qm = dQmn0 + st * kStage, om = ddOmn0 + st * kStage;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdV, tmem + kTS + kk * 8, om + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTdV, tmem + kTS + kk * 8 + (kk >= 4 ? 32 : 0), om + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdK, tmem + kTdP + kk * 8, qm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTdK, tmem + kTdP + kk * 8 + (kk >= 4 ? 32 : 0), qm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_QE + st));
         }
         __syncwarp();
@@ -643,7 +649,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
     __syncwarp();
     if (!ok) mbar_wait(bar(B_DONE), 0, nullptr, kBwdDrainCap);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ elementwise warpgroup + epilogue
+    // ------------------------------------------------------------ elementwise warpgroups + epilogue
+    // Two threads per row: warps 4..7 take columns 0..63, warps 8..11 columns 64..127 (every
+    // element is independent: P and dS need only per-row and per-column constants).  Each half
+    // writes its packed bf16 results inside its own S / dP columns (columns 32 h.. + 0..31).
+    const int half = (warp - 4) >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off + kTS, tdP = tmem + lane_off + kTdP;
@@ -692,7 +702,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
       const float* vl = reinterpret_cast<const float*>(smem + 2 * C::kTileBytes + st * C::kKVStage + 2 * C::kTileBytes);
       const float* vd = vl + 128;
 #pragma unroll 1
-      for (int wd = 0; wd < 4; ++wd) {
+      for (int wd = 2 * half; wd < 2 * half + 2; ++wd) {
         uint32_t sr[32], dr[32];
         tmem_ld32_nowait(tS + 32 * wd, sr);
         tmem_ld32_nowait(tdP + 32 * wd, dr);
@@ -723,8 +733,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
           pkp[i] = pack_bf16x2(p0, p1);
           pks[i] = pack_bf16x2(d0, d1);
         }
-        tmem_st16_nowait(tS + 16 * wd, pkp);    // P^T over S^T columns already read
-        tmem_st16_nowait(tdP + 16 * wd, pks);   // dS^T over dP^T columns already read
+        tmem_st16_nowait(tS + 16 * wd + 32 * half, pkp);    // P^T over this half's S^T columns, already read
+        tmem_st16_nowait(tdP + 16 * wd + 32 * half, pks);   // dS^T over this half's dP^T columns, already read
       }
       tmem_wait_st();
       tc_fence_before();
@@ -738,13 +748,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
         const uint32_t tdV = tmem + lane_off + kTdV, tdK = tmem + lane_off + kTdK;
         if (w.grow) {
           const size_t prow = (static_cast<size_t>(w.bh) * p.n_glob + w.gt * 128 + r) * p.ns_stride + w.x0 / p.split;
-          store_partial_rows<D>(p.part_a + prow * D, tdK, p.part_b + prow * D, tdV, valid);
+          const int c0 = half * (D / 64), c1 = c0 + D / 64;   // this half's 32-column chunks
+          store_partial_rows<D>(p.part_a + prow * D, tdK, p.part_b + prow * D, tdV, valid, c0, c1);
         } else {
           // staging: the first stage's Q tile (every load has landed and been consumed)
           const uint32_t stage = sQS + (warp - 4) * 4096;
           const int y0 = w.c + p.d * (w.t0 + 32 * (warp & 3));
-          store_rows_tma<D>(&p.sA, stage, tdK, p.scale, y0, w.bh, lane);
-          store_rows_tma<D>(&p.sB, stage, tdV, 1.f, y0, w.bh, lane);
+          if (D == 128 || half == 0) {
+            store_rows_tma<D>(&p.sA, stage, tdK, p.scale, y0, w.bh, lane, half);
+            store_rows_tma<D>(&p.sB, stage, tdV, 1.f, y0, w.bh, lane, half);
+          }
         }
       }
     }
