@@ -773,71 +773,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
 
 // ======================================================================== prep and reduce
 
-// One warp per (b, h, row): Delta = sum_d dO * O and lse2 = LSE * log2(e),
+// One thread per (b, h, row): Delta = sum_d dO * O and lse2 = LSE * log2(e),
 // stored class-major; rows of global positions also go to the gathered
 // global-side arrays (with their dO row).  ETC: the global-side rows come
 // from their own inputs (rows bh * N .. are the long input, then the global
 // input's rows follow in the row index).
-__global__ void bwd_prep_kernel(const BwdPrepParams p) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdPrepParams p) {
   grid_dep_launch();
-  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  // one thread per row: Delta = <dO, O> with 16-byte loads, LSE * log2(e), written class-major
   const long long n_main = static_cast<long long>(p.BH) * p.N;
   const long long n_rows = n_main + (p.etc ? static_cast<long long>(p.BH) * p.n_glob : 0);
-  const long long stride = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long row = warp_id; row < n_rows; row += stride) {
+  const int q8 = p.D / 8;
+  for (long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; row < n_rows;
+       row += static_cast<long long>(gridDim.x) * blockDim.x) {
     const bool gside = row >= n_main;   // ETC global input row
     int bh, i;
     const __nv_bfloat16 *o, *dO;
     float lse;
     if (!gside) {
       bh = static_cast<int>(row / p.N);
-      i = static_cast<int>(row % p.N);
+      i = static_cast<int>(row - static_cast<long long>(bh) * p.N);
       o = p.out + row * p.D;
       dO = p.dout + row * p.D;
       lse = p.lse[row];
     } else {
       const long long g = row - n_main;
       bh = static_cast<int>(g / p.n_glob);
-      i = static_cast<int>(g % p.n_glob);
+      i = static_cast<int>(g - static_cast<long long>(bh) * p.n_glob);
       o = p.out_g + g * p.D;
       dO = p.dout_g + g * p.D;
       lse = p.lse_g[g];
     }
-    float acc = 0.f;
-    for (int x = lane * 2; x < p.D; x += 64) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + x);
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + x);
-      acc = fmaf(__bfloat162float(a.x), __bfloat162float(b.x), acc);
-      acc = fmaf(__bfloat162float(a.y), __bfloat162float(b.y), acc);
-    }
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+    for (int x = 0; x < q8; ++x) {
+      const uint4 va = __ldg(reinterpret_cast<const uint4*>(o) + x), vb = __ldg(reinterpret_cast<const uint4*>(dO) + x);
+      const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+        const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+        a0 = fmaf(fa.x, fb.x, a0);
+        a1 = fmaf(fa.y, fb.y, a1);
+      }
+    }
+    const float acc = a0 + a1;
     const float l2 = lse * kLog2e;
     if (gside) {
-      if (lane == 0) {
-        p.lse2g[static_cast<size_t>(bh) * p.gpad + i] = l2;
-        p.deltag[static_cast<size_t>(bh) * p.gpad + i] = acc;
-      }
+      p.lse2g[static_cast<size_t>(bh) * p.gpad + i] = l2;
+      p.deltag[static_cast<size_t>(bh) * p.gpad + i] = acc;
       continue;
     }
     const int d = p.dil[bh % p.H];
     const int M = bwd_class_stride(p.N, d);
-    if (lane == 0) {
-      const size_t ix = static_cast<size_t>(bh) * p.CM + static_cast<size_t>(i % d) * M + i / d;
-      p.lse2[ix] = l2;
-      p.delta[ix] = acc;
-    }
+    const int cls = i % d;
+    const size_t ix = static_cast<size_t>(bh) * p.CM + static_cast<size_t>(cls) * M + (i - cls) / d;
+    p.lse2[ix] = l2;
+    p.delta[ix] = acc;
     if (p.gidx != nullptr) {
       const int gi = __ldg(p.gcount + i);
       if (__ldg(p.gcount + i + 1) != gi) {   // position i is global number gi
-        if (lane == 0) {
-          p.lse2g[static_cast<size_t>(bh) * p.gpad + gi] = l2;
-          p.deltag[static_cast<size_t>(bh) * p.gpad + gi] = acc;
-        }
-        const size_t dst = (static_cast<size_t>(bh) * p.n_glob + gi) * p.D;
-        for (int x = lane * 2; x < p.D; x += 64)
-          *reinterpret_cast<__nv_bfloat162*>(p.dog + dst + x) = *reinterpret_cast<const __nv_bfloat162*>(dO + x);
+        p.lse2g[static_cast<size_t>(bh) * p.gpad + gi] = l2;
+        p.deltag[static_cast<size_t>(bh) * p.gpad + gi] = acc;
+        uint4* dst = reinterpret_cast<uint4*>(p.dog + (static_cast<size_t>(bh) * p.n_glob + gi) * p.D);
+        for (int x = 0; x < q8; ++x) dst[x] = __ldg(reinterpret_cast<const uint4*>(dO) + x);
       }
     }
   }
@@ -875,8 +874,8 @@ cudaError_t set_smem_attrs() {
 
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.BH) * p.N + (p.etc ? static_cast<long long>(p.BH) * p.n_glob : 0);
-  long long blocks = (rows * 32 + 255) / 256;
-  if (blocks > 8192) blocks = 8192;
+  long long blocks = (rows + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
   if (blocks < 1) blocks = 1;
   bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
   return cudaGetLastError();

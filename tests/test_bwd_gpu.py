@@ -21,12 +21,25 @@ def W(name, dtype, B, H, N, D, wl, wr, dil=(), causal=False, g=None, nrand=0, se
     return Workload(name, dtype, B, H, N, D, wl, wr, tuple(dil), causal, g, nrand, seed=seed, **kw)
 
 
-def grad_errors(name, got, ref):
-    """max |err| / max |ref| and mean |err| / mean |ref| of one gradient."""
+def grad_errors(name, got, ref, floor=1e-30):
+    """max |err| / max |ref| and mean |err| / mean |ref| of one gradient.
+
+    floor: the smallest reference scale used.  A gradient can be exactly zero
+    (a row whose only key is itself has P = 1, dP = Delta, dS = 0), and then
+    the kernel's fp32 rounding of dP - Delta is to be compared with the size of
+    one term of that gradient, not with zero (see ``term_floors``)."""
     g = got.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(g).all(), f"{name}: non-finite gradient"
     err = np.abs(g - ref)
-    return err.max() / max(np.abs(ref).max(), 1e-30), err.mean() / max(np.abs(ref).mean(), 1e-30)
+    return err.max() / max(np.abs(ref).max(), floor), err.mean() / max(np.abs(ref).mean(), floor)
+
+
+def term_floors(q, k, v, dout, D, scale):
+    """1e-4 of the largest single term of dQ (s dS_ij k_j, |dS| <= D |dO| |v|), dK and dV (P_ij dO_i)."""
+    s = scale if scale else 1.0 / np.sqrt(D)
+    mx = lambda x: float(np.abs(x).max())
+    base = s * D * mx(dout) * mx(v)
+    return {"dq": 1e-4 * base * mx(k), "dk": 1e-4 * base * mx(q), "dv": 1e-4 * mx(dout)}
 
 
 def run_bwd(lg, w, scale=None):
@@ -43,7 +56,8 @@ def run_bwd(lg, w, scale=None):
     assert lg.query_status(lg.attn_bwd.last_workspace) == 0
     qn, kn, vn, don = (pu.to_np32(x) for x in (inp["q"], inp["k"], inp["v"], gr["dout"]))
     rq, rk, rv = lg_oracle.attn_bwd(qn, kn, vn, don, w.w_left, w.w_right, w.dilations(), w.causal, g, scale=scale)
-    return {n: grad_errors(f"{w.name} {n}", x, r) for n, x, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv))}
+    fl = term_floors(qn, kn, vn, don, w.D, scale)
+    return {n: grad_errors(f"{w.name} {n}", x, r, fl[n]) for n, x, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv))}
 
 
 def run_etc_bwd(lg, w, scale=None):
@@ -59,7 +73,9 @@ def run_etc_bwd(lg, w, scale=None):
     npx = [pu.to_np32(inp[n]) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
     ref = lg_oracle.etc_attn_bwd(*npx, w.radius, pu.to_np32(gr["dout"]), pu.to_np32(gr["dout_g"]), scale=scale)
     names = ("dq_l", "dk_l", "dv_l", "dq_g", "dk_g", "dv_g")
-    return {n: grad_errors(f"{w.name} {n}", x, r) for n, x, r in zip(names, grads, ref)}
+    fl = term_floors(np.concatenate([npx[0], npx[3]], 2), np.concatenate([npx[1], npx[4]], 2),
+                     np.concatenate([npx[2], npx[5]], 2), pu.to_np32(gr["dout"]), w.D, scale)
+    return {n: grad_errors(f"{w.name} {n}", x, r, fl[n[:2]]) for n, x, r in zip(names, grads, ref)}
 
 
 BWD_TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 1e-2)}   # (max rel. to max |ref|, mean rel. to mean |ref|)
