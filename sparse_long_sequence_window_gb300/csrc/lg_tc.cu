@@ -309,6 +309,28 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   return upper & ~((1u << a) - 1u);
 }
 
+// Cold paths of the softmax tile loop, out of line so that the loop's code stays compact.
+// O_q *= f, 32 columns at a time (every lane of the warp calls it).
+__device__ __noinline__ void rescale_o(uint32_t tO, float f, int n32) {
+#pragma unroll 1
+  for (int cc = 0; cc < n32; ++cc) {
+    float o[32];
+    tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] *= f;
+    tmem_st32(tO + cc * 32, o);
+  }
+}
+// Columns [ca, cb) of a global tile starting at list index jj0 whose position is on the
+// stride-d lattice of pos_q, as bits of four 32-column words.
+__device__ __noinline__ uint4 lattice_bits(const int* gidx, int jj0, int ca, int cb, int pos_q, int d) {
+  uint32_t b[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
+  for (int c = ca; c < cb; ++c)
+    if ((__ldg(gidx + jj0 + c) - pos_q) % d == 0) b[c >> 5] |= 1u << (c & 31);
+  return make_uint4(b[0], b[1], b[2], b[3]);
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -804,15 +826,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
 #pragma unroll
             for (int wd = 0; wd < 4; ++wd) keep[wd] &= ~range_bits(ca, cb - 1, 32 * wd);
           } else {
-            for (int c = ca; c < cb; ++c) {
-              if ((__ldg(p.gidx + jj0 + c) - pos_q) % w.d == 0) {
-                const uint32_t bit = 1u << (c & 31);
-                if ((c >> 5) == 0) keep[0] &= ~bit;
-                else if ((c >> 5) == 1) keep[1] &= ~bit;
-                else if ((c >> 5) == 2) keep[2] &= ~bit;
-                else keep[3] &= ~bit;
-              }
-            }
+            const uint4 lb = lattice_bits(p.gidx, jj0, ca, cb, pos_q, w.d);
+            keep[0] &= ~lb.x;
+            keep[1] &= ~lb.y;
+            keep[2] &= ~lb.z;
+            keep[3] &= ~lb.w;
           }
         }
       }
@@ -881,17 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
         if (!wait_all(bar(B_PEMPTY + q), (ns - 1) & 1)) { fail(); ok = false; break; }
         tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        const float f = need_rescale ? corr : 1.f;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(tO + cc * 32, o);
-        }
-      }
+      if (__any_sync(0xffffffffu, need_rescale)) rescale_o(tO, need_rescale ? corr : 1.f, D / 32);
       tmem_st64(tP, pk);
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + q));
