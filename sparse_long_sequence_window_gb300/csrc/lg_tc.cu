@@ -50,10 +50,10 @@ constexpr int kThreads = 384;
 constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsLaunchMin = (128 * kRegsControl + 256 * kRegsSoftmax + kThreads - 1) / kThreads;
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only when the max grows more
 constexpr int kUnitSlots = 4;              // ring of claimed unit indices
 constexpr int kTailRounds = 2;             // rounds of units claimed dynamically at the end
-constexpr int kUnitReaders = 11;           // V producer + two issuing warps + eight softmax warps  // log2 units; O is rescaled only when the max grows more
+constexpr int kUnitReaders = 11;           // V producer + two issuing warps + eight softmax warps
 constexpr float kLn2 = 0.6931471805599453f;
 // Bound of the drain waits, which hold a CTA until the TMA loads and MMAs it
 // has already issued complete (always finite) before TMEM and shared memory
