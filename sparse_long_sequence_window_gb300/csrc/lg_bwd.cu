@@ -334,7 +334,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
     atomicOr(p.status, ST_TIMEOUT);
   };
   const BUnit w = decode_bwd_unit(p, blockIdx.x, false);
-  constexpr uint32_t kTS = 0, kTdP = 128, kTdQ = 256;
+  // S of key tile j in buffer j & 1 (columns 0 or 384): S of tile j + 1 is computed while
+  // the elementwise warps work on tile j, and only dP of tile j + 1 waits for them.
+  constexpr uint32_t kTS = 0, kTdP = 128, kTdQ = 256, kTS1 = 384;
+  auto s_col = [&](int j) -> uint32_t { return (j & 1) ? kTS1 : kTS; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -380,34 +383,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
       ok = false;
       return false;
     };
-    if (wait_or_fail(B_QF, 0)) {
+    // S(j) = Q K(j)^T into buffer j & 1; dP(j) = dO V(j)^T; dQ += dS(j) K(j) with dS(j) read
+    // from S(j)'s buffer.  Order per tile: S(j + 1) (its buffer was last read by dQ(j - 1),
+    // issued before it), then, once the elementwise warps are done with tile j, dQ(j) and
+    // dP(j + 1) (dP's columns are free again), then the commit that S(j + 1) and dP(j + 1)
+    // are ready.
+    auto s_mmas = [&](int j) {
+      const uint64_t dk = dK0 + (j & 1) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+        umma_bf16_ss(tmem + s_col(j), dQd + o, dk + o, kIdSS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto dp_mmas = [&](int j) {
+      const uint64_t dv = dV0 + (j & 1) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+        umma_bf16_ss(tmem + kTdP, ddO + o, dv + o, kIdSS, kk > 0 ? 1u : 0u);
+      }
+    };
+    if (wait_or_fail(B_QF, 0) && w.n_tiles > 0 && wait_or_fail(B_KVF, 0)) {
+      tc_fence_after();
+      if (leader) {
+        s_mmas(0);
+        dp_mmas(0);
+        umma_commit(bar(B_SR));
+      }
+      __syncwarp();
       for (int j = 0; j < w.n_tiles; ++j) {
         const int st = j & 1;
-        if (!wait_or_fail(B_KVF + st, (j >> 1) & 1)) break;
-        tc_fence_after();
-        if (leader) {
-          const uint64_t dk = dK0 + st * kStage, dv = dV0 + st * kStage;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-            umma_bf16_ss(tmem + kTS, dQd + o, dk + o, kIdSS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-            umma_bf16_ss(tmem + kTdP, ddO + o, dv + o, kIdSS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(B_SR));
+        const bool next = j + 1 < w.n_tiles;
+        if (next) {
+          if (!wait_or_fail(B_KVF + (st ^ 1), ((j + 1) >> 1) & 1)) break;
+          tc_fence_after();
+          if (leader) s_mmas(j + 1);
+          __syncwarp();
         }
-        __syncwarp();
         if (!wait_or_fail(B_PR, j & 1)) break;
         tc_fence_after();
         if (leader) {
           const uint64_t dkm = dKmn0 + st * kStage;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdQ, tmem + kTS + kk * 8 + (kk >= 4 ? 32 : 0), dkm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTdQ, tmem + s_col(j) + kk * 8 + (kk >= 4 ? 32 : 0), dkm + kk * 128, kIdTS,
+                         (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_KVE + st));
+          if (next) {
+            dp_mmas(j + 1);
+            umma_commit(bar(B_SR));
+          }
         }
         __syncwarp();
       }
@@ -423,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
     const int half = (warp - 4) >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_off + kTS, tdP = tmem + lane_off + kTdP, tdQ = tmem + lane_off + kTdQ;
+    const uint32_t tdP = tmem + lane_off + kTdP, tdQ = tmem + lane_off + kTdQ;
     bool valid;
     float lse2r, deltar;
     int t = 0, pos = 0;
@@ -466,6 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(const __grid_cons
       const KeepMask km = make_keep(lo, hi, ca, cb, p.gidx, o.g0, p.d, pos);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SR), j & 1, abort_flag, cap))) { fail(); ok = false; break; }
       tc_fence_after();
+      const uint32_t tS = tmem + lane_off + s_col(j);
 #pragma unroll 1
       for (int wd = 2 * half; wd < 2 * half + 2; ++wd) {
         uint32_t sr[32], dr[32];
