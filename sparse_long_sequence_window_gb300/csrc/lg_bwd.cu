@@ -585,6 +585,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
   };
   const BUnit w = decode_bwd_unit(p, blockIdx.x, true);
   constexpr uint32_t kTS = 0, kTdP = 128, kTdV = 256, kTdK = 256 + D;
+  // D = 64 leaves columns 384..511 free: S^T of query tile j in buffer j & 1 (columns 0 or
+  // 384), so S^T of tile j + 1 is computed while the elementwise warps work on tile j.
+  // D = 128 fills the 512 columns and keeps one buffer.
+  constexpr bool kDB = D == 64;
+  constexpr uint32_t kTS1 = 384;
+  auto s_col = [&](int j) -> uint32_t { return (kDB && (j & 1)) ? kTS1 : kTS; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -637,39 +643,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
       ok = false;
       return false;
     };
+    // S^T(j) = K Q(j)^T into buffer s_col(j); dP^T(j) = V dO(j)^T; then dV += P^T(j) dO(j)
+    // and dK += dS^T(j) Q(j) with P^T and dS^T read from TMEM.  D = 64 issues S^T(j + 1)
+    // before waiting for the elementwise warps on tile j (its buffer was last read by
+    // dV(j - 1), issued before it), and dP^T(j + 1) after dV(j) and dK(j).
+    auto st_mmas = [&](int j) {
+      const uint64_t dq = dQ0 + (j & 1) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+        umma_bf16_ss(tmem + s_col(j), dK + o, dq + o, kIdSS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto dpt_mmas = [&](int j) {
+      const uint64_t ddo = ddO0 + (j & 1) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+        umma_bf16_ss(tmem + kTdP, dV + o, ddo + o, kIdSS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto grad_mmas = [&](int j) {
+      const int st = j & 1;
+      const uint64_t qm = dQmn0 + st * kStage, om = ddOmn0 + st * kStage;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16_ts(tmem + kTdV, tmem + s_col(j) + kk * 8 + (kk >= 4 ? 32 : 0), om + kk * 128, kIdTS,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16_ts(tmem + kTdK, tmem + kTdP + kk * 8 + (kk >= 4 ? 32 : 0), qm + kk * 128, kIdTS,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(bar(B_QE + st));
+    };
     if (wait_or_fail(B_KVF, 0)) {
-      for (int j = 0; j < w.n_tiles; ++j) {
-        const int st = j & 1;
-        if (!wait_or_fail(B_QF + st, (j >> 1) & 1)) break;
-        tc_fence_after();
-        if (leader) {
-          const uint64_t dq = dQ0 + st * kStage, ddo = ddO0 + st * kStage;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-            umma_bf16_ss(tmem + kTS, dK + o, dq + o, kIdSS, kk > 0 ? 1u : 0u);
+      if constexpr (kDB) {
+        if (w.n_tiles > 0 && wait_or_fail(B_QF, 0)) {
+          tc_fence_after();
+          if (leader) {
+            st_mmas(0);
+            dpt_mmas(0);
+            umma_commit(bar(B_SR));
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-            umma_bf16_ss(tmem + kTdP, dV + o, ddo + o, kIdSS, kk > 0 ? 1u : 0u);
+          __syncwarp();
+          for (int j = 0; j < w.n_tiles; ++j) {
+            const bool next = j + 1 < w.n_tiles;
+            if (next) {
+              if (!wait_or_fail(B_QF + ((j + 1) & 1), ((j + 1) >> 1) & 1)) break;
+              tc_fence_after();
+              if (leader) st_mmas(j + 1);
+              __syncwarp();
+            }
+            if (!wait_or_fail(B_PR, j & 1)) break;
+            tc_fence_after();
+            if (leader) {
+              grad_mmas(j);
+              if (next) {
+                dpt_mmas(j + 1);
+                umma_commit(bar(B_SR));
+              }
+            }
+            __syncwarp();
           }
-          umma_commit(bar(B_SR));
         }
-        __syncwarp();
-        if (!wait_or_fail(B_PR, j & 1)) break;
-        tc_fence_after();
-        if (leader) {
-          const uint64_t qm = dQmn0 + st * kStage, om = ddOmn0 + st * kStage;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdV, tmem + kTS + kk * 8 + (kk >= 4 ? 32 : 0), om + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kTdK, tmem + kTdP + kk * 8 + (kk >= 4 ? 32 : 0), qm + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(B_QE + st));
+      } else {
+        for (int j = 0; j < w.n_tiles; ++j) {
+          const int st = j & 1;
+          if (!wait_or_fail(B_QF + st, (j >> 1) & 1)) break;
+          tc_fence_after();
+          if (leader) {
+            st_mmas(j);
+            dpt_mmas(j);
+            umma_commit(bar(B_SR));
+          }
+          __syncwarp();
+          if (!wait_or_fail(B_PR, j & 1)) break;
+          tc_fence_after();
+          if (leader) grad_mmas(j);
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     if (leader) umma_commit(bar(B_DONE));
@@ -683,7 +735,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
     const int half = (warp - 4) >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_off + kTS, tdP = tmem + lane_off + kTdP;
+    const uint32_t tdP = tmem + lane_off + kTdP;
     bool valid;
     int u = 0, pos = 0;
     if (w.grow) {
@@ -726,6 +778,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(const __grid_con
         break;
       }
       tc_fence_after();
+      const uint32_t tS = tmem + lane_off + s_col(j);
       const float* vl = reinterpret_cast<const float*>(smem + 2 * C::kTileBytes + st * C::kKVStage + 2 * C::kTileBytes);
       const float* vd = vl + 128;
 #pragma unroll 1
