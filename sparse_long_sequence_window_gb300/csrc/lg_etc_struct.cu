@@ -195,8 +195,20 @@ struct EsCfg {
   static constexpr int kMisc = 8192;
   static constexpr int kOffQa = kOffMisc + kMisc;        // q . a^K of the tile's rows, [label][row]
   static constexpr int kMaxLabels = D == 64 ? kEsMaxLabels : 40;   // what fits in 227 KB next to D = 128 tiles
-  static constexpr int kSmem = kOffQa + kMaxLabels * 512 + 1024;   // + alignment slack
+  // D = 64: the table has a row for every 7-bit label, so that any code byte's label reads
+  // inside it without a clamp (labels past the vocabulary are reported by the packing kernel);
+  // D = 128: kMaxLabels rows, the label clamped.
+  static constexpr int kTableLabels = D == 64 ? 128 : kMaxLabels;
+  static constexpr int kSmem = kOffQa + kTableLabels * 512 + 1024;   // + alignment slack
 };
+
+// Bits e of a 32-column chunk with lo <= e <= hi (any lo, hi; empty when lo > hi).
+__device__ __forceinline__ uint32_t es_range_bits(int lo, int hi) {
+  const int a = max(lo, 0), b = min(hi, 31);
+  if (a > b) return 0u;
+  const uint32_t upper = (b >= 31) ? 0xFFFFFFFFu : ((1u << (b + 1)) - 1u);
+  return upper & ~((1u << a) - 1u);
+}
 
 template <int D>
 __device__ __forceinline__ void es_load_tile(const CUtensorMap* map, int y0, int bh, uint32_t dst, uint32_t bar) {
@@ -367,6 +379,7 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
     const bool valid = qi < (glob ? g.G : g.L);
     const float cs = p.scale_log2;
     const int vmax = p.V - 1;
+    const uint32_t qa_row = sQa + r * 4;     // this row's entry of label 0 in the q . a^K table
     // The -C of a blocked edge never enters the fp32 logits: while a row has
     // seen only blocked edges ("blocked frame") their weights are exp2(x - m)
     // of the unshifted logits (the common -C cancels); once it has an allowed
@@ -391,7 +404,7 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
         for (int e = 0; e < 32; ++e)
           if (32 * half + e < p.V) tab[(32 * half + e) * 128 + r] = qa[e] * cs;
       }
-      named_bar_sync(1, 256);
+      named_bar_sync(2 + (warp & 3), 64);   // the two warps on these rows
     }
     for (int j = 0; j < n_steps; ++j) {
       // this row's keys in tile j: columns [lo, hi] of the full tile
@@ -429,20 +442,23 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
                        : "=r"(cw[4 * h]), "=r"(cw[4 * h + 1]), "=r"(cw[4 * h + 2]), "=r"(cw[4 * h + 3])
                        : "r"(a));
         }
-        const int clo = lo - 32 * c4, chi = hi - 32 * c4;
+        // this row's keys of the chunk as a bit mask (one bit test per edge below)
+        const uint32_t kmask = es_range_bits(lo - 32 * c4, hi - 32 * c4);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const uint32_t code = (cw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-          float v = s[e] * cs;
+          float v;
           if (BIAS) {
-            const int label = min(static_cast<int>(code & 127u), vmax);
+            const uint32_t label = D == 64 ? (code & 127u) : min(code & 127u, static_cast<uint32_t>(vmax));
             float qa;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qa) : "r"(sQa + (label * 128 + r) * 4));
-            v += qa;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qa) : "r"(qa_row + label * 512));
+            v = fmaf(s[e], cs, qa);
+          } else {
+            v = s[e] * cs;
           }
           const uint32_t blk = code >> 7;
           v = __uint_as_float((__float_as_uint(v) & ~1u) | blk);
-          const float xv = (e >= clo && e <= chi) ? v : -INFINITY;
+          const float xv = ((kmask >> e) & 1u) ? v : -INFINITY;
           x[32 * c2 + e] = xv;
           tall = fmaxf(tall, xv);
           ta = fmaxf(ta, blk ? -INFINITY : xv);
@@ -451,7 +467,7 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
       // combine the two halves' maxima
       x_allowed[(j & 1) * 256 + half * 128 + r] = ta;
       x_all[(j & 1) * 256 + half * 128 + r] = tall;
-      named_bar_sync(1, 256);
+      named_bar_sync(2 + (warp & 3), 64);   // the two warps on these rows
       ta = fmaxf(ta, x_allowed[(j & 1) * 256 + (1 - half) * 128 + r]);
       tall = fmaxf(tall, x_all[(j & 1) * 256 + (1 - half) * 128 + r]);
       if (!ok) continue;
@@ -486,29 +502,36 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
         }
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      float sum = 0.f;
+      const uint64_t negm2 = f2_pack(-m_sub, -m_sub);
+      const uint32_t tag = has_allowed ? 1u : 0u;   // blocked edges weigh 0 once the row has an allowed one
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int wd = 0; wd < 2; ++wd) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float x0 = x[32 * wd + 2 * i], x1 = x[32 * wd + 2 * i + 1];
-          float p0 = ex2_approx(x0 - m_sub), p1 = ex2_approx(x1 - m_sub);
-          p0 = (has_allowed && (__float_as_uint(x0) & 1u)) ? 0.f : p0;
-          p1 = (has_allowed && (__float_as_uint(x1) & 1u)) ? 0.f : p1;
-          sum += p0 + p1;
+          float a0, a1;
+          f2_unpack(f2_add(f2_pack(x0, x1), negm2), a0, a1);
+          float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+          p0 = (__float_as_uint(x0) & tag) ? 0.f : p0;
+          p1 = (__float_as_uint(x1) & tag) ? 0.f : p1;
+          sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16_nowait(tS + 64 * half + 16 * wd, pk);   // P of this half's keys over its own S columns
       }
-      l_half += sum;
+      float s0, s1, s2, s3;
+      f2_unpack(sum2[0], s0, s1);
+      f2_unpack(sum2[1], s2, s3);
+      l_half += (s0 + s1) + (s2 + s3);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PF + (j & 1)));
     }
     // the row's sum: both halves' partial sums
     x_sum[half * 128 + r] = l_half;
-    named_bar_sync(1, 256);
+    named_bar_sync(2 + (warp & 3), 64);   // the two warps on these rows
     const float l_run = l_half + x_sum[(1 - half) * 128 + r];
     if (ok) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, abort_flag, cap))) {
