@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
       const uint32_t crow = stage(j & 1) + 2 * C::kTile + r * 128;
       float x[64];
       float ta = -INFINITY, tall = -INFINITY;   // maxima over this half's allowed / member edges
+      uint32_t blk_any = 0u;                    // blocked bits of this row's code bytes
 #pragma unroll
       for (int c2 = 0; c2 < 2 && ok; ++c2) {
         const int c4 = 2 * half + c2;          // 32-column chunk of the tile
@@ -442,6 +443,8 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
                        : "=r"(cw[4 * h]), "=r"(cw[4 * h + 1]), "=r"(cw[4 * h + 2]), "=r"(cw[4 * h + 3])
                        : "r"(a));
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) blk_any |= cw[k];
         // this row's keys of the chunk as a bit mask (one bit test per edge below)
         const uint32_t kmask = es_range_bits(lo - 32 * c4, hi - 32 * c4);
 #pragma unroll
@@ -461,8 +464,15 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
           const float xv = ((kmask >> e) & 1u) ? v : -INFINITY;
           x[32 * c2 + e] = xv;
           tall = fmaxf(tall, xv);
-          ta = fmaxf(ta, blk ? -INFINITY : xv);
         }
+      }
+      // The maximum over the allowed edges differs only where a code byte is blocked (tagged
+      // logits: lowest bit 1); taken in a second loop only for such warps.
+      ta = tall;
+      if (__any_sync(0xffffffffu, (blk_any & 0x80808080u) != 0u)) {
+        ta = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) ta = fmaxf(ta, (__float_as_uint(x[e]) & 1u) ? -INFINITY : x[e]);
       }
       // combine the two halves' maxima
       x_allowed[(j & 1) * 256 + half * 128 + r] = ta;
