@@ -449,17 +449,24 @@ __global__ void __launch_bounds__(kEsThreads, 1) es_attn_kernel(const __grid_con
         const uint32_t kmask = es_range_bits(lo - 32 * c4, hi - 32 * c4);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const uint32_t code = (cw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+          const uint32_t wv = cw[e >> 2];
+          const int kByte = 8 * (e & 3);   // a constant once the loop is unrolled
           float v;
           if (BIAS) {
-            const uint32_t label = D == 64 ? (code & 127u) : min(code & 127u, static_cast<uint32_t>(vmax));
+            // the label's table row: (label << 9) taken straight from the code word
+            uint32_t off;
+            if constexpr (D == 64) {
+              off = (kByte >= 9 ? (wv >> (kByte - 9)) : (wv << (9 - kByte))) & (127u << 9);
+            } else {
+              off = min((wv >> kByte) & 127u, static_cast<uint32_t>(vmax)) << 9;
+            }
             float qa;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qa) : "r"(qa_row + label * 512));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qa) : "r"(qa_row + off));
             v = fmaf(s[e], cs, qa);
           } else {
             v = s[e] * cs;
           }
-          const uint32_t blk = code >> 7;
+          const uint32_t blk = (wv >> (kByte + 7)) & 1u;
           v = __uint_as_float((__float_as_uint(v) & ~1u) | blk);
           const float xv = ((kmask >> e) & 1u) ? v : -INFINITY;
           x[32 * c2 + e] = xv;
