@@ -16,19 +16,22 @@
 // "ETC: Encoding Long and Structured Inputs in Transformers", section 3.4,
 // "Global-Local Attention".
 //
-// Two kernels, one CTA per work unit (256 threads: warp 0 loads tiles with
-// TMA, warp 1 owns TMEM and issues the MMAs from one elected lane, warps 4..7
-// are the elementwise warpgroup with one thread per TMEM lane):
+// Two kernels, one CTA per work unit (384 threads: warp 0 loads tiles with
+// TMA, warp 1 owns TMEM and issues the MMAs from one elected lane, warps 4..11
+// are two elementwise warpgroups, one thread per TMEM lane in each, taking the
+// two 64-column halves of every tile):
 //  * bwd_q_kernel: TMEM rows are 128 queries.  Per key tile: S = Q K^T and
-//    dP = dO V^T (TMEM), then the warpgroup writes dS (bf16) over S, then
-//    dQ += dS K (A operand read from TMEM).  Band units: a query tile of one
+//    dP = dO V^T (TMEM; S alternates between two buffers, so S of the next key
+//    tile is computed during this tile's elementwise step), then the warpgroups
+//    write dS (bf16) over S, then dQ += dS K (A operand read from TMEM).  Band units: a query tile of one
 //    dilation residue class against its band key tiles and the global-key
 //    tiles (global keys inside the band masked there, as in the forward).
 //    Global-row units: 128 global queries against a split of all key tiles,
 //    writing partial sums of dQ.
 //  * bwd_kv_kernel: TMEM rows are 128 keys.  Per query tile: S^T = K Q^T and
-//    dP^T = V dO^T, then the warpgroup writes P^T over S^T and dS^T over
-//    dP^T, then dV += P^T dO and dK += dS^T Q.  Band units: a key tile of one
+//    dP^T = V dO^T (at D = 64 S^T alternates between two buffers as S does
+//    above), then the warpgroups write P^T over S^T and dS^T over dP^T, then
+//    dV += P^T dO and dK += dS^T Q.  Band units: a key tile of one
 //    residue class against the query tiles whose windows reach it and the
 //    global-query tiles (a global row whose band already holds the key is
 //    masked there, so every pair counts once).  Global-key units: 128 global
