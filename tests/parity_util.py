@@ -35,11 +35,16 @@ def compare(name, dtype, out_gpu, lse_gpu, out_ref, lse_ref):
     return float(err.max()), float(err.mean()), float(lerr.max())
 
 
-def run_longformer(lg, w: workloads.Workload, rows=None, scale=None):
+def run_longformer(lg, w: workloads.Workload, rows=None, scale=None, key_ramp=None):
     """CUDA path vs oracle for a (non-ETC) workload; rows=None compares every row.
 
-    scale: the logit scale passed to both sides (None: the default 1/sqrt(D))."""
+    scale: the logit scale passed to both sides (None: the default 1/sqrt(D)).
+    key_ramp: if given, key n is multiplied by 1 + key_ramp * n / N (rounded back to the
+    input dtype; both sides get the same keys), so the logits grow along the sequence."""
     inp = workloads.make_inputs(w)
+    if key_ramp is not None:
+        ramp = 1.0 + key_ramp * torch.arange(w.N, dtype=torch.float32) / w.N
+        inp["k"] = (inp["k"].float() * ramp[None, None, :, None]).to(inp["k"].dtype)
     dev = torch.device("cuda")
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     g = inp["global_idx"]

@@ -76,6 +76,21 @@ BF16_CASES = [
 ]
 
 
+# Keys whose magnitude grows 30-fold along the sequence: every new key tile raises the row
+# maximum past the lazy-rescale threshold (2^8), so O is rescaled on nearly every tile, a
+# path that N(0, 1) inputs rarely take; band rows, global-query rows and causal rows.
+RESCALE_CASES = [
+    W("bf16 rising keys D64 dilated + globals", "bf16", 1, 2, 1100, 64, 300, 300, (1, 2), False, (0, 700)),
+    W("bf16 rising keys D128 causal", "bf16", 1, 2, 900, 128, 400, 0, (), True),
+    W("bf16 rising keys D128 + 130 globals", "bf16", 1, 1, 1500, 128, 128, 128, (), False, None, 130),
+]
+
+
+@pytest.mark.parametrize("w", RESCALE_CASES, ids=lambda w: w.name)
+def test_bf16_running_max_rescales(cuda_lib, w):
+    pu.run_longformer(cuda_lib, w, key_ramp=30.0)
+
+
 @pytest.mark.parametrize("w", BF16_CASES, ids=lambda w: w.name)
 def test_bf16_small(cuda_lib, w):
     pu.run_longformer(cuda_lib, w)
