@@ -35,8 +35,14 @@ def random_codes(w, V, p_block, seed):
     return {"code_l2l": c(B, L, 2 * r + 1), "code_l2g": c(B, L, G), "code_g2l": c(B, G, L), "code_g2g": c(B, G, G)}
 
 
-def run_case(lg, w, codes, rel, rows=None, scale=None):
+def run_case(lg, w, codes, rel, rows=None, scale=None, key_ramp=None):
     inp = workloads.make_inputs(w)
+    if key_ramp is not None:
+        # long key n times 1 + key_ramp * n / L, global key i times 1 + key_ramp * i / G (both
+        # sides get the same keys): the row maximum keeps growing along the key tiles
+        for n, cnt in (("k", w.N), ("k_g", w.etc_G)):
+            ramp = 1.0 + key_ramp * torch.arange(cnt, dtype=torch.float32) / cnt
+            inp[n] = (inp[n].float() * ramp[None, None, :, None]).to(inp[n].dtype)
     dev = torch.device("cuda")
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "q_g", "k_g", "v_g")}
     cd = {n: (None if c is None else torch.from_numpy(np.ascontiguousarray(c)).to(dev)) for n, c in codes.items()}
@@ -136,3 +142,13 @@ def test_etc_struct_bad_label_is_reported(cuda_lib):
     cd["code_l2g"] = torch.from_numpy(codes["code_l2g"]).cuda()
     lg.etc_struct_attn_fwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], w.radius, rel, **cd, workspace=ws)
     assert lg.query_status(ws) == 0
+
+
+def test_etc_struct_running_max_rescales(cuda_lib):
+    """Keys growing 30-fold along both key sequences, labels and blocked edges at random: the
+    running maximum passes the rescale threshold on most key tiles, so O is rescaled in TMEM
+    (a path N(0, 1) inputs rarely take), in long and global rows, at D 64 and 128."""
+    for w, V, p_block in ((E("rising keys D64", 1, 2, 520, 150, 64, 60, seed=470), 12, 0.2),
+                          (E("rising keys D128", 1, 2, 400, 40, 128, 90, seed=471), 9, 0.1)):
+        codes = random_codes(w, V, p_block, seed=w.seed + 1)
+        run_case(cuda_lib, w, codes, rel_for(w, V, w.seed + 2), key_ramp=30.0)
