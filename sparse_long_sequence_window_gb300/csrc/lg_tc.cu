@@ -26,14 +26,13 @@
 // Warp roles (384 threads): warp 0 issues the K loads, warp 2 the V loads
 // (TMA); warp 1 owns TMEM and issues the MMAs and Q loads of query tile 0,
 // warp 3 those of tile 1; warps 4..7 and 8..11 are the two softmax
-// warpgroups (one thread per query row = TMEM lane).  TMEM holds S_q (128
-// fp32 columns), P_q (packed bf16, over the first 64 columns of S_q for
-// D = 128, in its own columns for D = 64) and O_q (D columns) for both tiles.
-// For D = 128 the MMA order per key tile j is PV_0(j-1), QK_0(j), PV_1(j-1),
-// QK_1(j), so the tensor core works on one tile while the other tile's
-// softmax runs; because the MMAs of one thread execute in order, the
-// completion of QK_q(j) also means PV_q(j-1) is done, and the softmax may
-// rescale O_q and overwrite S_q with P_q without further waits.
+// warpgroups (one thread per query row = TMEM lane).  For D = 128 warp 0
+// issues both K and V into one ring.  TMEM holds S_q (128 fp32 columns) and O_q (D columns) for
+// both tiles, and for D = 64 also P_q (packed bf16, 64 columns); for D = 128
+// P_q is in shared memory.  S_q takes the next key tile's QK as soon as the
+// softmax has read it, so the tensor core computes S_q(j+1) while the
+// softmax of tile j runs, and PV_q(j) follows once P_q(j) is written; the
+// softmax waits for PV_q(j) before it rescales O_q or writes P_q(j+1).
 #include <atomic>
 #include <mutex>
 
@@ -53,7 +52,6 @@ constexpr int kRegsLaunchMin = (128 * kRegsControl + 256 * kRegsSoftmax + kThrea
 constexpr float kRescaleThreshold = 8.0f;  // log2 units; O is rescaled only when the max grows more
 constexpr int kUnitSlots = 4;              // ring of claimed unit indices
 constexpr int kTailRounds = 2;             // rounds of units claimed dynamically at the end
-constexpr int kUnitReaders = 11;           // V producer + two issuing warps + eight softmax warps
 constexpr float kLn2 = 0.6931471805599453f;
 // Bound of the drain waits, which hold a CTA until the TMA loads and MMAs it
 // has already issued complete (always finite) before TMEM and shared memory
@@ -61,31 +59,39 @@ constexpr float kLn2 = 0.6931471805599453f;
 // work waits (which a caller may shorten).
 constexpr long long kDrainCap = 4000000000LL;
 
-#ifndef LG_TC_KSTAGES128
-#define LG_TC_KSTAGES128 2
-#endif
-
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kTileM * D * 2;      // 128 rows x D bf16
-  static constexpr int kKStages = (D == 64) ? 4 : LG_TC_KSTAGES128;
-  static constexpr int kVStages = (D == 64) ? 4 : 2;
+  // Where P goes, so that QK_q of the next key tile can overwrite S_q as soon
+  // as the softmax has read it (S, P and O of two query tiles do not fit the
+  // 512 TMEM columns twice over).  D = 64: P_q in its own 64 TMEM columns.
+  // D = 128: P_q in shared memory, one 32 KB buffer per query tile; K and V
+  // then share one ring of three tiles, loaded in the order the MMAs take
+  // them (K(0), then K(j) and V(j - 1) for each later j, then V(last)), and
+  // the epilogue stages O in the query tile's own P buffer.
+  static constexpr bool kSplitP = (D == 64);
+  static constexpr bool kPSmem = (D == 128);
+  static constexpr int kKStages = kPSmem ? 3 : 4;        // D = 128: the shared K/V ring
+  static constexpr int kVStages = kPSmem ? 0 : 4;
   static constexpr int kOffQ = 0;                        // two query tiles
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // output staging, 4 KB per softmax warp
-  static constexpr int kOffMisc = kOffStage + 8 * 4096;
+  // D = 64: output staging, 4 KB per softmax warp; D = 128: P_0 and P_1.
+  static constexpr int kOffStage = kOffV + kVStages * kTileBytes;
+  static constexpr int kPBytes = kTileM * kTileN * 2;
+  static constexpr int kOffMisc = kOffStage + (kPSmem ? 2 * kPBytes : 8 * 4096);
   static constexpr int kMiscBytes = 1024;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
-  // TMEM columns.  D = 128: S_q at 128 q (P_q over its first 64 columns), O_q
-  // at 256 + 128 q.  D = 64: S_q at 128 q, P_q in its own 64 columns at
-  // 256 + 64 q, O_q at 384 + 64 q, so QK_q of the next key tile can run while
-  // the softmax of the current one is still writing P.
-  static constexpr bool kSplitP = (D == 64);
+  // Readers of a unit slot: both issuing warps, the eight softmax warps and
+  // (two rings) the V producer.
+  static constexpr int kUnitReaders = kPSmem ? 10 : 11;
+  // TMEM columns: S_q at 128 q; D = 64: P_q at 256 + 64 q, O_q at 384 + 64 q;
+  // D = 128: O_q at 256 + 128 q.
   static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColP = kSplitP ? 256 : 0;
-  static constexpr uint32_t kPStride = kSplitP ? 64 : 128;
+  static constexpr uint32_t kColP = 256;
+  static constexpr uint32_t kPStride = 64;
   static constexpr uint32_t kColO = kSplitP ? 384 : 256;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 // Rows one strided TMA box delivers for a dilation d (box height R*d <= 256).
@@ -378,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   static_assert(NBARS * 8 <= 512, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
-  volatile int* issued = reinterpret_cast<volatile int*>(misc + 520);  // last key tile each issuer issued a QK for
   volatile int* unit_ring = reinterpret_cast<volatile int*>(misc + 528);  // claimed unit indices
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
@@ -386,17 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    issued[0] = -1;
-    issued[1] = -1;
     for (int i = 0; i < NBARS; ++i) {
       uint32_t count = 1;
       if (i == B_PFULL || i == B_PFULL + 1 || i == B_OFREE || i == B_OFREE + 1 || i == B_SEMPTY ||
           i == B_SEMPTY + 1)
         count = 128;
-      // K/V stages are released by both MMA issuers (one arrival each).
+      // K/V stages are released by both MMA issuers (one arrival each; each
+      // issuer waits on every stage it releases, so none falls two phases behind).
       if ((i >= B_KEMPTY && i < B_KEMPTY + KS) || (i >= B_VEMPTY && i < B_VEMPTY + VS)) count = 2;
-      // A unit slot is read by the V producer, both issuing warps and the eight softmax warps.
-      if (i >= B_UEMPTY && i < B_UEMPTY + kUnitSlots) count = kUnitReaders;
+      // A unit slot is read by each of its readers once.
+      if (i >= B_UEMPTY && i < B_UEMPTY + kUnitSlots) count = C::kUnitReaders;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -448,8 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ K and V producers
     // Warp 0 loads the K ring, warp 2 the V ring, over all units of this CTA
-    // (one global tile counter, so a ring never drains between units).
-    if (lane == 0) {
+    // (one global tile counter, so a ring never drains between units).  With
+    // the shared K/V ring (D = 128) warp 0 loads both, warp 2 idles.
+    if (lane == 0 && !(C::kPSmem && warp == 2)) {
       const bool is_k = (warp == 0);
       const int S = is_k ? KS : VS;
       const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
@@ -486,21 +491,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           prefetch_unit(p, un);   // every role decodes it at its next unit
         }
         const Unit w = decode_unit(p, u);
-        // (p.withhold: a test of the timeout path; no load is issued, so the
-        // consumers' first wait runs out with nothing in flight.)
-        for (int j = 0; j < w.n_tiles && !p.withhold; ++j, ++g) {
+        // Tile j of the unit (K or V) into the next ring slot.
+        auto put = [&](int j, bool kk) -> bool {
           const CUtensorMap* m;
           bool strided;
           int y;
-          tile_source(p, w, j, is_k, gt_src, m, strided, y);
+          tile_source(p, w, j, kk, gt_src, m, strided, y);
           const int st = g % S;
-          if (g >= S && !mbar_wait(bar(b_empty + st), ((g / S) - 1) & 1, abort_flag, cap)) { fail(); ok = false; break; }
+          if (g >= S && !mbar_wait(bar(b_empty + st), ((g / S) - 1) & 1, abort_flag, cap)) return false;
           mbar_arrive_expect_tx(bar(b_full + st), C::kTileBytes);
           load_tile<D>(m, strided, strided ? w.d : 1, y, w.bh, ring + st * C::kTileBytes, bar(b_full + st));
-          issued = g + 1;
-          // At the start of a launch every CTA wants its first tiles at once:
-          // the CTA's first tile lands before the rest of the ring is
-          // requested, so that it does not queue behind the others' prefetches.
+          issued = ++g;
+          return true;
+        };
+        // (p.withhold: a test of the timeout path; no load is issued, so the
+        // consumers' first wait runs out with nothing in flight.)
+        if (C::kPSmem) {
+          // The shared ring, in the order the MMAs take the tiles: K(x), then V(x - 1).
+          for (int x = 0; x <= w.n_tiles && !p.withhold; ++x) {
+            if (x < w.n_tiles && !put(x, true)) { fail(); ok = false; break; }
+            if (x >= 1 && !put(x - 1, false)) { fail(); ok = false; break; }
+          }
+        } else {
+          for (int j = 0; j < w.n_tiles && !p.withhold; ++j) {
+            if (!put(j, is_k)) { fail(); ok = false; break; }
+          }
         }
         if (ok && !is_k && !take(k + 1, un)) { fail(); ok = false; }
         u = un;
@@ -516,29 +531,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     // issuing warp runs its loop converged (every lane waits, so the loop
     // state stays warp-uniform) and one elected lane issues every MMA, commit,
     // arrival and Q load (the same lane throughout: tcgen05 ordering and
-    // commit tracking are per thread).  Per key tile j a tile's group is
-    // PV_q(j-1) then QK_q(j).  The groups alternate between the tiles on key
-    // tiles both use (tile 1's group for j after tile 0's, tile 0's group for
-    // j + 1 after tile 1's), so one tile's softmax overlaps the other tile's
-    // MMAs.  An issuer first waits for its K and V tiles, the O slot and its
-    // Q tile, then for its turn (a monotonic counter in shared memory, so no
-    // phase can alias), and for its P last, which is usually the latest, so
-    // little is left between P and the first MMA.  Every K/V full phase is
-    // observed by both issuers in order (a parity wait is only sound once the
-    // barrier's previous phase has been seen); a tile an issuer does not use
-    // is released by it at once, a used one after its MMAs (commit).  The
-    // issuer reloads its Q slot for the next unit as soon as its last QK of
-    // the unit has completed, and a unit's first PV (which overwrites O)
-    // waits until the softmax warpgroup has read the previous unit's O.  For
-    // D = 64 (P in its own columns) a tile's QK_q(j) goes first, as soon as
-    // the softmax has read S_q(j-1), and PV_q(j-1) follows once P_q(j-1) is
-    // written; the tiles do not take turns there.
+    // commit tracking are per thread).  A tile's QK_q(j) goes first, as soon
+    // as the softmax has read S_q of its previous tile, and the PV of that
+    // previous tile follows once its P_q is written; the two issuers do not
+    // wait for each other, so one tile's softmax overlaps the other tile's
+    // MMAs.  Every ring phase is observed by both issuers in the order the
+    // producer fills the ring (a parity wait is only sound once the barrier's
+    // previous phase has been seen); a tile an issuer does not use is
+    // released by it at once, a used one after its MMAs (commit).  The issuer
+    // reloads its Q slot for the next unit as soon as its last QK of the unit
+    // has completed, and a unit's first PV (which overwrites O) waits until
+    // the softmax warpgroup has read the previous unit's O.
     // Every descriptor is precomputed: a K-major step adds 32 B (2 in 16-B
     // units) inside a 128-B row and 16 KB per 64-column block, an MN-major V
     // step adds 2 KB, a stage adds one tile; shared-memory addresses stay
     // below 256 KB, so the additions never carry out of the 14-bit address
     // field.
-    static_assert((VS & (VS - 1)) == 0, "V ring depth must be a power of two");
     constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, true);
     constexpr uint64_t kStage = C::kTileBytes >> 4;
@@ -546,11 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     const bool leader = elect_one();
     const uint64_t dQ = sdesc_sw128(sQ + q * C::kTileBytes, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(sV, kTileN * 128, 1024);
+    const uint64_t dV0 = sdesc_sw128(C::kPSmem ? sK : sV, kTileN * 128, 1024);
+    const uint64_t dP = sdesc_sw128(sbase + C::kOffStage + q * C::kPBytes, 16, 1024);   // P_q in shared memory
     const uint32_t tS = tmem + C::kColS + q * 128;
-    const uint32_t tP = tmem + C::kColP + q * C::kPStride;
+    const uint32_t tP = tmem + C::kColP + q * C::kPStride;                             // P_q in TMEM
     const uint32_t tO = tmem + C::kColO + q * D;
-    int g = 0, ks = 0, kph = 0;   // key tiles seen (all units), K stage of tile g and its phase parity
+    int g = 0, ks = 0, kph = 0;   // two rings: key tiles seen (all units), K stage of tile g and its phase parity
+    int gr = 0;                   // shared ring: loads seen (all units)
     int ns = 0;                   // QKs issued
     int npv = 0;                  // PVs issued
     int nact = 0;                 // units in which this query tile was active
@@ -581,32 +591,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const int un = unit_in_slot(k + 1);
       if (!ok) break;
       const Unit w = decode_unit(p, u);
-      const TileView tv = tile_view(w, q), tvo = tile_view(w, 1 - q);
+      const TileView tv = tile_view(w, q);
       int last = -1;
       for (int j = w.n_tiles - 1; j >= 0; --j)
         if (tv.uses(j)) { last = j; break; }
-      int pend = -1, pend_g = 0;
       bool first_pv = true, q_ready = false;
-      // What the pending PV needs besides its P: its V stage and the O slot
-      // (first PV of a unit).  P comes last: it is usually the latest.
-      auto pv_waits = [&]() -> bool {
-        if (!wait_or_fail(B_VFULL + (pend_g & (VS - 1)), (pend_g / VS) & 1)) return false;
-        return !(first_pv && nact > 0) || wait_or_fail(B_OFREE + q, (nact - 1) & 1);
-      };
-      // O_q += P_q V(pend), P read from TMEM; leader only.
-      auto pv_mmas = [&]() {
-        const int vs = pend_g & (VS - 1);
-        const uint64_t dv = dV0 + vs * kStage;
-        umma_bf16_ts(tO, tP, dv, kIdPV, first_pv ? 0u : 1u);
-#pragma unroll
-        for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tP + kk * 8, dv + kk * 128, kIdPV, 1u);
-        if (pend == last) umma_commit(bar(B_ODONE + q));
-        umma_commit(bar(B_VEMPTY + vs));
-        if (C::kSplitP) umma_commit(bar(B_PEMPTY + q));   // P_q may be rewritten, O_q rescaled
-      };
-      // S_q = Q_q K(g)^T; leader only.
-      auto qk_mmas = [&]() {
-        const uint64_t dk = dK0 + ks * kStage;
+      // S_q = Q_q K^T with K in stage st; leader only.
+      auto qk_mmas = [&](int st) {
+        const uint64_t dk = dK0 + st * kStage;
         umma_bf16_ss(tS, dQ, dk, kIdQK, 0u);
 #pragma unroll
         for (int kk = 1; kk < D / 16; ++kk) {
@@ -614,103 +606,120 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           umma_bf16_ss(tS, dQ + o, dk + o, kIdQK, 1u);
         }
         umma_commit(bar(B_SFULL + q));
-        umma_commit(bar(B_KEMPTY + ks));
+        umma_commit(bar(B_KEMPTY + st));
       };
-      for (int j = 0; j < w.n_tiles; ++j, ++g) {
-        if (!wait_or_fail(B_KFULL + ks, kph)) break;
-        if (!tv.uses(j)) {
-          if (leader) mbar_arrive(bar(B_KEMPTY + ks));
-          __syncwarp();
-          const int vs = g & (VS - 1);
-          if (!wait_or_fail(B_VFULL + vs, (g / VS) & 1)) break;
-          if (leader) mbar_arrive(bar(B_VEMPTY + vs));
-          __syncwarp();
-          if (++ks == KS) { ks = 0; kph ^= 1; }
-          continue;
-        }
-        if (C::kSplitP) {
-          // QK_q(j) as soon as the softmax has read the previous S_q, then the
-          // pending PV once its P is written.
-          if (ns > 0 && !wait_or_fail(B_SEMPTY + q, (ns - 1) & 1)) break;
-          if (!q_ready) {
-            if (!wait_or_fail(B_QFULL + q, q_seen & 1)) break;
-            ++q_seen;
-            q_ready = true;
+      // O_q += P_q V with V in stage vs; leader only.  The commits: O_q
+      // complete (last PV of the unit), the V stage free, P_q free (and O_q
+      // idle for a rescale).
+      auto pv_mmas = [&](int vs, bool unit_last) {
+        const uint64_t dv = dV0 + vs * kStage;
+        if constexpr (C::kPSmem) {
+          // P from its buffer: K-major, 128-byte swizzle, the Q tile's layout
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint64_t o = static_cast<uint64_t>(((kk >> 2) * (kTileM * 128) + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(tO, dP + o, dv + kk * 128, kIdPV, (first_pv && kk == 0) ? 0u : 1u);
           }
-          tc_fence_after();
-          if (leader) qk_mmas();
-          __syncwarp();
-          ++ns;
-          if (pend >= 0) {
-            if (!pv_waits() || !wait_or_fail(B_PFULL + q, npv & 1)) break;
-            tc_fence_after();
-            if (leader) pv_mmas();
+        } else {
+          umma_bf16_ts(tO, tP, dv, kIdPV, first_pv ? 0u : 1u);
+#pragma unroll
+          for (int kk = 1; kk < kTileN / 16; ++kk) umma_bf16_ts(tO, tP + kk * 8, dv + kk * 128, kIdPV, 1u);
+        }
+        if (unit_last) umma_commit(bar(B_ODONE + q));
+        umma_commit(bar(C::kPSmem ? B_KEMPTY + vs : B_VEMPTY + vs));
+        umma_commit(bar(B_PEMPTY + q));
+      };
+      // QK_q of a tile: once the softmax has read the previous S_q and Q_q has landed.
+      auto qk_step = [&](int st) -> bool {
+        if (ns > 0 && !wait_or_fail(B_SEMPTY + q, (ns - 1) & 1)) return false;
+        if (!q_ready) {
+          if (!wait_or_fail(B_QFULL + q, q_seen & 1)) return false;
+          ++q_seen;
+          q_ready = true;
+        }
+        tc_fence_after();
+        if (leader) qk_mmas(st);
+        __syncwarp();
+        ++ns;
+        return true;
+      };
+      // PV_q of tile jp (its V in stage vs): once the O slot is free (first PV
+      // of a unit) and P_q is written, which is usually the latest.
+      auto pv_step = [&](int vs, int jp) -> bool {
+        if (first_pv && nact > 0 && !wait_or_fail(B_OFREE + q, (nact - 1) & 1)) return false;
+        if (!wait_or_fail(B_PFULL + q, npv & 1)) return false;
+        tc_fence_after();
+        if (leader) pv_mmas(vs, jp == last);
+        __syncwarp();
+        first_pv = false;
+        ++npv;
+        return true;
+      };
+      // The Q slot is free once QK_q of the unit's last tile has completed: load the next unit's tile.
+      auto reload_q = [&]() -> bool {
+        if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) return false;
+        if (leader) load_q(q, decode_unit(p, un));
+        __syncwarp();
+        ++q_loads;
+        return true;
+      };
+      if constexpr (C::kPSmem) {
+        // The shared ring, in the producer's order: K(x), then V(x - 1).
+        for (int x = 0; x <= w.n_tiles; ++x) {
+          if (x < w.n_tiles) {
+            const int st = gr % KS;
+            if (!wait_or_fail(B_KFULL + st, (gr / KS) & 1)) break;
+            ++gr;
+            if (tv.uses(x)) {
+              if (!qk_step(st)) break;
+            } else {
+              if (leader) mbar_arrive(bar(B_KEMPTY + st));
+              __syncwarp();
+            }
+          }
+          if (x >= 1) {
+            const int st = gr % KS;
+            if (!wait_or_fail(B_KFULL + st, (gr / KS) & 1)) break;
+            ++gr;
+            if (tv.uses(x - 1)) {
+              if (!pv_step(st, x - 1)) break;
+            } else {
+              if (leader) mbar_arrive(bar(B_KEMPTY + st));
+              __syncwarp();
+            }
+          }
+          if (x == last && un >= 0 && !reload_q()) break;
+        }
+      } else {
+        // Two rings: QK_q(j), then the PV of the previous used tile (pend).
+        static_assert((VS & (VS - 1)) == 0, "V ring depth must be a power of two");
+        int pend = -1, pend_g = 0;
+        for (int j = 0; j < w.n_tiles; ++j, ++g) {
+          if (!wait_or_fail(B_KFULL + ks, kph)) break;
+          if (!tv.uses(j)) {
+            if (leader) mbar_arrive(bar(B_KEMPTY + ks));
             __syncwarp();
-            first_pv = false;
-            ++npv;
+            const int vs = g & (VS - 1);
+            if (!wait_or_fail(B_VFULL + vs, (g / VS) & 1)) break;
+            if (leader) mbar_arrive(bar(B_VEMPTY + vs));
+            __syncwarp();
+            if (++ks == KS) { ks = 0; kph ^= 1; }
+            continue;
+          }
+          if (!qk_step(ks)) break;
+          if (pend >= 0) {
+            const int vs = pend_g & (VS - 1);
+            if (!wait_or_fail(B_VFULL + vs, (pend_g / VS) & 1) || !pv_step(vs, pend)) break;
           }
           pend = j;
           pend_g = g;
           if (++ks == KS) { ks = 0; kph ^= 1; }
-          if (j == last && un >= 0) {
-            if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
-            if (leader) load_q(q, decode_unit(p, un));
-            __syncwarp();
-            ++q_loads;
-          }
-          continue;
+          if (j == last && un >= 0 && !reload_q()) break;
         }
-        if (pend >= 0 && !pv_waits()) break;
-        if (!q_ready) {
-          if (!wait_or_fail(B_QFULL + q, q_seen & 1)) break;
-          ++q_seen;
-          q_ready = true;
+        if (ok && pend >= 0) {
+          const int vs = pend_g & (VS - 1);
+          if (wait_or_fail(B_VFULL + vs, (pend_g / VS) & 1)) pv_step(vs, pend);
         }
-        // Band units: both tiles use the same key tiles; global-row units: the
-        // tiles take alternate key tiles, and each follows the other's previous one.
-        const bool turn = w.grow ? (j >= 1)
-                                 : ((q == 0) ? ((j >= 1) & tv.uses(j - 1) & tvo.uses(j - 1)) : tvo.uses(j));
-        const int need_other = (w.grow || q == 0) ? g - 1 : g;
-        if (turn && issued[1 - q] < need_other) {
-          const long long t0 = clock64();
-          while (issued[1 - q] < need_other) {
-            if (*abort_flag || clock64() - t0 > cap) { ok = false; break; }
-          }
-          if (!__all_sync(0xffffffffu, ok)) {
-            if (leader) fail();
-            ok = false;
-            break;
-          }
-        }
-        if (pend >= 0 && !wait_or_fail(B_PFULL + q, npv & 1)) break;
-        tc_fence_after();
-        if (leader) {
-          if (pend >= 0) pv_mmas();
-          qk_mmas();
-          issued[q] = g;
-        }
-        __syncwarp();
-        if (pend >= 0) {
-          first_pv = false;
-          ++npv;
-        }
-        ++ns;
-        pend = j;
-        pend_g = g;
-        if (++ks == KS) { ks = 0; kph ^= 1; }
-        if (j == last && un >= 0) {
-          // The Q slot is free once this QK has completed: load the next unit's tile.
-          if (!wait_or_fail(B_SFULL + q, (ns - 1) & 1)) break;
-          if (leader) load_q(q, decode_unit(p, un));
-          __syncwarp();
-          ++q_loads;
-        }
-      }
-      if (ok && pend >= 0 && pv_waits() && wait_or_fail(B_PFULL + q, npv & 1)) {
-        tc_fence_after();
-        if (leader) pv_mmas();
-        __syncwarp();
-        ++npv;
       }
       if (ok && last < 0) {
         // No key tile for this query tile: its Q load is consumed unused.
@@ -742,6 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
     const uint32_t tS = tmem + lane_off + C::kColS + q * 128;
     const uint32_t tP = tmem + lane_off + C::kColP + q * C::kPStride;
     const uint32_t tO = tmem + lane_off + C::kColO + q * D;
+    const uint32_t sP = sbase + C::kOffStage + q * C::kPBytes;   // P_q in shared memory
+    bool store_pending = false;                         // output stores of this warp may still read sP
     const float sl2 = p.scale_log2;
     int ns = 0;                                         // tiles processed (all units)
     int nact = 0;                                       // units in which this tile was active
@@ -839,10 +850,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       tc_fence_after();
       float s[kTileN];
       tmem_ld128(tS, s);
-      if (C::kSplitP) {
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY + q));                 // S_q may take the next QK
-      }
+      tc_fence_before();
+      mbar_arrive(bar(B_SEMPTY + q));                   // S_q may take the next QK
 
       if (need_mask) {
         // Per 32-column word: nothing to do when every row of the warp keeps
@@ -891,16 +900,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
       const float psum = (a0 + a1) + (b0 + b1);
       l_run = l_run * corr + psum;
       m_run = m_new;
-      // O_q is idle here: PV_q of the previous tile has finished (D = 128:
-      // it was issued before QK_q of this tile by the same thread; D = 64: its
-      // commit is waited for below, which also frees P_q), and PV_q of this
-      // tile waits for P_q.
-      if (C::kSplitP && ns > 0) {
+      // O_q is idle once PV_q of the previous tile has finished (its commit,
+      // waited for here, also frees P_q), and PV_q of this tile waits for P_q.
+      if (ns > 0) {
         if (!wait_all(bar(B_PEMPTY + q), (ns - 1) & 1)) { fail(); ok = false; break; }
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, need_rescale)) rescale_o(tO, need_rescale ? corr : 1.f, D / 32);
-      tmem_st64(tP, pk);
+      if constexpr (C::kPSmem) {
+        // The previous unit's output stores read this warp's rows of the buffer.
+        if (store_pending) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          store_pending = false;
+        }
+        // row r's 128 bf16 values: two 64-key blocks of 128-byte rows, the
+        // 16-byte chunks XOR-swizzled by the row (the layout the MMA reads)
+        const uint32_t prow = sP + r * 128;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int wv = 32 * blk + 4 * c;
+            st_shared_v4(prow + blk * (kTileM * 128) + ((c ^ (r & 7)) << 4), pk[wv], pk[wv + 1], pk[wv + 2], pk[wv + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      } else {
+        tmem_st64(tP, pk);
+      }
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + q));
       ++ns;
@@ -922,13 +950,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           // conflict-free) and writes them with one TMA store per 64 columns
           // through the slot's store map, whose element stride d puts row k of
           // the box at position row0 + d*k; rows past the end of the sequence
-          // are clipped by the store.
-          const uint32_t stage = sbase + C::kOffStage + (warp - 4) * 4096;
+          // are clipped by the store.  D = 128: the 64-column halves go to
+          // this warp's rows of the two 64-key blocks of its P buffer (free:
+          // the unit's last PV has completed), so neither waits for a store.
           const int row0 = w.c + w.d * (w.t0 + q * kTileM + 32 * (warp & 3));
 #pragma unroll 1
           for (int half = 0; half < D / 64; ++half) {
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+            const uint32_t stage = C::kPSmem ? sP + half * (kTileM * 128) + (warp & 3) * 4096
+                                             : sbase + C::kOffStage + (warp - 4) * 4096;
+            if (!C::kPSmem) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
               float o[32];
@@ -949,6 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
               bulk_commit_group();
             }
           }
+          store_pending = true;
           tc_fence_before();
           mbar_arrive(bar(B_OFREE + q));
           if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;

@@ -51,6 +51,7 @@ def run_bwd(lg, w, scale=None):
     g = inp["global_idx"]
     gd = torch.from_numpy(g).to(dev) if g.size else None
     out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd, scale=scale)
+    assert lg.query_status(lg.attn_fwd.last_workspace) == 0
     dq, dk, dv = lg.attn_bwd(q, k, v, out, lse, dout, w.w_left, w.w_right, w.dilations(), w.causal, gd, scale=scale)
     torch.cuda.synchronize()
     assert lg.query_status(lg.attn_bwd.last_workspace) == 0
@@ -66,6 +67,7 @@ def run_etc_bwd(lg, w, scale=None):
     dev = torch.device("cuda")
     t = [inp[n].to(dev) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
     out_l, out_g, lse_l, lse_g = lg.etc_attn_fwd(*t, w.radius, scale=scale)
+    assert lg.query_status(lg.etc_attn_fwd.last_workspace) == 0
     grads = lg.etc_attn_bwd(*t, out_l, out_g, lse_l, lse_g, gr["dout"].to(dev), gr["dout_g"].to(dev), w.radius,
                             scale=scale)
     torch.cuda.synchronize()
@@ -162,6 +164,7 @@ def _fwd_bwd(lg, w):
     g = inp["global_idx"]
     gd = torch.from_numpy(g).to(dev) if g.size else None
     out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd)
+    assert lg.query_status(lg.attn_fwd.last_workspace) == 0
     dq, dk, dv = lg.attn_bwd(q, k, v, out, lse, dout, w.w_left, w.w_right, w.dilations(), w.causal, gd)
     torch.cuda.synchronize()
     assert lg.query_status(lg.attn_bwd.last_workspace) == 0
@@ -232,6 +235,7 @@ def test_bwd_etc_base_two_slices(cuda_lib):
     dev = torch.device("cuda")
     t = [inp[n].to(dev) for n in ("q", "k", "v", "q_g", "k_g", "v_g")]
     out_l, out_g, lse_l, lse_g = lg.etc_attn_fwd(*t, w.radius)
+    assert lg.query_status(lg.etc_attn_fwd.last_workspace) == 0
     grads = lg.etc_attn_bwd(*t, out_l, out_g, lse_l, lse_g, gr["dout"].to(dev), gr["dout_g"].to(dev), w.radius)
     torch.cuda.synchronize()
     assert lg.query_status(lg.etc_attn_bwd.last_workspace) == 0
