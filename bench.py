@@ -365,6 +365,12 @@ def run_native(args, rank, world):
                     "peak_source": f"bf16_tflops of {peak_kind}", "kernel": "tc_attn_kernel",
                     "kernel_ms_per_launch": round(kernel_ms / max(1, kernel_launches), 4),
                     "launches": kernel_launches}
+        # The kernel runs back to back for the whole timed region, under the power cap: the
+        # cuBLAS figure measured the same way (seconds of back-to-back GEMMs) sits beside it.
+        if peaks and "bf16_tflops_sustained" in peaks:
+            sus = float(peaks["bf16_tflops_sustained"])
+            roofline["peak_sustained"] = sus
+            roofline["frac_sustained"] = round(achieved / sus, 4)
     else:
         roofline = None
 
