@@ -35,12 +35,15 @@ def compare(name, dtype, out_gpu, lse_gpu, out_ref, lse_ref):
     return float(err.max()), float(err.mean()), float(lerr.max())
 
 
-def run_longformer(lg, w: workloads.Workload, rows=None, scale=None, key_ramp=None):
+def run_longformer(lg, w: workloads.Workload, rows=None, scale=None, key_ramp=None, workspace_fill=None):
     """CUDA path vs oracle for a (non-ETC) workload; rows=None compares every row.
 
     scale: the logit scale passed to both sides (None: the default 1/sqrt(D)).
     key_ramp: if given, key n is multiplied by 1 + key_ramp * n / N (rounded back to the
-    input dtype; both sides get the same keys), so the logits grow along the sequence."""
+    input dtype; both sides get the same keys), so the logits grow along the sequence.
+    workspace_fill: if given, the call gets its own workspace with every byte set to this
+    value first (0xFF makes every float in it a NaN), so that a value the library reads
+    without having written it in this call shows in the output."""
     inp = workloads.make_inputs(w)
     if key_ramp is not None:
         ramp = 1.0 + key_ramp * torch.arange(w.N, dtype=torch.float32) / w.N
@@ -49,7 +52,11 @@ def run_longformer(lg, w: workloads.Workload, rows=None, scale=None, key_ramp=No
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     g = inp["global_idx"]
     gd = torch.from_numpy(g).to(dev) if g.size else None
-    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd, scale=scale)
+    ws = None
+    if workspace_fill is not None:
+        nbytes = lg.attn_fwd_workspace_size(w.B, w.H, w.N, w.D, int(g.size), 1 if w.dtype == "bf16" else 0)
+        ws = torch.full((max(nbytes, 256),), workspace_fill, dtype=torch.uint8, device=dev)
+    out, lse = lg.attn_fwd(q, k, v, w.w_left, w.w_right, w.dilations(), w.causal, gd, scale=scale, workspace=ws)
     torch.cuda.synchronize()
     st = lg.query_status(lg.attn_fwd.last_workspace)
     assert st == 0, lg.status_string(st)

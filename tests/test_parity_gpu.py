@@ -96,6 +96,25 @@ def test_bf16_small(cuda_lib, w):
     pu.run_longformer(cuda_lib, w)
 
 
+# Global rows over a sequence of one key tile: of the two warpgroups that share a global
+# row's key tiles (alternate tiles), the second gets none and leaves an empty partial
+# (maximum -inf, accumulator never written), which the merge must leave out.  The
+# workspace is filled with 0xFF bytes (NaN as floats) before the call, so an accumulator
+# read anyway would show; any bytes are a valid workspace (the call clears its status area).
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_empty_global_partials_nan_workspace(cuda_lib, D):
+    w = W(f"bf16 one key tile + globals D{D}", "bf16", 1, 2, 100, D, 10, 10, (), False, (0, 37, 99))
+    pu.run_longformer(cuda_lib, w, workspace_fill=0xFF)
+
+
+@pytest.mark.parametrize("name", ["bf16 globals at edges D128", "bf16 fine global-row splits D128"])
+def test_bf16_nan_workspace(cuda_lib, name):
+    """Global rows with several key splits (few partials per row, and many), on a
+    NaN-filled workspace."""
+    w = next(c for c in BF16_CASES if c.name == name)
+    pu.run_longformer(cuda_lib, w, workspace_fill=0xFF)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_bf16_etc_small(cuda_lib, D):
     pu.run_etc(cuda_lib, W(f"bf16 etc D{D}", "bf16", 2, 2, 700, D, 0, 0, etc_G=70, radius=20))
