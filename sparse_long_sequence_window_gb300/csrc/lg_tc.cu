@@ -27,9 +27,9 @@
 // (TMA); warp 1 owns TMEM and issues the MMAs and Q loads of query tile 0,
 // warp 3 those of tile 1; warps 4..7 and 8..11 are the two softmax
 // warpgroups (one thread per query row = TMEM lane).  For D = 128 warp 0
-// issues both K and V into one ring.  TMEM holds S_q (128 fp32 columns) and O_q (D columns) for
-// both tiles, and for D = 64 also P_q (packed bf16, 64 columns); for D = 128
-// P_q is in shared memory.  S_q takes the next key tile's QK as soon as the
+// issues both K and V into one ring.  TMEM holds S_q (128 fp32 columns) and
+// O_q (D columns) for both tiles, and for D = 64 also P_q (packed bf16, 64
+// columns); for D = 128 P_q is in shared memory.  S_q takes the next key tile's QK as soon as the
 // softmax has read it, so the tensor core computes S_q(j+1) while the
 // softmax of tile j runs, and PV_q(j) follows once P_q(j) is written; the
 // softmax waits for PV_q(j) before it rescales O_q or writes P_q(j+1).
