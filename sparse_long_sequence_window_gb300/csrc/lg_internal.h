@@ -27,7 +27,9 @@ constexpr size_t kStatusBytes = 256;     // status area at the head of every wor
 constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;              // keys per tile
 constexpr int kGrowSplitMax = 32;        // most key tiles per split of a global-query row block (two partials)
-constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
+constexpr int kMaxSlots = 8;             // tensor-map slots per tensor-core launch
+constexpr int kMaxDilSlots = 4;          // distinct dilations per launch of the window path (slot 0 is d = 1)
+constexpr int kMaxFusedHeads = 32;       // heads of a LongNet call whose patterns share one launch
 
 // ---------------------------------------------------------------- launch chaining
 // The kernels of one call run back to back on one stream.  A kernel launched
@@ -147,6 +149,16 @@ struct TcParams {
   int seg_w, seg_r, seg_n, seg_packed;
   int seg_causal;                 // segment mode: only keys at or before the query
   int head_unit_start[LG_MAX_HEADS + 1];  // prefix of band units over heads (one batch)
+  // Several LongNet patterns in one launch (n_pat > 0; seg_n, seg_causal as
+  // above): pattern k uses slot k (its tensor maps and slot_dil[k]); its units
+  // are [pat_unit_start[k], pat_unit_start[k + 1]) of the table, per batch in
+  // the head order of pat_head_unit_start[k]; its LSE rows go to pat_lse[k],
+  // pat_rows[k] rows per (b, h) (N, or the packed length).
+  int n_pat;
+  int pat_unit_start[kMaxSlots + 1];
+  int pat_w[kMaxSlots], pat_r[kMaxSlots], pat_packed[kMaxSlots], pat_rows[kMaxSlots];
+  float* pat_lse[kMaxSlots];
+  int pat_head_unit_start[kMaxSlots][kMaxFusedHeads + 1];
 };
 
 // LongNet pattern (w, r), head offset s = h mod r: the kept rows of segment i

@@ -156,33 +156,63 @@ size_t rup_ln(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct LnLayout {
   size_t o[kMaxPatterns] = {}, l[kMaxPatterns] = {};
   int rows[kMaxPatterns] = {};
-  size_t gather[3] = {}, units = 0, max_units = 0, total = 0;
+  bool fused = false;                 // every pattern in one tensor-core launch
+  size_t gather[kMaxPatterns][3] = {};  // packed q, k, v of each packed pattern (one shared set unless fused)
+  size_t units = 0, max_units = 0, total = 0;
 };
 
-// Work units of one pattern's launch, at most: per head ceil(rows / 256)
-// (rows <= N), and half as many again for the split tail.
+// One launch for all patterns when their tensor maps fit the slots of one
+// launch and the per-pattern head tables fit the launch parameters.
+bool fused_call(int H, int n_pat) { return n_pat <= kMaxSlots && H <= kMaxFusedHeads; }
+
+// Work units of a launch, at most: per head and pattern ceil(rows / 256)
+// (rows <= N, the pattern's kept rows of the longest head), and half as many
+// again for the split tail; one pattern per launch, or all of them (fused).
 LnLayout ln_layout(int BH, int H, int N, int D, int n_pat, const int32_t* seg_w, const int32_t* seg_r) {
   LnLayout w;
+  w.fused = fused_call(H, n_pat);
   size_t off = kStatusBytes;
   int p_max = 0;
+  size_t per_head_max = 0, per_head_sum = 0;
   for (int k = 0; k < n_pat; ++k) {
     const bool strided = strided_layout(seg_w[k], seg_r[k]);
     w.rows[k] = strided ? N : std::max(1, packed_rows(H, N, seg_w[k], seg_r[k]));
     if (!strided) p_max = std::max(p_max, w.rows[k]);
     w.o[k] = off; off += rup_ln(static_cast<size_t>(BH) * w.rows[k] * D * 2, 256);
     w.l[k] = off; off += rup_ln(static_cast<size_t>(BH) * w.rows[k] * 4, 256);
+    const size_t per_head = (static_cast<size_t>(w.rows[k]) + 255) / 256;
+    per_head_max = std::max(per_head_max, per_head);
+    per_head_sum += per_head;
   }
-  for (int a = 0; a < 3; ++a) {
-    w.gather[a] = off;
-    off += rup_ln(static_cast<size_t>(BH) * p_max * D * 2, 256);
+  // Packed q, k, v: a set per packed pattern when fused (all are read by the
+  // one launch); otherwise one set of the longest size, which every packed
+  // pattern uses in turn.
+  size_t shared[3] = {0, 0, 0};
+  if (!w.fused && p_max > 0) {
+    for (int a = 0; a < 3; ++a) {
+      shared[a] = off;
+      off += rup_ln(static_cast<size_t>(BH) * p_max * D * 2, 256);
+    }
+  }
+  for (int k = 0; k < n_pat; ++k) {
+    if (strided_layout(seg_w[k], seg_r[k])) continue;
+    for (int a = 0; a < 3; ++a) {
+      if (w.fused) {
+        w.gather[k][a] = off;
+        off += rup_ln(static_cast<size_t>(BH) * w.rows[k] * D * 2, 256);
+      } else {
+        w.gather[k][a] = shared[a];
+      }
+    }
   }
   w.units = off;
-  const size_t per_head = (static_cast<size_t>(N) + 255) / 256;
+  const size_t per_head = w.fused ? per_head_sum : per_head_max;
   w.max_units = static_cast<size_t>(BH) * per_head + static_cast<size_t>(BH) * per_head / 2 + 1;
   off += rup_ln(w.max_units * 64, 256);
   w.total = off;
   return w;
 }
+
 
 lg_status check_patterns(int n_pat, const int32_t* seg_w, const int32_t* seg_r) {
   if (n_pat < 1 || seg_w == nullptr || seg_r == nullptr) return LG_ERR_INVALID_ARG;
@@ -248,76 +278,138 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
   const LnLayout lay = ln_layout(BH, H, N, D, n_patterns, seg_w, seg_r);
   if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return LG_ERR_CUDA;
 
-  MixParams mp{};
-  for (int pk = 0; pk < n_patterns; ++pk) {
-    const int w = seg_w[pk], r = seg_r[pk];
-    const bool strided = strided_layout(w, r);
-    const int d = strided ? r : 1;          // stride of the kernel's tensor maps
-    const int rows = lay.rows[pk];          // rows of the kernel's tensors (N, or the packed length)
-    const void* src[3] = {q, k, v};
-    if (!strided) {
-      GatherParams g{};
-      for (int a = 0; a < 3; ++a) {
-        g.src[a] = static_cast<const uint4*>(src[a]);
-        g.dst[a] = reinterpret_cast<uint4*>(ws + lay.gather[a]);
-        src[a] = ws + lay.gather[a];
-      }
-      g.H = H; g.N = N; g.P = rows; g.chunks = D / 8; g.w = w; g.r = r;
-      g.total = static_cast<long long>(BH) * rows * g.chunks;
-      const long long blocks = std::min<long long>((g.total + 255) / 256, 16LL * device_sm_count());
-      // plain launch: the previous pattern's kernel reads the packed buffers until it completes
-      if (launch_kernel(longnet_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, false, g) !=
-          cudaSuccess)
-        return LG_ERR_CUDA;
+  // Packs pattern pk's kept rows of q, k, v into its gather buffers; src gets their addresses.
+  auto gather = [&](int pk, const void* (&src)[3]) -> bool {
+    GatherParams g{};
+    for (int a = 0; a < 3; ++a) {
+      g.src[a] = static_cast<const uint4*>(src[a]);
+      g.dst[a] = reinterpret_cast<uint4*>(ws + lay.gather[pk][a]);
+      src[a] = ws + lay.gather[pk][a];
     }
-    TcParams tp{};
-    if (!encode_map(&tp.mapQ[0], src[0], D, rows, BH, d) || !encode_map(&tp.mapK[0], src[1], D, rows, BH, d) ||
-        !encode_map(&tp.mapV[0], src[2], D, rows, BH, d) || !encode_store_map(&tp.mapO[0], ws + lay.o[pk], D, rows, BH, d))
-      return LG_ERR_CUDA;
-    for (int sl = 0; sl < kMaxSlots; ++sl) {
-      tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
-      tp.slot_dil[sl] = d;
-    }
-    tp.mapQg = tp.mapQ[0]; tp.mapKg = tp.mapK[0]; tp.mapVg = tp.mapV[0];
-    tp.mapKgr = tp.mapK[0]; tp.mapVgr = tp.mapV[0];
-    tp.seg_w = w; tp.seg_r = r; tp.seg_n = N; tp.seg_packed = strided ? 0 : 1;
-    tp.seg_causal = causal;
+    g.H = H; g.N = N; g.P = lay.rows[pk]; g.chunks = D / 8; g.w = seg_w[pk]; g.r = seg_r[pk];
+    g.total = static_cast<long long>(BH) * lay.rows[pk] * g.chunks;
+    const long long blocks = std::min<long long>((g.total + 255) / 256, 16LL * device_sm_count());
+    // plain launch: it waits for every kernel before it (the previous pattern's
+    // kernel reads the shared buffers until it completes)
+    return launch_kernel(longnet_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, false, g) ==
+           cudaSuccess;
+  };
+  // Band units of pattern (w, r) per head, prefix over the heads in hs[0..H].
+  auto head_units = [&](int w, int r, bool strided, int* hs) {
     int start = 0;
     for (int h = 0; h < H; ++h) {
       const int sh = h % r;
       const int n_c = strided ? (N - sh + r - 1) / r : seg_class_len(N, w, r, sh);
-      tp.head_slot[h] = 0;
-      tp.head_class[h] = 0;
-      tp.head_unit_start[h] = start;
+      hs[h] = start;
       start += n_c > 0 ? (n_c + 2 * kTileM - 1) / (2 * kTileM) : 0;
     }
-    tp.head_unit_start[H] = start;
-    tp.band_units_per_batch = start;
-    tp.out = ws + lay.o[pk];
-    tp.lse = reinterpret_cast<float*>(ws + lay.l[pk]);
+    hs[H] = start;
+    return start;
+  };
+  auto common = [&](TcParams& tp) {
+    tp.mapQg = tp.mapQ[0]; tp.mapKg = tp.mapK[0]; tp.mapVg = tp.mapV[0];
+    tp.mapKgr = tp.mapK[0]; tp.mapVgr = tp.mapV[0];
+    tp.seg_n = N;
+    tp.seg_causal = causal;
     tp.status = status;
     tp.wait_cap = wait_cap_cycles();
     tp.withhold = withhold_for_test();
-    tp.unit_counter = status + 1 + pk;   // one zeroed word of the status area per launch
     tp.scale_log2 = s * 1.4426950408889634f;
-    tp.BH = BH; tp.H = H; tp.N = rows; tp.D = D; tp.wl = 0; tp.wr = 0; tp.n_glob = 0; tp.etc = 0;
+    tp.BH = BH; tp.H = H; tp.D = D; tp.wl = 0; tp.wr = 0; tp.n_glob = 0; tp.etc = 0;
     tp.grow_split = 1;
-    const long long band_units = static_cast<long long>(B) * start;
-    const long long tail = tail_split(band_units, band_units);
-    tp.n_tail_split = static_cast<int>(tail);
-    const long long units = band_units + tail;
-    if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
     tp.units = ws + lay.units;
-    // The unit table of a later pattern may not overwrite the one the previous
-    // pattern's kernel reads: chained only after the memset or a gather (which
-    // itself waited for that kernel).
-    if (prof_mark(stream, true) != cudaSuccess ||
-        launch_tc(tp, static_cast<int>(units), stream, pk == 0 || !strided) != cudaSuccess ||
+  };
+
+  if (lay.fused) {
+    // Every pattern in one launch, pattern k in slot k: the CTAs claim the
+    // units of all patterns from one counter, so a pattern with few or
+    // uneven units (the last segments' units of a causal block are the
+    // longest) no longer ends its own launch on a few busy SMs.
+    TcParams tp{};
+    tp.n_pat = n_patterns;
+    long long units = 0;
+    for (int pk = 0; pk < n_patterns; ++pk) {
+      const int w = seg_w[pk], r = seg_r[pk];
+      const bool strided = strided_layout(w, r);
+      const int d = strided ? r : 1;
+      const int rows = lay.rows[pk];
+      const void* src[3] = {q, k, v};
+      if (!strided && !gather(pk, src)) return LG_ERR_CUDA;
+      if (!encode_map(&tp.mapQ[pk], src[0], D, rows, BH, d) || !encode_map(&tp.mapK[pk], src[1], D, rows, BH, d) ||
+          !encode_map(&tp.mapV[pk], src[2], D, rows, BH, d) ||
+          !encode_store_map(&tp.mapO[pk], ws + lay.o[pk], D, rows, BH, d))
+        return LG_ERR_CUDA;
+      tp.slot_dil[pk] = d;
+      tp.pat_w[pk] = w; tp.pat_r[pk] = r; tp.pat_packed[pk] = strided ? 0 : 1; tp.pat_rows[pk] = rows;
+      tp.pat_lse[pk] = reinterpret_cast<float*>(ws + lay.l[pk]);
+      tp.pat_unit_start[pk] = static_cast<int>(units);
+      units += static_cast<long long>(B) * head_units(w, r, strided, tp.pat_head_unit_start[pk]);
+    }
+    tp.pat_unit_start[n_patterns] = static_cast<int>(units);
+    for (int sl = n_patterns; sl < kMaxSlots; ++sl) {
+      tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
+      tp.slot_dil[sl] = 1;
+    }
+    common(tp);
+    tp.N = N;
+    tp.lse = tp.pat_lse[0];
+    tp.unit_counter = status + 1;
+    const long long tail = tail_split(units, units);
+    tp.n_tail_split = static_cast<int>(tail);
+    units += tail;
+    if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
+    if (prof_mark(stream, true) != cudaSuccess || launch_tc(tp, static_cast<int>(units), stream, true) != cudaSuccess ||
         prof_mark(stream, false) != cudaSuccess)
       return LG_ERR_CUDA;
+  } else {
+    for (int pk = 0; pk < n_patterns; ++pk) {
+      const int w = seg_w[pk], r = seg_r[pk];
+      const bool strided = strided_layout(w, r);
+      const int d = strided ? r : 1;          // stride of the kernel's tensor maps
+      const int rows = lay.rows[pk];          // rows of the kernel's tensors (N, or the packed length)
+      const void* src[3] = {q, k, v};
+      if (!strided && !gather(pk, src)) return LG_ERR_CUDA;
+      TcParams tp{};
+      if (!encode_map(&tp.mapQ[0], src[0], D, rows, BH, d) || !encode_map(&tp.mapK[0], src[1], D, rows, BH, d) ||
+          !encode_map(&tp.mapV[0], src[2], D, rows, BH, d) ||
+          !encode_store_map(&tp.mapO[0], ws + lay.o[pk], D, rows, BH, d))
+        return LG_ERR_CUDA;
+      for (int sl = 0; sl < kMaxSlots; ++sl) {
+        tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
+        tp.slot_dil[sl] = d;
+      }
+      tp.seg_w = w; tp.seg_r = r; tp.seg_packed = strided ? 0 : 1;
+      for (int h = 0; h < H; ++h) {
+        tp.head_slot[h] = 0;
+        tp.head_class[h] = 0;
+      }
+      const int start = head_units(w, r, strided, tp.head_unit_start);
+      tp.band_units_per_batch = start;
+      common(tp);
+      tp.N = rows;
+      tp.out = ws + lay.o[pk];
+      tp.lse = reinterpret_cast<float*>(ws + lay.l[pk]);
+      tp.unit_counter = status + 1 + pk;   // one zeroed word of the status area per launch
+      const long long band_units = static_cast<long long>(B) * start;
+      const long long tail = tail_split(band_units, band_units);
+      tp.n_tail_split = static_cast<int>(tail);
+      const long long units = band_units + tail;
+      if (units > static_cast<long long>(lay.max_units)) return LG_ERR_WORKSPACE;
+      // The unit table of a later pattern may not overwrite the one the previous
+      // pattern's kernel reads: chained only after the memset or a gather (which
+      // itself waited for that kernel).
+      if (prof_mark(stream, true) != cudaSuccess ||
+          launch_tc(tp, static_cast<int>(units), stream, pk == 0 || !strided) != cudaSuccess ||
+          prof_mark(stream, false) != cudaSuccess)
+        return LG_ERR_CUDA;
+    }
+  }
+  MixParams mp{};
+  for (int pk = 0; pk < n_patterns; ++pk) {
     mp.o[pk] = reinterpret_cast<const __nv_bfloat16*>(ws + lay.o[pk]);
     mp.l[pk] = reinterpret_cast<const float*>(ws + lay.l[pk]);
-    mp.w[pk] = w; mp.r[pk] = r; mp.rows[pk] = rows; mp.packed[pk] = strided ? 0 : 1;
+    mp.w[pk] = seg_w[pk]; mp.r[pk] = seg_r[pk]; mp.rows[pk] = lay.rows[pk];
+    mp.packed[pk] = strided_layout(seg_w[pk], seg_r[pk]) ? 0 : 1;
   }
   mp.n_pat = n_patterns; mp.H = H; mp.BH = BH; mp.N = N; mp.D = D;
   mp.out = static_cast<__nv_bfloat16*>(out);

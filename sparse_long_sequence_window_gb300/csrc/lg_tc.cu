@@ -128,74 +128,97 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
     half = (u - n_full) & 1;
     u = n_full + ((u - n_full) >> 1);
   }
-  // Two orders.  Global-row units first (the longest units start first), when
-  // the launch's K and V fit in L2 anyway.  Otherwise, per (batch, head) block,
-  // the head's band units with its global-row units interleaved in key order
-  // (the n_gtiles units of key split s before band unit floor(nb s / n_splits)),
-  // so that units reading the same K/V tiles run in the same round and share
-  // them through L2 instead of reading them from HBM twice.
-  const bool first = p.n_grow_units > 0 && !p.grow_interleave;
-  if (first && u < p.n_grow_units) {
-    w.grow = 1;
-    const int split = u % p.n_splits;
-    const int r = u / p.n_splits;
-    w.grow0 = (r % p.n_gtiles) * kTileM;
-    w.bh = r / p.n_gtiles;
-    w.kt0 = split * p.grow_split;
-    w.n_tiles = min(p.grow_split, p.n_key_tiles_grow - w.kt0);
-    w.slot = 0; w.d = 1;
-    w.active[0] = 1; w.active[1] = w.n_tiles > 1;
-    return w;
-  }
-  if (first) u -= p.n_grow_units;
-  const int gu = (p.n_grow_units > 0 && !first) ? p.n_gtiles * p.n_splits : 0;   // interleaved units per (b, h)
-  const int per_batch = p.band_units_per_batch + p.H * gu;
-  const int b = u / per_batch;
-  int rem = u - b * per_batch;
-  int h = 0;
-  while (h + 1 < p.H && p.head_unit_start[h + 1] + (h + 1) * gu <= rem) ++h;
-  rem -= p.head_unit_start[h] + h * gu;
-  if (gu > 0) {
-    const long long nb = p.head_unit_start[h + 1] - p.head_unit_start[h];
-    int split = -1, gt = 0, band = rem - p.n_splits * p.n_gtiles;
-    for (int sp = 0; sp < p.n_splits; ++sp) {
-      const int st = static_cast<int>(nb * sp / p.n_splits) + sp * p.n_gtiles;
-      if (rem < st) { band = rem - sp * p.n_gtiles; break; }
-      if (rem < st + p.n_gtiles) { split = sp; gt = rem - st; break; }
-    }
-    if (split >= 0) {
+  if (p.n_pat > 0) {
+    // Several LongNet patterns: pattern k's units, then per batch and head as
+    // for one pattern (one residue class per head, offset h mod r, in slot k).
+    int k = 0;
+    while (k + 1 < p.n_pat && p.pat_unit_start[k + 1] <= u) ++k;
+    const int* hs = p.pat_head_unit_start[k];
+    int rem = u - p.pat_unit_start[k];
+    const int b = rem / hs[p.H];
+    rem -= b * hs[p.H];
+    int h = 0;
+    while (h + 1 < p.H && hs[h + 1] <= rem) ++h;
+    rem -= hs[h];
+    const int pw = p.pat_w[k], pr = p.pat_r[k], s = h % pr;
+    w.grow = 0;
+    w.bh = b * p.H + h;
+    w.slot = k;
+    w.d = p.slot_dil[k];
+    w.seg = p.pat_packed[k] ? seg_block(pw, pr, s) : pw / pr;
+    w.c = p.pat_packed[k] ? 0 : s;
+    w.n_c = p.pat_packed[k] ? seg_class_len(p.seg_n, pw, pr, s) : (p.seg_n - s + w.d - 1) / w.d;
+    w.t0 = rem * 2 * kTileM;
+  } else {
+    // Two orders.  Global-row units first (the longest units start first), when
+    // the launch's K and V fit in L2 anyway.  Otherwise, per (batch, head) block,
+    // the head's band units with its global-row units interleaved in key order
+    // (the n_gtiles units of key split s before band unit floor(nb s / n_splits)),
+    // so that units reading the same K/V tiles run in the same round and share
+    // them through L2 instead of reading them from HBM twice.
+    const bool first = p.n_grow_units > 0 && !p.grow_interleave;
+    if (first && u < p.n_grow_units) {
       w.grow = 1;
-      w.grow0 = gt * kTileM;
-      w.bh = b * p.H + h;
+      const int split = u % p.n_splits;
+      const int r = u / p.n_splits;
+      w.grow0 = (r % p.n_gtiles) * kTileM;
+      w.bh = r / p.n_gtiles;
       w.kt0 = split * p.grow_split;
       w.n_tiles = min(p.grow_split, p.n_key_tiles_grow - w.kt0);
       w.slot = 0; w.d = 1;
       w.active[0] = 1; w.active[1] = w.n_tiles > 1;
       return w;
     }
-    rem = band;
-  }
-  w.grow = 0;
-  w.bh = b * p.H + h;
-  w.slot = p.head_slot[h];
-  w.d = p.slot_dil[w.slot];
-  w.seg = 0;
-  if (p.seg_w > 0) {            // LongNet: one residue class per head (offset h mod r)
-    const int s = h % p.seg_r;
-    w.seg = p.seg_packed ? seg_block(p.seg_w, p.seg_r, s) : p.seg_w / p.seg_r;
-    w.c = p.seg_packed ? 0 : s;
-    w.n_c = p.seg_packed ? seg_class_len(p.seg_n, p.seg_w, p.seg_r, s) : (p.N - s + w.d - 1) / w.d;
-    w.t0 = rem * 2 * kTileM;
-  } else if (p.head_class[h] >= 0) {
-    w.c = p.head_class[h];
-    w.n_c = (p.N - w.c + w.d - 1) / w.d;
-    w.t0 = rem * 2 * kTileM;
-  } else {
-    for (int c = 0; c < w.d; ++c) {
-      const int n_c = (p.N - c + w.d - 1) / w.d;
-      const int units = (n_c + 2 * kTileM - 1) / (2 * kTileM);
-      if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
-      rem -= units;
+    if (first) u -= p.n_grow_units;
+    const int gu = (p.n_grow_units > 0 && !first) ? p.n_gtiles * p.n_splits : 0;   // interleaved units per (b, h)
+    const int per_batch = p.band_units_per_batch + p.H * gu;
+    const int b = u / per_batch;
+    int rem = u - b * per_batch;
+    int h = 0;
+    while (h + 1 < p.H && p.head_unit_start[h + 1] + (h + 1) * gu <= rem) ++h;
+    rem -= p.head_unit_start[h] + h * gu;
+    if (gu > 0) {
+      const long long nb = p.head_unit_start[h + 1] - p.head_unit_start[h];
+      int split = -1, gt = 0, band = rem - p.n_splits * p.n_gtiles;
+      for (int sp = 0; sp < p.n_splits; ++sp) {
+        const int st = static_cast<int>(nb * sp / p.n_splits) + sp * p.n_gtiles;
+        if (rem < st) { band = rem - sp * p.n_gtiles; break; }
+        if (rem < st + p.n_gtiles) { split = sp; gt = rem - st; break; }
+      }
+      if (split >= 0) {
+        w.grow = 1;
+        w.grow0 = gt * kTileM;
+        w.bh = b * p.H + h;
+        w.kt0 = split * p.grow_split;
+        w.n_tiles = min(p.grow_split, p.n_key_tiles_grow - w.kt0);
+        w.slot = 0; w.d = 1;
+        w.active[0] = 1; w.active[1] = w.n_tiles > 1;
+        return w;
+      }
+      rem = band;
+    }
+    w.grow = 0;
+    w.bh = b * p.H + h;
+    w.slot = p.head_slot[h];
+    w.d = p.slot_dil[w.slot];
+    w.seg = 0;
+    if (p.seg_w > 0) {            // LongNet: one residue class per head (offset h mod r)
+      const int s = h % p.seg_r;
+      w.seg = p.seg_packed ? seg_block(p.seg_w, p.seg_r, s) : p.seg_w / p.seg_r;
+      w.c = p.seg_packed ? 0 : s;
+      w.n_c = p.seg_packed ? seg_class_len(p.seg_n, p.seg_w, p.seg_r, s) : (p.N - s + w.d - 1) / w.d;
+      w.t0 = rem * 2 * kTileM;
+    } else if (p.head_class[h] >= 0) {
+      w.c = p.head_class[h];
+      w.n_c = (p.N - w.c + w.d - 1) / w.d;
+      w.t0 = rem * 2 * kTileM;
+    } else {
+      for (int c = 0; c < w.d; ++c) {
+        const int n_c = (p.N - c + w.d - 1) / w.d;
+        const int units = (n_c + 2 * kTileM - 1) / (2 * kTileM);
+        if (rem < units) { w.c = c; w.n_c = n_c; w.t0 = rem * 2 * kTileM; break; }
+        rem -= units;
+      }
     }
   }
   const int span = half >= 0 ? 1 : 2;                 // query tiles of this unit
@@ -430,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   // -1 once the units are exhausted.  Every reader takes the slots in order,
   // so a parity wait on a slot always refers to its latest phase.  Waits on a
   // slot: all lanes of the calling warp (or the single thread).
-  const int k_static = max(0, n_units / static_cast<int>(gridDim.x) - kTailRounds);
+  // (Several LongNet patterns: every unit is claimed, since their lengths
+  // vary from one key tile to a whole segment block.)
+  const int k_static = p.n_pat > 0 ? 0 : max(0, n_units / static_cast<int>(gridDim.x) - kTailRounds);
   auto slot_wait = [&](int k) -> bool {
     return mbar_wait(bar(B_UFULL + (k % kUnitSlots)), (k / kUnitSlots) & 1, abort_flag, cap);
   };
@@ -985,7 +1010,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           store_pending = true;
           tc_fence_before();
           mbar_arrive(bar(B_OFREE + q));
-          if (row_valid) p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = (m_run + __log2f(l_run)) * kLn2;
+          if (row_valid) {
+            float* lse = p.n_pat > 0 ? p.pat_lse[w.slot] : p.lse;
+            const int lse_rows = p.n_pat > 0 ? p.pat_rows[w.slot] : p.N;
+            lse[static_cast<size_t>(w.bh) * lse_rows + pos_q] = (m_run + __log2f(l_run)) * kLn2;
+          }
         } else {
           {
             // Every lane takes part in the warp-collective TMEM loads; only valid rows store.
