@@ -3,7 +3,8 @@
 
 Small cases compare every element: the strided layout (r divides w, r <= 8)
 and the packed one (any other r), causal and not, ragged N, D 64 and 128,
-r > 8, r > w, and rows that no pattern keeps.  The LongNet language-model
+r > 8, r > w, rows that no pattern keeps, and the two launch plans (all
+patterns in one launch up to 8 patterns and 32 heads, else one per pattern).  The LongNet language-model
 workload at full size compares sampled rows, which the oracle computes one
 at a time.  Tolerances as for the other bf16 outputs: max |dO| <= 2e-2,
 mean |dO| <= 2e-3 over the kept rows, |dLSE| <= 1e-3; a row no pattern
@@ -37,6 +38,13 @@ CASES = [
       [1, 2, 4, 6, 12], True),
     L("single token", 1, 2, 1, 64, [16, 4], [1, 2]),
     L("one-row segments", 1, 3, 130, 64, [1, 3], [1, 5]),
+    # Up to 8 patterns and 32 heads share one tensor-core launch; beyond that each
+    # pattern has its own launch (and the packed patterns share one set of buffers).
+    L("eight patterns in one launch", 1, 4, 900, 64, [32, 64, 96, 128, 256, 300, 512, 900],
+      [1, 2, 3, 4, 6, 7, 8, 10], True),
+    L("nine patterns, one launch each", 1, 4, 900, 64, [32, 64, 96, 128, 256, 300, 512, 900, 450],
+      [1, 2, 3, 4, 6, 7, 8, 10, 9], True),
+    L("33 heads, one launch per pattern", 1, 33, 400, 64, [64, 200], [2, 6]),
 ]
 
 
