@@ -386,16 +386,16 @@ lg_status attn_fwd_impl(const void* q, const void* k, const void* v, const void*
     if (dilation[h] != 1 && std::find(others.begin(), others.end(), dilation[h]) == others.end())
       others.push_back(dilation[h]);
   std::sort(others.begin(), others.end());
-  const int n_groups = std::max(1, cdiv(static_cast<long long>(others.size()), kMaxDilSlots - 1));
-  static_assert(1 + (LG_MAX_HEADS + kMaxDilSlots - 2) / (kMaxDilSlots - 1) <= static_cast<int>(kStatusBytes / sizeof(int)),
+  const int n_groups = std::max(1, cdiv(static_cast<long long>(others.size()), kMaxSlots - 1));
+  static_assert(1 + (LG_MAX_HEADS + kMaxSlots - 2) / (kMaxSlots - 1) <= static_cast<int>(kStatusBytes / sizeof(int)),
                 "one unit counter per launch fits in the status area");
 
   TcParams tp;  // filled per launch (a few KB; calls from several host threads keep their own)
   for (int grp = 0; grp < n_groups; ++grp) {
     tp = TcParams{};
-    int slot_d[kMaxDilSlots] = {1, 0, 0, 0};
+    int slot_d[kMaxSlots] = {1, 0, 0, 0};
     int n_slots = 1;
-    for (size_t x = grp * (kMaxDilSlots - 1); x < others.size() && n_slots < kMaxDilSlots; ++x) slot_d[n_slots++] = others[x];
+    for (size_t x = grp * (kMaxSlots - 1); x < others.size() && n_slots < kMaxSlots; ++x) slot_d[n_slots++] = others[x];
     for (int sl = 0; sl < n_slots; ++sl) {
       tp.slot_dil[sl] = slot_d[sl];
       tp.slot_units[sl] = band_units_for(N, slot_d[sl]);

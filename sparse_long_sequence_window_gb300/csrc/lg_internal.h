@@ -27,8 +27,8 @@ constexpr size_t kStatusBytes = 256;     // status area at the head of every wor
 constexpr int kTileM = 128;              // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;              // keys per tile
 constexpr int kGrowSplitMax = 32;        // most key tiles per split of a global-query row block (two partials)
-constexpr int kMaxSlots = 8;             // tensor-map slots per tensor-core launch
-constexpr int kMaxDilSlots = 4;          // distinct dilations per launch of the window path (slot 0 is d = 1)
+constexpr int kMaxSlots = 4;             // distinct dilations per tensor-core launch (slot 0 is d = 1)
+constexpr int kMaxPatternSlots = 8;      // LongNet patterns sharing one launch (a slot each)
 constexpr int kMaxFusedHeads = 32;       // heads of a LongNet call whose patterns share one launch
 
 // ---------------------------------------------------------------- launch chaining
@@ -103,12 +103,18 @@ struct SimtBwdParams {
 // One launch covers all batches and the heads whose dilation has a slot here.
 // Work units: first the global-query row units (gtile, split) per (b, h), then
 // the band units (dilation residue class c, query tile) per (b, h).
-struct TcParams {
-  CUtensorMap mapQ[kMaxSlots];   // main q/k/v viewed as {D, N, BH}, rows strided by the slot's dilation
-  CUtensorMap mapK[kMaxSlots];
-  CUtensorMap mapV[kMaxSlots];
+// S slots of tensor maps.  The window and ETC paths use S = kMaxSlots, which
+// keeps the block within the 4 KB that a launch passes without an extra copy
+// of its parameters; the one launch of several LongNet patterns uses
+// TcParamsLn below.
+template <int S>
+struct TcParamsT {
+  static constexpr bool kPatterns = false;
+  CUtensorMap mapQ[S];           // main q/k/v viewed as {D, N, BH}, rows strided by the slot's dilation
+  CUtensorMap mapK[S];
+  CUtensorMap mapV[S];
   CUtensorMap mapQg, mapKg, mapVg;  // global side {D, g, BH}: gathered rows (Longformer) or q_g/k_g/v_g (ETC)
-  CUtensorMap mapO[kMaxSlots];    // output {D, N, BH}, boxes of 32 rows x 64 columns, rows strided by the slot's dilation
+  CUtensorMap mapO[S];            // output {D, N, BH}, boxes of 32 rows x 64 columns, rows strided by the slot's dilation
   CUtensorMap mapKgr, mapVgr;     // keys / values of the global-row units over the main sequence {D, N, BH}
                                   // (the separate global projections, or the main k / v)
   void* out;                      // bf16 [BH, N, D]
@@ -136,8 +142,8 @@ struct TcParams {
   int n_parts;                    // partial slots per global row (two per split)
   int n_key_tiles_grow;           // key tiles of one global row block (ETC: ceil(G/128) + ceil(L/128))
   int band_units_per_batch;
-  int slot_dil[kMaxSlots];
-  int slot_units[kMaxSlots];      // band units of one head with this slot's dilation
+  int slot_dil[S];
+  int slot_units[S];              // band units of one head with this slot's dilation
   unsigned char head_slot[LG_MAX_HEADS];  // 255: head not in this launch
   signed char head_class[LG_MAX_HEADS];   // >= 0: the one residue class this head computes (LongNet offset); -1: all
   // Segment mode (LongNet dilated attention), seg_w > 0: pattern (seg_w,
@@ -149,16 +155,21 @@ struct TcParams {
   int seg_w, seg_r, seg_n, seg_packed;
   int seg_causal;                 // segment mode: only keys at or before the query
   int head_unit_start[LG_MAX_HEADS + 1];  // prefix of band units over heads (one batch)
-  // Several LongNet patterns in one launch (n_pat > 0; seg_n, seg_causal as
-  // above): pattern k uses slot k (its tensor maps and slot_dil[k]); its units
-  // are [pat_unit_start[k], pat_unit_start[k + 1]) of the table, per batch in
-  // the head order of pat_head_unit_start[k]; its LSE rows go to pat_lse[k],
-  // pat_rows[k] rows per (b, h) (N, or the packed length).
+};
+using TcParams = TcParamsT<kMaxSlots>;
+
+// Several LongNet patterns in one launch (seg_n, seg_causal as above): pattern
+// k uses slot k (its tensor maps and slot_dil[k]); its units are
+// [pat_unit_start[k], pat_unit_start[k + 1]) of the table, per batch in the
+// head order of pat_head_unit_start[k]; its LSE rows go to pat_lse[k],
+// pat_rows[k] rows per (b, h) (N, or the packed length).
+struct TcParamsLn : TcParamsT<kMaxPatternSlots> {
+  static constexpr bool kPatterns = true;
   int n_pat;
-  int pat_unit_start[kMaxSlots + 1];
-  int pat_w[kMaxSlots], pat_r[kMaxSlots], pat_packed[kMaxSlots], pat_rows[kMaxSlots];
-  float* pat_lse[kMaxSlots];
-  int pat_head_unit_start[kMaxSlots][kMaxFusedHeads + 1];
+  int pat_unit_start[kMaxPatternSlots + 1];
+  int pat_w[kMaxPatternSlots], pat_r[kMaxPatternSlots], pat_packed[kMaxPatternSlots], pat_rows[kMaxPatternSlots];
+  float* pat_lse[kMaxPatternSlots];
+  int pat_head_unit_start[kMaxPatternSlots][kMaxFusedHeads + 1];
 };
 
 // LongNet pattern (w, r), head offset s = h mod r: the kept rows of segment i
@@ -258,6 +269,7 @@ cudaError_t launch_simt_bwd(const SimtBwdParams& p, cudaStream_t s);
 // chained to the stream's previous kernel when chain_table (not when that
 // kernel may still read the unit table), the tensor-core kernel always is.
 cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table);
+cudaError_t launch_tc(const TcParamsLn& p, int n_units, cudaStream_t s, bool chain_table);
 cudaError_t launch_merge(const MergeParams& p, int bf16_out, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t s);

@@ -163,7 +163,7 @@ struct LnLayout {
 
 // One launch for all patterns when their tensor maps fit the slots of one
 // launch and the per-pattern head tables fit the launch parameters.
-bool fused_call(int H, int n_pat) { return n_pat <= kMaxSlots && H <= kMaxFusedHeads; }
+bool fused_call(int H, int n_pat) { return n_pat <= kMaxPatternSlots && H <= kMaxFusedHeads; }
 
 // Work units of a launch, at most: per head and pattern ceil(rows / 256)
 // (rows <= N, the pattern's kept rows of the longest head), and half as many
@@ -306,7 +306,7 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
     hs[H] = start;
     return start;
   };
-  auto common = [&](TcParams& tp) {
+  auto common = [&](auto& tp) {
     tp.mapQg = tp.mapQ[0]; tp.mapKg = tp.mapK[0]; tp.mapVg = tp.mapV[0];
     tp.mapKgr = tp.mapK[0]; tp.mapVgr = tp.mapV[0];
     tp.seg_n = N;
@@ -325,7 +325,7 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
     // units of all patterns from one counter, so a pattern with few or
     // uneven units (the last segments' units of a causal block are the
     // longest) no longer ends its own launch on a few busy SMs.
-    TcParams tp{};
+    TcParamsLn tp{};
     tp.n_pat = n_patterns;
     long long units = 0;
     for (int pk = 0; pk < n_patterns; ++pk) {
@@ -346,7 +346,7 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
       units += static_cast<long long>(B) * head_units(w, r, strided, tp.pat_head_unit_start[pk]);
     }
     tp.pat_unit_start[n_patterns] = static_cast<int>(units);
-    for (int sl = n_patterns; sl < kMaxSlots; ++sl) {
+    for (int sl = n_patterns; sl < kMaxPatternSlots; ++sl) {
       tp.mapQ[sl] = tp.mapQ[0]; tp.mapK[sl] = tp.mapK[0]; tp.mapV[sl] = tp.mapV[0]; tp.mapO[sl] = tp.mapO[0];
       tp.slot_dil[sl] = 1;
     }

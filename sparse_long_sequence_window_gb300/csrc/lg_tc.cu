@@ -120,7 +120,8 @@ struct Unit {
 // two one-tile units, which come last (u = n_full + 2 i + h: rows t0 + 128 h
 // of band unit n_full + i, worked by query tile 0), so that the last round of
 // a launch can spread over more CTAs.
-__device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
+template <class P>
+__device__ Unit decode_unit_slow(const P& p, int u, int n_units) {
   Unit w{};
   const int n_full = n_units - 2 * p.n_tail_split;
   int half = -1;
@@ -128,7 +129,7 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
     half = (u - n_full) & 1;
     u = n_full + ((u - n_full) >> 1);
   }
-  if (p.n_pat > 0) {
+  if constexpr (P::kPatterns) {
     // Several LongNet patterns: pattern k's units, then per batch and head as
     // for one pattern (one residue class per head, offset h mod r, in slot k).
     int k = 0;
@@ -248,7 +249,8 @@ __device__ Unit decode_unit_slow(const TcParams& p, int u, int n_units) {
 
 // Unit records: 16 ints per unit, built once per launch by unit_table_kernel,
 // so that a CTA reads a unit with four 16-byte loads.
-__global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_units) {
+template <class P>
+__global__ void unit_table_kernel(const __grid_constant__ P p, int n_units) {
   grid_dep_launch();   // the tensor-core kernel may start its prologue
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
     const Unit w = decode_unit_slow(p, u, n_units);
@@ -264,12 +266,14 @@ __global__ void unit_table_kernel(const __grid_constant__ TcParams p, int n_unit
 
 // Brings unit u's 64-byte record into this SM's L1 (shared by every warp of
 // the CTA), so that the decode at the start of that unit does not wait for L2.
-__device__ __forceinline__ void prefetch_unit(const TcParams& p, int u) {
+template <class P>
+__device__ __forceinline__ void prefetch_unit(const P& p, int u) {
   if (u >= 0)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const int4*>(p.units) + 4 * static_cast<size_t>(u)));
 }
 
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+template <class P>
+__device__ __forceinline__ Unit decode_unit(const P& p, int u) {
   const int4* rec = reinterpret_cast<const int4*>(p.units) + 4 * static_cast<size_t>(u);
   const int4 a = __ldg(rec), b = __ldg(rec + 1), c = __ldg(rec + 2), d = __ldg(rec + 3);
   Unit w;
@@ -368,7 +372,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // Where key/value tile j of unit w comes from: the tensor map, whether it is
 // the dilation-strided view, and the row coordinate.
-__device__ __forceinline__ void tile_source(const TcParams& p, const Unit& w, int j, bool is_k, int gt_src,
+template <class P>
+__device__ __forceinline__ void tile_source(const P& p, const Unit& w, int j, bool is_k, int gt_src,
                                             const CUtensorMap*& m, bool& strided, int& y) {
   if (!w.grow) {
     if (j < w.n_band) {
@@ -389,8 +394,8 @@ __device__ __forceinline__ void tile_source(const TcParams& p, const Unit& w, in
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ TcParams p, int n_units) {
+template <int D, class P>
+__global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_constant__ P p, int n_units) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
   // slot: all lanes of the calling warp (or the single thread).
   // (Several LongNet patterns: every unit is claimed, since their lengths
   // vary from one key tile to a whole segment block.)
-  const int k_static = p.n_pat > 0 ? 0 : max(0, n_units / static_cast<int>(gridDim.x) - kTailRounds);
+  const int k_static = P::kPatterns ? 0 : max(0, n_units / static_cast<int>(gridDim.x) - kTailRounds);
   auto slot_wait = [&](int k) -> bool {
     return mbar_wait(bar(B_UFULL + (k % kUnitSlots)), (k / kUnitSlots) & 1, abort_flag, cap);
   };
@@ -1011,9 +1016,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attn_kernel(const __grid_const
           tc_fence_before();
           mbar_arrive(bar(B_OFREE + q));
           if (row_valid) {
-            float* lse = p.n_pat > 0 ? p.pat_lse[w.slot] : p.lse;
-            const int lse_rows = p.n_pat > 0 ? p.pat_rows[w.slot] : p.N;
-            lse[static_cast<size_t>(w.bh) * lse_rows + pos_q] = (m_run + __log2f(l_run)) * kLn2;
+            const float lv = (m_run + __log2f(l_run)) * kLn2;
+            if constexpr (P::kPatterns) p.pat_lse[w.slot][static_cast<size_t>(w.bh) * p.pat_rows[w.slot] + pos_q] = lv;
+            else p.lse[static_cast<size_t>(w.bh) * p.N + pos_q] = lv;
           }
         } else {
           {
@@ -1061,13 +1066,13 @@ size_t tc_smem_bytes(int D) { return D == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem;
 
 // The register split only fits if the kernel launches with at least
 // kRegsLaunchMin registers per thread; refuse to launch otherwise.
-template <int D>
+template <int D, class P>
 cudaError_t prepare_kernel() {
   cudaFuncAttributes a{};
-  cudaError_t e = cudaFuncGetAttributes(&a, tc_attn_kernel<D>);
+  cudaError_t e = cudaFuncGetAttributes(&a, tc_attn_kernel<D, P>);
   if (e != cudaSuccess) return e;
   if (a.numRegs < kRegsLaunchMin) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(tc_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  return cudaFuncSetAttribute(tc_attn_kernel<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
 }
 
 // Persistent grid: one CTA per SM (shared memory allows no second one), each
@@ -1079,12 +1084,13 @@ int grid_for(int n_units) {
 
 namespace {
 // The shared-memory attribute is a per-device setting: set it once for each
-// device and head size, under a lock (calls may come from several threads).
+// device and kernel instance (head size, parameter block), under a lock (calls
+// may come from several threads).
 constexpr int kMaxDevices = 64;
 std::mutex g_attr_mutex;
-bool g_attr_done[kMaxDevices][2] = {};
-}  // namespace
+bool g_attr_done[kMaxDevices][4] = {};
 
+// i: 0 / 1 for D = 64 / 128 with TcParams, 2 / 3 with TcParamsLn.
 cudaError_t ensure_kernel_attributes(int i) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1092,21 +1098,36 @@ cudaError_t ensure_kernel_attributes(int i) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (g_attr_done[dev][i]) return cudaSuccess;
-  e = i == 0 ? prepare_kernel<64>() : prepare_kernel<128>();
+  switch (i) {
+    case 0: e = prepare_kernel<64, TcParams>(); break;
+    case 1: e = prepare_kernel<128, TcParams>(); break;
+    case 2: e = prepare_kernel<64, TcParamsLn>(); break;
+    default: e = prepare_kernel<128, TcParamsLn>(); break;
+  }
   if (e == cudaSuccess) g_attr_done[dev][i] = true;
   return e;
 }
 
-cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table) {
+template <class P>
+cudaError_t launch_tc_impl(const P& p, int n_units, cudaStream_t s, bool chain_table) {
   if (n_units <= 0) return cudaSuccess;
-  const int i = p.D == 64 ? 0 : 1;
+  const int i = (p.D == 64 ? 0 : 1) + (P::kPatterns ? 2 : 0);
   cudaError_t ea = ensure_kernel_attributes(i);
   if (ea != cudaSuccess) return ea;
-  cudaError_t e = launch_kernel(unit_table_kernel, dim3((n_units + 255) / 256), dim3(256), 0, s, chain_table, p, n_units);
+  cudaError_t e = launch_kernel(unit_table_kernel<P>, dim3((n_units + 255) / 256), dim3(256), 0, s, chain_table, p, n_units);
   if (e != cudaSuccess) return e;
-  if (i == 0)
-    return launch_kernel(tc_attn_kernel<64>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<64>::kSmem, s, true, p, n_units);
-  return launch_kernel(tc_attn_kernel<128>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<128>::kSmem, s, true, p, n_units);
+  if (p.D == 64)
+    return launch_kernel(tc_attn_kernel<64, P>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<64>::kSmem, s, true, p, n_units);
+  return launch_kernel(tc_attn_kernel<128, P>, dim3(grid_for(n_units)), dim3(kThreads), Cfg<128>::kSmem, s, true, p, n_units);
+}
+}  // namespace
+
+cudaError_t launch_tc(const TcParams& p, int n_units, cudaStream_t s, bool chain_table) {
+  return launch_tc_impl(p, n_units, s, chain_table);
+}
+
+cudaError_t launch_tc(const TcParamsLn& p, int n_units, cudaStream_t s, bool chain_table) {
+  return launch_tc_impl(p, n_units, s, chain_table);
 }
 
 long long device_l2_bytes() {
