@@ -87,15 +87,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// One thread per row and 64 columns (D / 64 threads per row): the pattern
-// membership arithmetic once per pattern in 32-bit integers, then eight
-// 16-byte loads of the pattern's output.  The patterns that keep the row are
-// merged online (running max of LSE_k).  The parameter block is read in place
-// (__grid_constant__): its per-pattern arrays are indexed by a runtime k.
+// One thread per row and kMixCols columns (D / kMixCols threads per row,
+// adjacent): the pattern membership arithmetic once per pattern in 32-bit
+// integers, then kMixCols / 8 16-byte loads of the pattern's output.  The
+// patterns that keep the row are merged online (running max of LSE_k).  The
+// parameter block is read in place (__grid_constant__): its per-pattern arrays
+// are indexed by a runtime k.  32 columns keep the accumulator at 32 registers,
+// so that enough warps are resident to cover the load latency (64 columns per
+// thread held 97 registers, two blocks per SM, and the kernel was
+// latency-bound at a third of DRAM bandwidth).
+constexpr int kMixCols = 32;
+
 template <int D>
 __global__ void __launch_bounds__(256) longnet_mix_kernel(const __grid_constant__ MixParams p) {
   grid_dep_wait();   // the patterns' kernels came before
-  constexpr int kParts = D / 64;
+  constexpr int kParts = D / kMixCols;
+  constexpr int kVec = kMixCols / 8;   // 16-byte pieces per thread
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tid >= static_cast<long long>(p.BH) * p.N * kParts) return;
   const int part = static_cast<int>(tid % kParts);
@@ -103,9 +110,9 @@ __global__ void __launch_bounds__(256) longnet_mix_kernel(const __grid_constant_
   const int i = row % p.N;
   const int bh = row / p.N;
   const int h = bh % p.H;
-  float acc[64];
+  float acc[kMixCols];
 #pragma unroll
-  for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+  for (int c = 0; c < kMixCols; ++c) acc[c] = 0.f;
   float m = -INFINITY, l = 0.f;
   for (int k = 0; k < p.n_pat; ++k) {
     const int w = p.w[k], r = p.r[k], s = h % r;
@@ -114,22 +121,22 @@ __global__ void __launch_bounds__(256) longnet_mix_kernel(const __grid_constant_
     const long long src = p.packed[k] ? static_cast<long long>(bh) * p.rows[k] +
                                             static_cast<long long>(seg) * seg_block(w, r, s) + rel / r
                                       : row;
+    const uint4* o = reinterpret_cast<const uint4*>(p.o[k] + src * D + part * kMixCols);
+    uint4 v[kVec];
+#pragma unroll
+    for (int x = 0; x < kVec; ++x) v[x] = __ldg(o + x);
     const float lk = __ldg(p.l[k] + src);
     if (lk > m) {   // new running maximum: rescale what is accumulated
       const float f = exp2f((m - lk) * 1.4426950408889634f);
       l *= f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) acc[c] *= f;
+      for (int c = 0; c < kMixCols; ++c) acc[c] *= f;
       m = lk;
     }
     const float wgt = exp2f((lk - m) * 1.4426950408889634f);
     l += wgt;
-    const uint4* o = reinterpret_cast<const uint4*>(p.o[k] + src * D + part * 64);
-    uint4 v[8];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) v[x] = __ldg(o + x);
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
+    for (int x = 0; x < kVec; ++x) {
       const uint32_t vw[4] = {v[x].x, v[x].y, v[x].z, v[x].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -140,9 +147,9 @@ __global__ void __launch_bounds__(256) longnet_mix_kernel(const __grid_constant_
     }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<long long>(row) * D + part * 64);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<long long>(row) * D + part * kMixCols);
 #pragma unroll
-  for (int x = 0; x < 8; ++x)
+  for (int x = 0; x < kVec; ++x)
     dst[x] = make_uint4(pack_bf16x2_rn(acc[8 * x] * inv, acc[8 * x + 1] * inv),
                         pack_bf16x2_rn(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
                         pack_bf16x2_rn(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
@@ -415,7 +422,7 @@ lg_status lg_longnet_attn_fwd(const void* q, const void* k, const void* v, void*
   mp.out = static_cast<__nv_bfloat16*>(out);
   mp.lse = lse;
   const long long rows = static_cast<long long>(BH) * N;
-  const unsigned blocks = static_cast<unsigned>((rows * (D / 64) + 255) / 256);
+  const unsigned blocks = static_cast<unsigned>((rows * (D / kMixCols) + 255) / 256);
   if (launch_kernel(D == 64 ? longnet_mix_kernel<64> : longnet_mix_kernel<128>, dim3(blocks), dim3(256), 0, stream, true,
                     mp) != cudaSuccess)
     return LG_ERR_CUDA;
