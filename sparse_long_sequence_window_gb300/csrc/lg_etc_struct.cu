@@ -146,8 +146,22 @@ __global__ void __launch_bounds__(256) es_pack_kernel(const EsPackParams p) {
     }
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     bool bad = false;
-    if (piece != 0) {
-      const uint8_t* src = piece == 1 ? p.l2l : piece == 2 ? p.l2g : piece == 3 ? p.g2l : p.g2g;
+    const uint8_t* src = piece == 1 ? p.l2l : piece == 2 ? p.l2g : piece == 3 ? p.g2l : p.g2g;
+    const int kj0 = key0 + 16 * k;
+    // A whole chunk of a g2g, l2g or g2l row whose bytes are 16-byte aligned: one load.
+    const size_t vcols = piece == 2 ? g.G : (piece == 3 ? g.L : g.G);
+    const size_t vrows = piece == 2 ? g.L : g.G;
+    const bool vec = piece >= 2 && src != nullptr && kj0 + 16 <= key_n && vcols % 16 == 0 &&
+                     (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    if (vec) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + (static_cast<size_t>(b) * vrows + qi) * vcols + kj0);
+      w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+      if (p.n_labels > 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (static_cast<int>((w[e >> 2] >> (8 * (e & 3))) & 127u) >= p.n_labels) bad = true;
+      }
+    } else if (piece != 0) {
       for (int e = 0; e < 16; ++e) {
         const int kj = key0 + 16 * k + e;
         if (kj >= key_n) continue;

@@ -80,6 +80,8 @@ CASES = [
     (E("64 labels", 1, 2, 333, 9, 64, 20), 64, 0.25),
     (E("40 labels D128 two global tiles", 1, 2, 260, 140, 128, 9), 40, 0.25),
     (E("single token", 1, 1, 1, 1, 64, 3), 2, 0.0),
+    # rows of l2g, g2l and g2g codes that are multiples of 16 bytes (packed 16 at a time)
+    (E("16-byte code rows", 2, 2, 512, 32, 64, 20), 8, 0.2),
 ]
 
 
@@ -126,20 +128,25 @@ def test_etc_struct_base_full_size_sampled(cuda_lib):
     run_case(cuda_lib, w, codes, st["rel_k"], rows=rows)
 
 
-def test_etc_struct_bad_label_is_reported(cuda_lib):
+# The packing kernel reads a code row byte by byte, or 16 bytes at once where the row's
+# length is a multiple of 16 (G = 32 here): a label past the vocabulary is reported on
+# either path.
+@pytest.mark.parametrize("L,G,name,at", [(200, 4, "code_l2g", (0, 17, 2)), (256, 32, "code_l2g", (0, 17, 18)),
+                                          (256, 32, "code_g2l", (0, 3, 40))])
+def test_etc_struct_bad_label_is_reported(cuda_lib, L, G, name, at):
     lg = cuda_lib
-    w = E("bad label", 1, 2, 200, 4, 64, 8)
+    w = E("bad label", 1, 2, L, G, 64, 8)
     codes = random_codes(w, 4, 0.1, 9)
-    codes["code_l2g"][0, 17, 2] = 4 | 128     # label 4 with a vocabulary of 4
+    codes[name][at] = 4 | 128     # label 4 with a vocabulary of 4
     inp = workloads.make_inputs(w)
     t = {n: inp[n].cuda() for n in ("q", "k", "v", "q_g", "k_g", "v_g")}
     cd = {n: torch.from_numpy(c).cuda() for n, c in codes.items()}
     rel = rel_for(w, 4, 10).cuda()
-    ws = torch.empty(lg.etc_struct_attn_fwd_workspace_size(1, 2, 200, 4, 64, 8, 4), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(lg.etc_struct_attn_fwd_workspace_size(1, 2, L, G, 64, 8, 4), dtype=torch.uint8, device="cuda")
     lg.etc_struct_attn_fwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], w.radius, rel, **cd, workspace=ws)
     assert lg.query_status(ws) == lg.LG_ERR_INVALID_ARG
-    codes["code_l2g"][0, 17, 2] = 3
-    cd["code_l2g"] = torch.from_numpy(codes["code_l2g"]).cuda()
+    codes[name][at] = 3
+    cd[name] = torch.from_numpy(codes[name]).cuda()
     lg.etc_struct_attn_fwd(t["q"], t["k"], t["v"], t["q_g"], t["k_g"], t["v_g"], w.radius, rel, **cd, workspace=ws)
     assert lg.query_status(ws) == 0
 
